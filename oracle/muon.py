@@ -1,0 +1,213 @@
+"""fp64 CPU oracle of the Muon half of the hybrid step.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this file; it
+exists so that tests, the smoke check and the CPU baseline can compare the
+CUDA library against a plain, slow, obviously correct statement of the method.
+
+Every function is written from the method's own description, step by step,
+in float64 NumPy. Matrix products use ``@`` (a library primitive) and nothing
+is fused or reordered beyond what the description states.
+
+Sources (page title, section):
+  [SPD]  Speedtronic docs, "v2 optimizers": "Newton-Schulz", "Muon update",
+         "Muon+", "Cautious updates".
+  [FLX]  flaxchat, "Optimizer": "Muon Algorithm" steps 1-4.
+  [KIMI] kimi-k3, "Optimization": "A tensor's storage shape can be misleading"
+         (matrix views) and "Why treat a matrix differently?".
+
+Readings taken where the pages are silent or ambiguous (each also listed in
+the design notes):
+  * Frobenius normalisation is X = T / (||T||_F + eps) with eps = 1e-7 [SPD].
+  * "tall" means rows > cols strictly; a square matrix is not transposed.
+  * The shape scale uses the stored view's rows/cols: max(1, rows/cols)**0.5.
+  * NorMuon [FLX step 3]: statistics per row of the stored view (mean over
+    columns); state zero-initialised, no bias correction; the per-row factor
+    is rsqrt(max(sm, 1e-10)) and "normalize" restores the Frobenius norm the
+    update had before the per-row rescale (guarded by 1e-10).
+  * Muon+ row_col [SPD]: rows to unit L2 norm, then columns, each with eps
+    inside the square root; eps defaults to the NS eps (1e-7).
+  * Order when several are on: NS -> NorMuon -> Muon+ -> apply.
+  * Cautious mode 1 [FLX step 4]: the mask gates weight decay only and keeps
+    entries where update * param >= 0. Cautious mode 2 [SPD]: the mask gates
+    the whole observed update (decay included) and keeps entries where
+    update * gradient > 0.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# [SPD "Newton-Schulz"]: quintic coefficients, five steps, eps.
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+NS_STEPS = 5
+NS_EPS = 1e-7
+NORMUON_FLOOR = 1e-10
+
+CAUTIOUS_OFF = 0
+CAUTIOUS_WD = 1       # [FLX step 4]
+CAUTIOUS_UPDATE = 2   # [SPD "Cautious updates"]
+
+
+@dataclass
+class MuonHparams:
+    lr: float = 0.02
+    momentum: float = 0.95
+    nesterov: bool = True
+    eps: float = NS_EPS
+    ns_steps: int = NS_STEPS
+    coeffs: tuple = NS_COEFFS
+    normuon: bool = False
+    beta2: float = 0.95
+    muon_plus: bool = False
+    plus_eps: float = NS_EPS
+    cautious: int = CAUTIOUS_OFF
+
+
+def momentum_nesterov(B: np.ndarray, G: np.ndarray, mu: float, nesterov: bool = True):
+    """[SPD "Muon update"], [FLX step 1].
+
+    B <- mu*B + (1-mu)*G, then the Nesterov form Q = lerp(G, B, mu) =
+    G + mu*(B - G). Without Nesterov the update direction is B itself.
+    Returns (B_new, Q).
+    """
+    B_new = mu * B + (1.0 - mu) * G
+    if nesterov:
+        Q = G + mu * (B_new - G)
+    else:
+        Q = B_new.copy()
+    return B_new, Q
+
+
+def newton_schulz(Q: np.ndarray, steps: int = NS_STEPS, coeffs=NS_COEFFS,
+                  eps: float = NS_EPS) -> np.ndarray:
+    """[SPD "Newton-Schulz"]: quintic iteration on one matrix.
+
+    A tall matrix (rows > cols) is transposed, normalised, iterated and
+    transposed back. Each step forms A = X X^T and X <- a X + (b A + c A^2) X.
+    A zero matrix stays zero (eps keeps the division finite).
+    """
+    a, b, c = coeffs
+    Q = np.asarray(Q, dtype=np.float64)
+    tall = Q.shape[0] > Q.shape[1]
+    T = Q.T if tall else Q
+    X = T / (np.sqrt(np.sum(T * T)) + eps)
+    for _ in range(steps):
+        A = X @ X.T
+        P = b * A + c * (A @ A)
+        X = a * X + P @ X
+    return X.T.copy() if tall else X
+
+
+def normuon(U: np.ndarray, sm: np.ndarray, beta2: float):
+    """[FLX step 3] NorMuon per-row second moment (reading: rows of the stored view).
+
+    v_i = mean_j U_ij^2; sm <- lerp(sm, v, 1 - beta2); each row is scaled by
+    rsqrt(max(sm_i, 1e-10)); then the whole matrix is rescaled so that its
+    Frobenius norm equals the norm U had before the per-row scaling.
+    Returns (U_new, sm_new).
+    """
+    v = np.mean(U * U, axis=1)
+    sm_new = sm + (1.0 - beta2) * (v - sm)
+    row_scale = 1.0 / np.sqrt(np.maximum(sm_new, NORMUON_FLOOR))
+    U1 = U * row_scale[:, None]
+    norm_before = np.sqrt(np.sum(U * U))
+    norm_after = np.sqrt(np.sum(U1 * U1))
+    kappa = norm_before / max(norm_after, NORMUON_FLOOR)
+    return kappa * U1, sm_new
+
+
+def muon_plus_row_col(U: np.ndarray, eps: float = NS_EPS) -> np.ndarray:
+    """[SPD "Muon+"] row_col mode: normalise rows, then columns, eps inside each sqrt."""
+    R = U / np.sqrt(np.sum(U * U, axis=1) + eps)[:, None]
+    return R / np.sqrt(np.sum(R * R, axis=0) + eps)[None, :]
+
+
+def shape_scale(rows: int, cols: int) -> float:
+    """[SPD "Muon update"]: max(1, rows/cols)^0.5 of the stored view."""
+    return max(1.0, rows / cols) ** 0.5
+
+
+def muon_apply(W: np.ndarray, U: np.ndarray, G: np.ndarray, lr: float, wd: float,
+               cautious: int = CAUTIOUS_OFF) -> np.ndarray:
+    """Parameter update of one view, fp64.
+
+    Plain [SPD]: W <- (1 - lr*wd) W - lr * s * U, s = max(1, rows/cols)^0.5.
+    Cautious mode 1 [FLX step 4], with g = s*U the update direction:
+        mask = (g * W >= 0);  W <- W - lr * (g + wd * W * mask).
+    Cautious mode 2 [SPD "Cautious updates"], the observed update of the plain
+    rule being delta = lr*wd*W + lr*s*U:
+        mask = (delta * G > 0);  W <- W - mask * delta.
+    """
+    s = shape_scale(W.shape[0], W.shape[1])
+    if cautious == CAUTIOUS_OFF:
+        return (1.0 - lr * wd) * W - lr * s * U
+    if cautious == CAUTIOUS_WD:
+        g = s * U
+        mask = (g * W >= 0).astype(np.float64)
+        return W - lr * (g + wd * W * mask)
+    if cautious == CAUTIOUS_UPDATE:
+        delta = lr * wd * W + lr * s * U
+        mask = (delta * G > 0).astype(np.float64)
+        return W - mask * delta
+    raise ValueError(f"unknown cautious mode {cautious}")
+
+
+@dataclass
+class ViewResult:
+    W: np.ndarray
+    B: np.ndarray
+    U: np.ndarray
+    sm: np.ndarray | None = None
+
+
+def muon_step_view(W, G, B, hp: MuonHparams, lr_mult: float = 1.0, wd: float = 0.0,
+                   sm=None) -> ViewResult:
+    """One Muon update of one r x c view, in the pages' order:
+    momentum + Nesterov -> Newton-Schulz -> [NorMuon] -> [Muon+] -> apply.
+    """
+    W = np.asarray(W, dtype=np.float64)
+    G = np.asarray(G, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    B_new, Q = momentum_nesterov(B, G, hp.momentum, hp.nesterov)
+    U = newton_schulz(Q, hp.ns_steps, hp.coeffs, hp.eps)
+    sm_new = None
+    if hp.normuon:
+        U, sm_new = normuon(U, np.zeros(W.shape[0]) if sm is None else np.asarray(sm, np.float64),
+                            hp.beta2)
+    if hp.muon_plus:
+        U = muon_plus_row_col(U, hp.plus_eps)
+    lr = hp.lr * lr_mult
+    W_new = muon_apply(W, U, G, lr, wd, hp.cautious)
+    return ViewResult(W=W_new, B=B_new, U=U, sm=sm_new)
+
+
+def muon_step_tensor(W, G, B, hp: MuonHparams, views: int = 1, lr_mult: float = 1.0,
+                     wd: float = 0.0, sm=None):
+    """[KIMI "storage shape"]: a packed tensor declared as (views, r, c) is
+    ``views`` independent r x c matrices sharing one momentum buffer.
+
+    W, G, B are arrays of total size views*r*c (any shape); they are viewed
+    as (views, r, c). Returns (W_new, B_new, U, sm_new) shaped like the input
+    (U and sm as (views, r, c) and (views, r)).
+    """
+    W = np.asarray(W, dtype=np.float64)
+    shape = W.shape
+    r, c = shape[-2], shape[-1]
+    if views > 1 and W.ndim == 2:
+        r = shape[0] // views
+    Wv = W.reshape(views, r, c)
+    Gv = np.asarray(G, dtype=np.float64).reshape(views, r, c)
+    Bv = np.asarray(B, dtype=np.float64).reshape(views, r, c)
+    smv = None if sm is None else np.asarray(sm, dtype=np.float64).reshape(views, r)
+    Wn = np.empty_like(Wv)
+    Bn = np.empty_like(Bv)
+    Un = np.empty_like(Wv)
+    smn = np.empty((views, r)) if hp.normuon else None
+    for k in range(views):
+        res = muon_step_view(Wv[k], Gv[k], Bv[k], hp, lr_mult, wd,
+                             None if smv is None else smv[k])
+        Wn[k], Bn[k], Un[k] = res.W, res.B, res.U
+        if hp.normuon:
+            smn[k] = res.sm
+    return Wn.reshape(shape), Bn.reshape(shape), Un, smn
