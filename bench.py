@@ -1,0 +1,582 @@
+#!/usr/bin/env python3
+"""Benchmark of the hybrid Muon + AdamW optimizer step on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama7b|gpt124m|moe_mla|single|adamw_2p30]
+
+A step is the whole hot path on one synthetic batch of gradients: the
+batched Muon update of every routed matrix and view (momentum/Nesterov/norm
+prologue, five quintic Newton-Schulz iterations as grouped tcgen05 GEMMs,
+apply epilogue) followed by the fused AdamW step of the embedding, head and
+norms. The default workload is the 7B-shape parameter set (d=4096, 32 layers,
+GQA; 224 Muon views, 6.98 G Muon elements, 1.05 G AdamW elements), with all
+inputs resident in HBM.
+
+The JSON line reports the step time (value, ms/step, lower is better), the
+Newton-Schulz throughput, a live roofline of the dominant kernel from CUDA
+events recorded by the library on its launch stream, the end-to-end time with
+host buffers (gradients copied in from pinned memory and updated parameters
+copied back every step), the SM clocks sampled during the timed region, and
+the fp64 CPU oracle timed on a bounded sample of the same workload.
+
+Under torchrun with N > 1 every rank runs an independent replica of the
+workload (the step has no exchange between GPUs); the time is the maximum
+over ranks.
+
+--impl reference times the oracle (the plain fp64 CPU statement of the
+method) on the host cores instead, each step a bounded sample of the same
+workload extrapolated to the full step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon+AdamW step ms at 7B-shape; Newton–Schulz TFLOP/s vs bf16 TC peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama7b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---- clocks ----------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        smax = max(num(r[2]) for r in rows)
+        power = [num(r[3]) for r in rows]
+        pmax = max(p for p in power if not math.isnan(p)) if any(not math.isnan(p) for p in power) else 0
+        loaded = [i for i, p in enumerate(power) if p >= 0.5 * pmax] or list(range(len(rows)))
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = []
+        for k, nm in enumerate(names):
+            if any(rows[i][5 + k].lower() == "active" for i in loaded):
+                reasons.append(nm)
+        return {"sm_mhz": statistics.median(sm[i] for i in loaded), "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": pmax}
+
+
+# ---- distributed plumbing ------------------------------------------------------------
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- workload on the device -------------------------------------------------------------
+
+class DeviceWorkload:
+    def __init__(self, wl, device):
+        import numpy as np
+        import torch
+        import muon_adamw_hybrid_gb300 as mh
+        from synth import workloads as W
+        self.wl, self.mh, self.torch = wl, mh, torch
+        hp = wl.muon_hp
+        self.hp = mh.make_hparams(lr=hp["lr"], momentum=hp["momentum"], nesterov=hp["nesterov"],
+                                  eps=hp["eps"], ns_steps=hp["ns_steps"], coeffs=hp["coeffs"],
+                                  normuon=hp.get("normuon", False), beta2=hp.get("beta2", 0.95),
+                                  muon_plus=hp.get("muon_plus", False),
+                                  plus_eps=hp.get("plus_eps", hp["eps"]),
+                                  cautious=hp.get("cautious", 0))
+        self.mW = [W.device_tensor(wl, W.KIND_W, i, device=device) for i in range(len(wl.muon))]
+        self.mG = [W.device_tensor(wl, W.KIND_G, i, 0, device=device) for i in range(len(wl.muon))]
+        self.mB = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.muon]
+        self.sm = [torch.zeros(s.views * s.rows, dtype=torch.float32, device=device)
+                   if self.hp.normuon else None for s in wl.muon]
+        self.aW = [W.device_tensor(wl, W.KIND_AW, j, device=device) for j in range(len(wl.adamw))]
+        self.aG = [W.device_tensor(wl, W.KIND_AG, j, 0, device=device) for j in range(len(wl.adamw))]
+        self.am = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.adamw]
+        self.av = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.adamw]
+        self.ts = [mh.muon_tensor(w, g, b, s.views, sm, s.lr_mult, s.wd)
+                   for w, g, b, sm, s in zip(self.mW, self.mG, self.mB, self.sm, wl.muon)]
+        self.at = [mh.adamw_tensor(w, g, m, v, s.lr_mult, s.wd)
+                   for w, g, m, v, s in zip(self.aW, self.aG, self.am, self.av, wl.adamw)]
+        need = mh.muon_workspace_bytes(self.ts, self.hp) if self.ts else 0
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.step_count = 0
+        self.resident_bytes = sum(t.numel() * t.element_size() for t in
+                                  self.mW + self.mG + self.mB + self.aW + self.aG + self.am + self.av)
+        self.resident_bytes += self.ws.numel()
+
+    def step(self, stream) -> None:
+        s = stream.cuda_stream
+        self.step_count += 1
+        if self.ts:
+            self.mh.muon_step_batched(self.ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
+        if self.at:
+            hp = self.wl.adam_hp
+            self.mh.adamw_step(self.at, hp["lr"], hp["betas"][0], hp["betas"][1], hp["eps"],
+                               self.step_count, s)
+
+    def check_status(self, stream) -> None:
+        if self.ts:
+            self.mh.workspace_status(self.ws.data_ptr(), stream.cuda_stream)
+
+
+def ns_flops(wl) -> float:
+    steps = wl.muon_hp["ns_steps"]
+    tot = 0.0
+    for s in wl.muon:
+        m, n = min(s.rows, s.cols), max(s.rows, s.cols)
+        tot += s.views * steps * (4.0 * m * m * n + 2.0 * m ** 3)
+    return tot
+
+
+# ---- host buffers for the end-to-end measurement -------------------------------------
+
+class PinnedMirror:
+    """One page-locked host buffer mirroring a list of device tensors."""
+
+    def __init__(self, tensors):
+        import numpy as np
+        import torch
+        self.tensors = tensors
+        self.nbytes = sum(t.numel() * t.element_size() for t in tensors)
+        self.buf = np.empty(max(self.nbytes, 1), dtype=np.uint8)
+        err = torch.cuda.cudart().cudaHostRegister(self.buf.ctypes.data, self.buf.nbytes, 0)
+        try:
+            self.registered = int(getattr(err, "value", err)) == 0
+        except (TypeError, ValueError):
+            self.registered = False
+        self.host = []
+        off = 0
+        base = torch.from_numpy(self.buf)
+        for t in tensors:
+            nb = t.numel() * t.element_size()
+            self.host.append(base[off:off + nb].view(t.dtype).view(t.shape))
+            off += nb
+
+    def fill_from_device(self):
+        for h, t in zip(self.host, self.tensors):
+            h.copy_(t)
+
+    def h2d(self):
+        for h, t in zip(self.host, self.tensors):
+            t.copy_(h, non_blocking=True)
+
+    def d2h(self):
+        for h, t in zip(self.host, self.tensors):
+            h.copy_(t, non_blocking=True)
+
+    def close(self):
+        import torch
+        if self.registered:
+            torch.cuda.cudart().cudaHostUnregister(self.buf.ctypes.data)
+
+
+# ---- oracle (CPU baseline / reference arm) ------------------------------------------------
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_sample_plan(wl, muon_flop_budget: float, adam_elems: int):
+    """Whole Muon views taken in workload order, skipping any view that would
+    overshoot the NS-FLOP budget, until the budget is half used or more; and
+    the first ``adam_elems`` AdamW elements."""
+    steps = wl.muon_hp["ns_steps"]
+    cands = []
+    for i, s in enumerate(wl.muon):
+        m, n = min(s.rows, s.cols), max(s.rows, s.cols)
+        f = steps * (4.0 * m * m * n + 2.0 * m ** 3)
+        for v in range(s.views):
+            cands.append((i, v, f))
+    views, got = [], 0.0
+    for c in cands:
+        if got >= 0.5 * muon_flop_budget:
+            break
+        if got + c[2] <= muon_flop_budget:
+            views.append(c)
+            got += c[2]
+    if not views and cands:
+        views.append(min(cands, key=lambda c: c[2]))
+    adam = []
+    left = adam_elems
+    for j, s in enumerate(wl.adamw):
+        if left <= 0:
+            break
+        take = min(left, s.numel)
+        adam.append((j, take))
+        left -= take
+    return views, adam
+
+
+class OracleSample:
+    """Inputs of a bounded sample, generated once; ``run()`` times the fp64
+    oracle on them and returns (muon seconds, adamw seconds)."""
+
+    def __init__(self, wl, views, adam):
+        import numpy as np
+        import oracle
+        from synth import workloads as W
+        self.wl, self.views, self.adam = wl, views, adam
+        hp = wl.muon_hp
+        self.hp = oracle.MuonHparams(
+            lr=hp["lr"], momentum=hp["momentum"], nesterov=hp["nesterov"], eps=hp["eps"],
+            ns_steps=hp["ns_steps"], coeffs=tuple(hp["coeffs"]),
+            normuon=hp.get("normuon", False), beta2=hp.get("beta2", 0.95),
+            muon_plus=hp.get("muon_plus", False), plus_eps=hp.get("plus_eps", hp["eps"]),
+            cautious=hp.get("cautious", 0))
+        self.inputs = []
+        for i, v, _ in views:
+            s = wl.muon[i]
+            off, cnt = v * s.rows * s.cols, s.rows * s.cols
+            Wv = W.host_tensor(wl, W.KIND_W, i, offset=off, count=cnt).reshape(s.rows, s.cols)
+            Gv = W.host_tensor(wl, W.KIND_G, i, offset=off, count=cnt).reshape(s.rows, s.cols)
+            self.inputs.append((Wv, Gv, np.zeros_like(Wv), s))
+        self.ainputs = [(W.host_tensor(wl, W.KIND_AW, j, count=cnt),
+                         W.host_tensor(wl, W.KIND_AG, j, count=cnt), wl.adamw[j])
+                        for j, cnt in adam]
+
+    def run(self):
+        import numpy as np
+        import oracle
+        t0 = time.perf_counter()
+        for Wv, Gv, Bv, s in self.inputs:
+            res = oracle.muon_step_view(Wv, Gv, Bv, self.hp, s.lr_mult, s.wd,
+                                        np.zeros(s.rows) if self.hp.normuon else None)
+            if s.param_dtype == "bf16":
+                oracle.round_bf16(res.W)
+        t1 = time.perf_counter()
+        ahp = self.wl.adam_hp
+        for Wa, Ga, s in self.ainputs:
+            n = Wa.size
+            Wn, _, _ = oracle.adamw_step(Wa, Ga, np.zeros(n), np.zeros(n), ahp["lr"] * s.lr_mult,
+                                         ahp["betas"][0], ahp["betas"][1], ahp["eps"], s.wd, 1)
+            if s.param_dtype == "bf16":
+                oracle.round_bf16(Wn)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+
+def oracle_extrapolated_ms(wl, views, adam, muon_s, adam_s):
+    """Full-step ms: Muon time scaled by NS FLOPs, AdamW time by elements."""
+    ms = 0.0
+    sample_flops = sum(f for _, _, f in views)
+    if sample_flops > 0:
+        ms += 1e3 * muon_s * ns_flops(wl) / sample_flops
+    sample_adam = sum(c for _, c in adam)
+    if sample_adam > 0:
+        ms += 1e3 * adam_s * wl.adam_elems / sample_adam
+    return ms
+
+
+def sample_desc(wl, views, adam):
+    parts = []
+    for i, v, _ in views:
+        s = wl.muon[i]
+        parts.append(f"{s.name}[view {v}] {s.rows}x{s.cols}")
+    for j, c in adam:
+        parts.append(f"AdamW {wl.adamw[j].name}[:{c}]")
+    return ("fp64 oracle on " + ", ".join(parts) +
+            "; Muon time scaled to the full step by nominal NS FLOPs, AdamW time by elements")
+
+
+# ---- main ---------------------------------------------------------------------------------
+
+def run_reference(args, wl):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    # One bounded sample per step: about a second of CPU work.
+    views, adam = oracle_sample_plan(wl, muon_flop_budget=2.0e11, adam_elems=1 << 22)
+    sample = OracleSample(wl, views, adam)
+    for _ in range(args.warmup):
+        sample.run()
+    per = []
+    for _ in range(args.steps):
+        ms_muon, ms_adam = sample.run()
+        per.append(oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam))
+    ms = statistics.mean(per)
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms/step",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(wl, world),
+        "cpu_baseline": {"value": round(ms, 3), "unit": "ms/step", "cores": cores,
+                         "kind": "oracle", "sample": sample_desc(wl, views, adam)},
+        "e2e": {"value": round(ms, 3), "unit": "ms/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(wl, world):
+    return {"workload": wl.name,
+            "muon_tensors": len(wl.muon), "muon_views": sum(s.views for s in wl.muon),
+            "muon_elems": wl.muon_elems, "adamw_tensors": len(wl.adamw),
+            "adamw_elems": wl.adam_elems, "ns_steps": wl.muon_hp["ns_steps"],
+            "variants": {k: wl.muon_hp.get(k) for k in ("normuon", "muon_plus", "cautious")
+                         if wl.muon_hp.get(k)},
+            "precision": "bf16 tensor-core NS operands, fp32 accumulate; fp32 elementwise math "
+                         "and optimizer state; bf16 params/grads",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
+def main():
+    args = parse_args()
+    from synth import workloads as W
+    if args.workload not in W.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(W.WORKLOADS)}")
+    wl = W.WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+
+    world, rank, local = dist_setup(args)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = load_peaks()
+
+    dw = DeviceWorkload(wl, device)
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 0)):
+        dw.step(stream)
+    torch.cuda.synchronize()
+    dw.check_status(stream)
+
+    # ---- timed region: K device-resident steps --------------------------------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    mh.profiler_reset()
+    mh.profiler_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        dw.step(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    mh.profiler_enable(False)
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_step = max_over_ranks(ms_total / args.steps, world)
+    kstats = mh.profiler_read()
+    dw.check_status(stream)
+    launches = sum(v["launches"] for v in kstats.values())
+
+    # ---- roofline of the dominant kernel and of the top HBM-bound kernel -------------
+    kernels = {}
+    for name, v in sorted(kstats.items(), key=lambda kv: -kv[1]["total_ms"]):
+        avg = v["total_ms"] / max(v["launches"], 1)
+        kernels[name] = {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
+                         "avg_ms": round(avg, 4),
+                         "share": round(v["total_ms"] / max(sum(x["total_ms"] for x in kstats.values()), 1e-9), 4)}
+        if v["flops"] > 0:
+            kernels[name]["tflops_nominal"] = round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1)
+            kernels[name]["tflops_executed"] = round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)
+        if v["bytes"] > 0:
+            kernels[name]["gbs"] = round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1)
+    roofline = None
+    if kstats:
+        top = max(kstats, key=lambda k: kstats[k]["total_ms"])
+        v = kstats[top]
+        if v["flops"] > 0:
+            peak = peaks["bf16_tflops_sustained"]
+            ach = v["flops"] / (v["total_ms"] * 1e-3) / 1e12
+            roofline = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "peak_source": f"bf16 sustained, of {peak_src}",
+                        "achieved_basis": "nominal NS FLOPs (2m^2n gram, 2m^3 poly, 2m^2n apply "
+                                          "per view) / event time",
+                        "executed_tflops": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)}
+        else:
+            peak = peaks["hbm_gbs"]
+            ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
+            roofline = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                        "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "peak_source": f"HBM copy, of {peak_src}"}
+    hbm = {k: v for k, v in kstats.items() if v["flops"] == 0 and v["bytes"] > 0}
+    roofline_hbm = None
+    if hbm:
+        top = max(hbm, key=lambda k: hbm[k]["total_ms"])
+        v = hbm[top]
+        ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
+        roofline_hbm = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1),
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                        "peak_source": f"HBM copy, of {peak_src}"}
+    nsf = ns_flops(wl)
+    ns_ms = kstats.get("ns_gemm", {}).get("total_ms", 0.0) / max(args.steps, 1)
+
+    # ---- end to end with host buffers --------------------------------------------------
+    e2e = None
+    if not args.no_e2e:
+        grads = dw.mG + dw.aG
+        params = dw.mW + dw.aW
+        gin = PinnedMirror(grads)
+        pout = PinnedMirror(params)
+        gin.fill_from_device()
+        torch.cuda.synchronize()
+        for _ in range(1):
+            gin.h2d(); dw.step(stream); pout.d2h()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            gin.h2d()
+            dw.step(stream)
+            pout.d2h()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        e2e = {"value": round(e2e_ms, 3), "unit": "ms/step", "h2d_bytes_per_step": gin.nbytes,
+               "d2h_bytes_per_step": pout.nbytes,
+               "path": "C ABI calls with gradients copied in from pinned host memory and "
+                       "updated parameters copied back each step",
+               "pinned": bool(gin.registered and pout.registered)}
+        gin.close()
+        pout.close()
+
+    # ---- CPU oracle baseline (rank 0, one GPU) -------------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        views, adam = oracle_sample_plan(wl, muon_flop_budget=4.0e12, adam_elems=1 << 24)
+        ms_muon, ms_adam = OracleSample(wl, views, adam).run()
+        cpu_ms = oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam)
+        cpu = {"value": round(cpu_ms, 1), "unit": "ms/step", "cores": blas_threads(),
+               "kind": "oracle", "sample": sample_desc(wl, views, adam),
+               "sample_seconds": round(ms_muon + ms_adam, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(ms_step, 3), "unit": "ms/step", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(wl, world),
+            "ns_tflops": round(nsf / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
+            "ns_ms_per_step": round(ns_ms, 3),
+            "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "resident_gb": round(dw.resident_bytes / 1e9, 1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

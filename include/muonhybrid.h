@@ -1,0 +1,203 @@
+/*
+ * muonhybrid.h -- C ABI of the GB300 (sm_103a) hybrid Muon + AdamW optimizer step.
+ *
+ * What it computes (sources are the pages' titles and sections):
+ *
+ *   Muon, for every routed 2-D matrix and every declared matrix view
+ *   (Speedtronic docs "v2 optimizers", sections "Newton-Schulz", "Muon update",
+ *   "Muon+", "Cautious updates"; flaxchat "Optimizer", "Muon Algorithm";
+ *   kimi-k3 "Optimization", "A tensor's storage shape can be misleading"):
+ *
+ *       B <- mu*B + (1-mu)*G                       momentum, fp32 state
+ *       Q <- lerp(G, B, mu) = G + mu*(B - G)        Nesterov form (else Q = B)
+ *       X <- T / (||T||_F + eps),  T = Q^T if rows > cols else Q
+ *       repeat ns_steps:  A = X X^T;  X <- a X + (b A + c A^2) X
+ *       U <- X^T if rows > cols else X
+ *       [NorMuon per-row second moment]  [Muon+ row_col]
+ *       W <- (1 - lr*wd) W - lr * max(1, rows/cols)^0.5 * U   (or a cautious form)
+ *
+ *   AdamW for everything else (dew.training.optim "OPTIMIZER_MAP" names
+ *   optax.adamw; Speedtronic "CPU/CUDA/MPS behavior" names PyTorch's fused
+ *   AdamW): standard decoupled AdamW with bias correction.
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers to tensors are DEVICE pointers into memory the caller owns
+ *     (parameters, gradients, optimizer state, workspace). The library never
+ *     allocates device memory in these calls and keeps no pointer after the
+ *     call returns.
+ *   - Tensors are contiguous and row-major. A Muon tensor with views = k is
+ *     k independent rows x cols matrices stored back to back, i.e. the array
+ *     (k*rows, cols); its momentum buffer has the same layout.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued on it; nothing synchronises the host.
+ *   - Arguments are checked on the host before anything is enqueued. A failed
+ *     check returns a non-zero mh_status, enqueues nothing, and leaves a
+ *     message for mh_last_error(). A CUDA launch error returns MH_ECUDA.
+ *   - Supported dtypes are fp32 and bf16. Anything else (complex, sparse
+ *     layouts, fp16, fp64) is rejected with MH_EDTYPE; the pages require a
+ *     clear error for sparse and complex gradients.
+ *   - Calls are thread-safe as long as concurrent calls use distinct
+ *     workspaces; the error message is per host thread.
+ */
+#ifndef MUONHYBRID_H
+#define MUONHYBRID_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MH_OK = 0,
+  MH_EINVAL = 1,       /* null pointer, bad count, bad hyperparameter */
+  MH_EDTYPE = 2,       /* unsupported dtype (complex/sparse/fp16/fp64...) */
+  MH_ESHAPE = 3,       /* non-positive or too large dimension */
+  MH_EWORKSPACE = 4,   /* workspace null, too small or misaligned */
+  MH_ECUDA = 5,        /* a CUDA runtime call or launch failed */
+  MH_EUNSUPPORTED = 6, /* valid request this build does not handle */
+  MH_ETIMEOUT = 7      /* a device-side bounded wait gave up (see mh_workspace_status) */
+} mh_status;
+
+typedef enum { MH_F32 = 0, MH_BF16 = 1 } mh_dtype;
+
+/* Cautious variants (both from the pages; 0 = off).
+ *   MH_CAUTIOUS_WD     flaxchat "Muon Algorithm" step 4: the mask gates the
+ *                      weight decay only and keeps entries with
+ *                      update*param >= 0.
+ *   MH_CAUTIOUS_UPDATE Speedtronic "Cautious updates": the mask gates the
+ *                      whole observed update (decay included) and keeps
+ *                      entries with update*gradient > 0. */
+enum { MH_CAUTIOUS_OFF = 0, MH_CAUTIOUS_WD = 1, MH_CAUTIOUS_UPDATE = 2 };
+
+/* One Muon-routed parameter (a 2-D matrix or a stack of `views` matrices). */
+typedef struct {
+  void* param;            /* (views*rows, cols), param_dtype, updated in place */
+  const void* grad;       /* (views*rows, cols), grad_dtype, read only */
+  float* momentum;        /* (views*rows, cols) fp32, updated in place */
+  float* normuon_sm;      /* (views*rows) fp32 NorMuon second moment, updated in
+                             place; required when hparams.normuon != 0, else
+                             ignored (may be NULL). Zero-initialise it. */
+  int32_t param_dtype;    /* mh_dtype */
+  int32_t grad_dtype;     /* mh_dtype */
+  int64_t views;          /* >= 1: independent matrices in the tensor */
+  int64_t rows;           /* rows of one view (>= 1) */
+  int64_t cols;           /* cols of one view (>= 1) */
+  float lr_mult;          /* this tensor's lr = hparams.lr * lr_mult */
+  float wd;               /* this tensor's decoupled weight decay */
+} mh_muon_tensor;
+
+/* Muon hyperparameters shared by one call. Defaults from the pages:
+ * momentum 0.95 with Nesterov, ns_steps 5, (a,b,c) = (3.4445, -4.7750, 2.0315),
+ * eps 1e-7 (Speedtronic "Newton-Schulz"). */
+typedef struct {
+  float lr;
+  float momentum;     /* mu in [0, 1) */
+  int32_t nesterov;   /* 1: Q = lerp(G, B, mu); 0: Q = B */
+  float eps;          /* Frobenius-normalisation guard, > 0 */
+  int32_t ns_steps;   /* 0..16 quintic iterations */
+  float a, b, c;      /* quintic coefficients */
+  int32_t normuon;    /* 1: NorMuon per-row second moment (flaxchat step 3) */
+  float beta2;        /* NorMuon EMA coefficient, in [0, 1) */
+  int32_t muon_plus;  /* 1: Muon+ row_col normalisation (Speedtronic "Muon+") */
+  float plus_eps;     /* Muon+ eps inside each square root, > 0 */
+  int32_t cautious;   /* MH_CAUTIOUS_* */
+} mh_muon_hparams;
+
+/* Bytes of device workspace mh_muon_step_batched needs for these tensors and
+ * flags (256-byte aligned pointer required). Returns 0 and sets the error
+ * message when the arguments are invalid. Host-only; touches no device. */
+size_t mh_muon_workspace_bytes(const mh_muon_tensor* tensors, int32_t n,
+                               const mh_muon_hparams* hp);
+
+/* The batched Muon update over all `n` tensors and all their views, in one
+ * stream-ordered sequence: a fused momentum/Nesterov/norm prologue, one
+ * grouped tcgen05 GEMM launch per Newton-Schulz stage over every view of
+ * every shape, and a fused NorMuon/Muon+/cautious/decay/apply epilogue.
+ * Views whose rows*cols is zero are skipped; n = 0 is a no-op.
+ * The workspace's previous contents do not matter. */
+int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon_hparams* hp,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* One Newton-Schulz problem: U = NS(X) for each of `views` rows x cols
+ * matrices (Speedtronic "Newton-Schulz": tall matrices are transposed
+ * internally, normalised by ||X||_F + eps, iterated, transposed back; a zero
+ * matrix stays zero). x and out may not overlap. */
+typedef struct {
+  const void* x;      /* (views*rows, cols) in in_dtype */
+  void* out;          /* (views*rows, cols) in out_dtype */
+  int32_t in_dtype;   /* mh_dtype */
+  int32_t out_dtype;  /* mh_dtype */
+  int64_t views, rows, cols;
+} mh_ns_problem;
+
+size_t mh_ns_workspace_bytes(const mh_ns_problem* problems, int32_t n);
+
+/* Batched Newton-Schulz only, with bf16 operands and fp32 accumulation. */
+int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t steps, float a,
+                             float b, float c, float eps, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* One AdamW-routed tensor, treated as a flat array of numel elements. */
+typedef struct {
+  void* param;            /* numel, param_dtype, updated in place */
+  const void* grad;       /* numel, grad_dtype */
+  float* exp_avg;         /* numel fp32 first moment, updated in place */
+  float* exp_avg_sq;      /* numel fp32 second moment, updated in place */
+  int32_t param_dtype;
+  int32_t grad_dtype;
+  int64_t numel;          /* >= 0 */
+  float lr_mult;
+  float wd;
+} mh_adamw_tensor;
+
+/* Fused multi-tensor AdamW step (step >= 1, the 1-based count used for bias
+ * correction):
+ *   m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2
+ *   W <- W (1 - lr*wd) - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
+ * in fp32, bf16 parameters rounded to nearest even on store. */
+int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1, float beta2,
+                  float eps, int64_t step, void* stream);
+
+/* Optional per-kernel timing. When enabled, every kernel the library launches
+ * is bracketed by two CUDA events recorded on its own stream, and the
+ * launch's algorithmic work is noted: bytes that must cross HBM at least
+ * once for the elementwise kernels, and the nominal dense FLOPs of the
+ * Newton-Schulz GEMM stages (2 m^2 n for X X^T and for P X, 2 m^3 for A A),
+ * plus the FLOPs the tensor cores actually execute (fewer, since only the
+ * upper triangle of the symmetric products is computed). Events are host
+ * objects created on first use; no device memory is allocated. Disabled by
+ * default; when disabled the calls above record nothing. */
+typedef struct {
+  char name[32];          /* kernel family, e.g. "ns_gemm", "muon_prologue" */
+  int64_t launches;       /* launches recorded since the last reset */
+  double total_ms;        /* summed event time of those launches */
+  double bytes;           /* summed algorithmic HBM bytes */
+  double flops;           /* summed nominal FLOPs (GEMM stages) */
+  double flops_executed;  /* summed tensor-core FLOPs actually issued */
+} mh_kernel_stats;
+
+int mh_profiler_enable(int32_t enable);
+/* Drops every recorded launch. */
+int mh_profiler_reset(void);
+/* Waits for the recorded events and aggregates them per kernel family into
+ * `out` (capacity `max`); `*count` receives the number of families. */
+int mh_profiler_read(mh_kernel_stats* out, int32_t max, int32_t* count);
+
+/* Reads the device status word the last Muon or Newton-Schulz call left in
+ * `workspace`, synchronising `stream`. MH_OK, or MH_ETIMEOUT when a kernel's
+ * bounded wait gave up (its outputs are then undefined). */
+int mh_workspace_status(const void* workspace, void* stream);
+
+/* Message for the last non-OK status on this host thread ("" if none). */
+const char* mh_last_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* mh_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUONHYBRID_H */

@@ -1,0 +1,483 @@
+// Elementwise passes of the Muon update, all HBM-bound and tiled over the
+// stored (rows x cols) layout of each view in 32 x 128 tiles:
+//
+//   EW_PROLOGUE  B <- mu B + (1-mu) G;  Q = lerp(G, B, mu) (or B);
+//                writes B (fp32), bf16(Q) into the Newton-Schulz buffer in NS
+//                orientation (transposed through shared memory for tall
+//                views), and accumulates ||Q||_F^2 per view from fp32 Q.
+//                Speedtronic "v2 optimizers", "Muon update" / "Newton-Schulz";
+//                flaxchat "Optimizer", "Muon Algorithm" step 1.
+//   EW_ROWSQ     per stored row and column tile: sum_j U_ij^2 (NorMuon
+//                statistics, Muon+ rows), as partials summed later in order.
+//   EW_COLSQ     per stored col and row tile: sum_i (f_i U_ij)^2 (Muon+
+//                columns), likewise.
+//   EW_APPLY     W <- (1 - lr wd) W - lr s U, or a cautious form, with
+//                U_ij = f_i h_j X_ji (tall) / X_ij (wide), f from NorMuon and
+//                Muon+ rows, h from Muon+ columns. Speedtronic "Muon update",
+//                "Muon+", "Cautious updates"; flaxchat step 4.
+//   EW_COPYOUT   Newton-Schulz-only output U in the caller's dtype.
+//
+// Plus the per-view row finalisation (NorMuon state update, norm restore,
+// Muon+ row factor; flaxchat step 3, Speedtronic "Muon+").
+#include "mh_internal.h"
+#include "muonhybrid.h"
+
+namespace mh {
+namespace {
+
+constexpr int kSqPad = 2;  // bf16 padding of the shared transpose tiles
+
+__device__ __forceinline__ int find_job(const EwParams& p, int64_t tile) {
+  int lo = 0, hi = p.njobs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.jobs[mid].tile_begin <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Loads `nvalid` (<= 4) consecutive elements starting at element `off`.
+__device__ __forceinline__ void load4(const void* base, int dt, int64_t off, int nvalid, bool vec,
+                                      float o[4]) {
+  if (vec && nvalid == 4) {
+    if (dt == MH_F32) {
+      const float4 t = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + off));
+      o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+    } else {
+      const uint2 t = __ldcs(reinterpret_cast<const uint2*>(static_cast<const bf16*>(base) + off));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+      o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < nvalid)
+      o[k] = dt == MH_F32 ? static_cast<const float*>(base)[off + k]
+                          : __bfloat162float(static_cast<const bf16*>(base)[off + k]);
+    else
+      o[k] = 0.0f;
+  }
+}
+
+__device__ __forceinline__ void store4(void* base, int dt, int64_t off, int nvalid, bool vec,
+                                       const float x[4]) {
+  if (vec && nvalid == 4) {
+    if (dt == MH_F32) {
+      __stcs(reinterpret_cast<float4*>(static_cast<float*>(base) + off),
+             make_float4(x[0], x[1], x[2], x[3]));
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+      uint2 t;
+      t.x = *reinterpret_cast<uint32_t*>(&a);
+      t.y = *reinterpret_cast<uint32_t*>(&b);
+      __stcs(reinterpret_cast<uint2*>(static_cast<bf16*>(base) + off), t);
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < nvalid) {
+      if (dt == MH_F32)
+        static_cast<float*>(base)[off + k] = x[k];
+      else
+        static_cast<bf16*>(base)[off + k] = __float2bfloat16_rn(x[k]);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct TileInfo {
+  int job;
+  int64_t v, r0, c0;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const EwParams& p, int64_t tile) {
+  TileInfo t;
+  t.job = find_job(p, tile);
+  const EwJob& J = p.jobs[t.job];
+  const int64_t local = tile - J.tile_begin;
+  const int64_t per_view = static_cast<int64_t>(J.tiles_r) * J.tiles_c;
+  t.v = local / per_view;
+  const int64_t w = local - t.v * per_view;
+  t.r0 = (w / J.tiles_c) * kEwTileR;
+  t.c0 = (w % J.tiles_c) * kEwTileC;
+  return t;
+}
+
+// Loads this thread's 4 x 4 block of U (rows r0+4*warp+i, cols c0+4*lane+k)
+// from the Newton-Schulz output buffer. Tall views are stored transposed, so
+// the tile is staged through shared memory. Must be called by the whole CTA.
+__device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t,
+                                             bf16 (*sU)[kEwTileR + kSqPad], float u[4][4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bf16* xv = J.xf + t.v * J.x_view_stride;
+  if (J.tall) {
+    // X rows are stored columns c0..c0+127; X columns are stored rows r0..r0+31.
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int task = threadIdx.x + rep * kEwThreads;
+      const int cc = task >> 2, seg = task & 3;
+      const int64_t xr = t.c0 + cc;
+      const int64_t xc0 = t.r0 + seg * 8;
+      if (xr < J.cols) {
+        const bf16* src = xv + xr * J.ldx + xc0;
+        const int64_t nval = J.rows - xc0;
+        if (nval >= 8) {
+          const uint4 q = *reinterpret_cast<const uint4*>(src);
+          const bf16* h = reinterpret_cast<const bf16*>(&q);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sU[cc][seg * 8 + k] = h[k];
+        } else {
+          for (int k = 0; k < 8; ++k)
+            sU[cc][seg * 8 + k] = k < nval ? src[k] : __float2bfloat16_rn(0.0f);
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) u[i][k] = __bfloat162float(sU[lane * 4 + k][warp * 4 + i]);
+    __syncthreads();
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = t.r0 + warp * 4 + i;
+      const int64_t col = t.c0 + lane * 4;
+      const int64_t nv = J.cols - col;
+      const int nvalid = nv >= 4 ? 4 : (nv > 0 ? static_cast<int>(nv) : 0);
+      if (row < J.rows && nvalid > 0) {
+        load4(xv + row * J.ldx, MH_BF16, col, nvalid, true, u[i]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) u[i][k] = 0.0f;
+      }
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ EwParams p) {
+  __shared__ __align__(16) bf16 sQ[kEwTileR][kEwTileC + kSqPad];     // prologue, tall
+  __shared__ __align__(16) bf16 sU[kEwTileC][kEwTileR + kSqPad];     // U loads, tall
+  __shared__ float sRed[kEwThreads / 32][kEwTileC];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    const TileInfo t = tile_info(p, tile);
+    const EwJob& J = p.jobs[t.job];
+    const int64_t view_elem0 = t.v * J.rows * J.cols;
+    const int64_t col = t.c0 + lane * 4;
+    const int64_t ncol = J.cols - col;
+    const int nvalid = ncol >= 4 ? 4 : (ncol > 0 ? static_cast<int>(ncol) : 0);
+
+    if constexpr (KIND == EW_PROLOGUE) {
+      float ss = 0.0f;
+      bf16* xv = J.x0 + t.v * J.x_view_stride;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int lr = warp * 4 + i;
+        const int64_t row = t.r0 + lr;
+        if (row >= J.rows || nvalid == 0) continue;
+        const int64_t off = view_elem0 + row * J.cols + col;
+        float g[4], q[4];
+        load4(J.src, J.src_dtype, off, nvalid, J.src_vec, g);
+        if (p.use_momentum) {
+          float b[4];
+          load4(J.mom, MH_F32, off, nvalid, J.mom_vec, b);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            b[k] = p.mu * b[k] + (1.0f - p.mu) * g[k];
+            q[k] = p.nesterov ? g[k] + p.mu * (b[k] - g[k]) : b[k];
+          }
+          store4(J.mom, MH_F32, off, nvalid, J.mom_vec, b);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) q[k] = g[k];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ss += q[k] * q[k];  // q[k] == 0 beyond nvalid
+        if (!J.tall) {
+          store4(xv + row * J.ldx, MH_BF16, col, nvalid, true, q);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sQ[lr][lane * 4 + k] = __float2bfloat16_rn(q[k]);
+        }
+      }
+      // ||Q||_F^2 of this tile, summed in a fixed order; the per-view total
+      // is formed from these partials by the view-norm kernel.
+      ss = warp_sum(ss);
+      if (lane == 0) sRed[warp][0] = ss;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double tot = 0.0;
+#pragma unroll
+        for (int w = 0; w < kEwThreads / 32; ++w) tot += static_cast<double>(sRed[w][0]);
+        J.tile_ss[tile - J.tile_begin] = tot;
+      }
+      if (J.tall) {
+        // Write the transpose: X row = stored col (c0+cc), X cols = stored rows.
+#pragma unroll
+        for (int rep = 0; rep < 2; ++rep) {
+          const int task = threadIdx.x + rep * kEwThreads;
+          const int cc = task >> 2, seg = task & 3;
+          const int64_t xr = t.c0 + cc;
+          const int64_t xc0 = t.r0 + seg * 8;
+          if (xr >= J.cols) continue;
+          bf16* dst = xv + xr * J.ldx + xc0;
+          const int64_t nval = J.rows - xc0;
+          if (nval >= 8) {
+            uint4 q;
+            bf16* h = reinterpret_cast<bf16*>(&q);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[k] = sQ[seg * 8 + k][cc];
+            *reinterpret_cast<uint4*>(dst) = q;
+          } else {
+            for (int k = 0; k < nval; ++k) dst[k] = sQ[seg * 8 + k][cc];
+          }
+        }
+      }
+      __syncthreads();
+    } else {
+      float u[4][4];
+      load_u_block(J, t, sU, u);
+
+      if constexpr (KIND == EW_ROWSQ) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float s = u[i][0] * u[i][0] + u[i][1] * u[i][1] + u[i][2] * u[i][2] + u[i][3] * u[i][3];
+          s = warp_sum(s);
+          const int64_t row = t.r0 + warp * 4 + i;
+          if (lane == 0 && row < J.rows)
+            J.rowpart[(t.v * J.tiles_c + t.c0 / kEwTileC) * J.rows + row] = s;
+        }
+      } else if constexpr (KIND == EW_COLSQ) {
+        float cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t row = t.r0 + warp * 4 + i;
+          const float f = row < J.rows ? J.rowfac[t.v * J.rows + row] : 0.0f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x = f * u[i][k];
+            cs[k] += x * x;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sRed[warp][lane * 4 + k] = cs[k];
+        __syncthreads();
+        if (threadIdx.x < kEwTileC) {
+          float s = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kEwThreads / 32; ++w) s += sRed[w][threadIdx.x];
+          const int64_t c = t.c0 + threadIdx.x;
+          if (c < J.cols) J.colpart[(t.v * J.tiles_r + t.r0 / kEwTileR) * J.cols + c] = s;
+        }
+        __syncthreads();
+      } else {
+        // EW_APPLY / EW_COPYOUT: final update direction U_ij.
+        float uscale = 1.0f;
+        if (p.u_scale_from_sumsq)
+          uscale = 1.0f / (sqrtf(static_cast<float>(J.sumsq[t.v])) + p.ns_eps);
+        float h[4] = {1.f, 1.f, 1.f, 1.f};
+        if (p.use_colfac) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k < nvalid) h[k] = J.colfac[t.v * J.cols + col + k];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t row = t.r0 + warp * 4 + i;
+          if (row >= J.rows || nvalid == 0) continue;
+          const float f = p.use_rowfac ? J.rowfac[t.v * J.rows + row] : 1.0f;
+          float uu[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) uu[k] = (u[i][k] * uscale) * f * h[k];
+          const int64_t off = view_elem0 + row * J.cols + col;
+          if constexpr (KIND == EW_COPYOUT) {
+            store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, uu);
+          } else {
+            float w[4];
+            load4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
+            const float lr = J.lr, wd = J.wd, s = J.shape_scale;
+            if (p.cautious == MH_CAUTIOUS_OFF) {
+              const float decay = 1.0f - lr * wd;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) w[k] = decay * w[k] - (lr * s) * uu[k];
+            } else if (p.cautious == MH_CAUTIOUS_WD) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float g = s * uu[k];
+                const float mask = (g * w[k] >= 0.0f) ? 1.0f : 0.0f;
+                w[k] = w[k] - lr * (g + wd * w[k] * mask);
+              }
+            } else {
+              float gr[4];
+              load4(J.src, J.src_dtype, off, nvalid, J.src_vec, gr);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float delta = lr * wd * w[k] + (lr * s) * uu[k];
+                if (delta * gr[k] > 0.0f) w[k] = w[k] - delta;
+              }
+            }
+            store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
+          }
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) row_finalize_kernel(const __grid_constant__ RowFinParams p) {
+  __shared__ double red[2][8];
+  __shared__ float s_kappa;
+  for (int64_t vv = blockIdx.x; vv < p.total_views; vv += gridDim.x) {
+    int lo = 0, hi = p.njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.jobs[mid].view_begin <= vv) lo = mid; else hi = mid - 1;
+    }
+    const RowFinJob& J = p.jobs[lo];
+    const int64_t v = vv - J.view_begin;
+    float* part = J.rowpart + v * J.tiles_c * J.rows;
+    float* fac = J.rowfac + v * J.rows;
+    double tot = 0.0, tot2 = 0.0;
+    for (int64_t i = threadIdx.x; i < J.rows; i += blockDim.x) {
+      float q = 0.0f;
+      for (int64_t tc = 0; tc < J.tiles_c; ++tc) q += part[tc * J.rows + i];
+      float f = 1.0f;
+      if (p.normuon) {
+        float* sm = J.sm + v * J.rows;
+        const float mean = q / static_cast<float>(J.cols);
+        const float smn = sm[i] + (1.0f - p.beta2) * (mean - sm[i]);
+        sm[i] = smn;
+        f = 1.0f / sqrtf(fmaxf(smn, 1e-10f));
+      }
+      // fac holds f for now; the row sum q is needed again below, so keep it
+      // in the first tile's partial slot (this view's partials are not read
+      // by anyone else).
+      fac[i] = f;
+      part[i] = q;
+      tot += static_cast<double>(q);
+      tot2 += static_cast<double>(f) * static_cast<double>(f) * static_cast<double>(q);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      tot2 += __shfl_xor_sync(0xffffffffu, tot2, o);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+      red[0][warp] = tot;
+      red[1][warp] = tot2;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double a = 0.0, b = 0.0;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+        a += red[0][w];
+        b += red[1][w];
+      }
+      float kappa = 1.0f;
+      if (p.normuon) kappa = static_cast<float>(sqrt(a) / fmax(sqrt(b), 1e-10));
+      s_kappa = kappa;
+    }
+    __syncthreads();
+    const float kappa = s_kappa;
+    for (int64_t i = threadIdx.x; i < J.rows; i += blockDim.x) {
+      float F = kappa * fac[i];
+      if (p.muon_plus) F = F / sqrtf(F * F * part[i] + p.plus_eps);
+      fac[i] = F;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(256) col_finalize_kernel(const __grid_constant__ ColFinParams p) {
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < p.total;
+       e += int64_t(gridDim.x) * blockDim.x) {
+    int lo = 0, hi = p.njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.jobs[mid].elem_begin <= e) lo = mid; else hi = mid - 1;
+    }
+    const ColFinJob& J = p.jobs[lo];
+    const int64_t local = e - J.elem_begin;
+    const int64_t v = local / J.cols, c = local - v * J.cols;
+    const float* part = J.colpart + v * J.tiles_r * J.cols + c;
+    float s = 0.0f;
+    for (int64_t tr = 0; tr < J.tiles_r; ++tr) s += part[tr * J.cols];
+    J.colfac[local] = 1.0f / sqrtf(s + p.plus_eps);
+  }
+}
+
+// One warp per view: ||Q||_F^2 = sum of the view's per-tile partials, each
+// lane summing a fixed stride of tiles, then a fixed butterfly.
+__global__ void __launch_bounds__(256) view_norm_kernel(const __grid_constant__ NormParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t vv = warp_global; vv < p.total_views; vv += nwarps) {
+    int lo = 0, hi = p.njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.jobs[mid].view_begin <= vv) lo = mid; else hi = mid - 1;
+    }
+    const NormJob& J = p.jobs[lo];
+    const int64_t v = vv - J.view_begin;
+    const double* part = J.tile_ss + v * J.tiles_per_view;
+    double s = 0.0;
+    for (int64_t k = lane; k < J.tiles_per_view; k += 32) s += part[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) J.sumsq[v] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_col_finalize(const ColFinParams& p, int num_sms, cudaStream_t s) {
+  if (p.total <= 0) return cudaSuccess;
+  const int64_t blocks = (p.total + 255) / 256;
+  const int64_t want = static_cast<int64_t>(num_sms) * 8;
+  col_finalize_kernel<<<static_cast<int>(blocks < want ? blocks : want), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s) {
+  if (p.total_views <= 0) return cudaSuccess;
+  const int64_t blocks = (p.total_views + 7) / 8;
+  view_norm_kernel<<<static_cast<int>(blocks < 1024 ? blocks : 1024), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int64_t want = static_cast<int64_t>(num_sms) * 4;
+  const int grid = static_cast<int>(p.total_tiles < want ? p.total_tiles : want);
+  switch (kind) {
+    case EW_PROLOGUE: ew_kernel<EW_PROLOGUE><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_COPYOUT: ew_kernel<EW_COPYOUT><<<grid, kEwThreads, 0, s>>>(p); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_finalize(const RowFinParams& p, cudaStream_t s) {
+  if (p.total_views <= 0) return cudaSuccess;
+  const int grid = static_cast<int>(p.total_views < 4096 ? p.total_views : 4096);
+  row_finalize_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mh

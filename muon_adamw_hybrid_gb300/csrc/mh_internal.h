@@ -1,0 +1,191 @@
+// Internal host/device interface of libmuonhybrid: the launch records the host
+// planner fills and the kernels read from their parameter space. Not part of
+// the public ABI (see include/muonhybrid.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mh {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// Elementwise passes (prologue, NorMuon/Muon+ statistics, apply, copy-out).
+// One record per tensor; all views of a tensor share one shape and therefore
+// one Newton-Schulz shape class, and occupy consecutive class slots.
+// ---------------------------------------------------------------------------
+constexpr int kEwTileR = 32;   // tile rows (stored orientation)
+constexpr int kEwTileC = 128;  // tile cols (stored orientation)
+constexpr int kEwThreads = 256;
+constexpr int kMaxJobs = 40;   // tensors per elementwise launch (param space)
+
+struct EwJob {
+  const void* src;       // prologue: gradient (Muon) or input x (NS only)
+  float* mom;            // Muon momentum (fp32), null for NS only
+  void* dst;             // apply: parameter; copy-out: NS output
+  float* sm;             // NorMuon second moment (views*rows)
+  double* tile_ss;       // per prologue tile: partial ||Q||^2 (this tensor's first tile)
+  float* rowpart;        // [views][tiles_c][rows] partial row sums of U^2
+  float* colpart;        // [views][tiles_r][cols] partial col sums of (f U)^2
+  float* rowfac;         // [views][rows] final row factor
+  float* colfac;         // [views][cols] final col factor
+  bf16* x0;              // NS input buffer: first view of this tensor
+  const bf16* xf;        // NS output buffer: first view of this tensor
+  const double* sumsq;   // per view ||Q||_F^2 (first view of this tensor)
+  int64_t rows, cols, views;
+  int64_t ldx;           // leading dimension of the X buffers (elements)
+  int64_t x_view_stride; // elements between views in the X buffers
+  int64_t tile_begin;    // first global tile index of this tensor
+  int32_t tiles_r, tiles_c;
+  int32_t tall;          // rows > cols: X holds the transpose
+  int32_t src_dtype, dst_dtype;
+  int32_t src_vec, dst_vec, mom_vec;  // 16-byte aligned and cols % 4 == 0
+  float lr, wd, shape_scale;
+};
+
+struct EwParams {
+  EwJob jobs[kMaxJobs];
+  int32_t njobs;
+  int64_t total_tiles;
+  // hyperparameters
+  float mu;
+  int32_t nesterov;
+  int32_t use_momentum;  // 0: NS only (Q = x)
+  int32_t cautious;
+  int32_t use_rowfac, use_colfac;
+  float ns_eps;
+  int32_t u_scale_from_sumsq;  // ns_steps == 0: U = X0 / (||Q|| + eps)
+};
+
+enum EwKind { EW_PROLOGUE = 0, EW_ROWSQ = 1, EW_COLSQ = 2, EW_APPLY = 3, EW_COPYOUT = 4 };
+
+// Row finalisation (NorMuon state, NorMuon norm restore, Muon+ row factor):
+// one CTA per view. Every reduction sums per-tile partials in a fixed order,
+// so a step is bitwise reproducible.
+struct RowFinJob {
+  float* sm;
+  float* rowpart;        // [views][tiles_c][rows]; slot tc = 0 reused for row sums
+  float* rowfac;
+  int64_t rows, cols, views, tiles_c;
+  int64_t view_begin;  // prefix over views
+};
+constexpr int kMaxRowFinJobs = 96;
+struct RowFinParams {
+  RowFinJob jobs[kMaxRowFinJobs];
+  int32_t njobs;
+  int64_t total_views;
+  int32_t normuon, muon_plus;
+  float beta2, plus_eps;
+};
+
+// Column finalisation (Muon+ column factor 1/sqrt(sum + eps)), one thread per
+// (view, column).
+struct ColFinJob {
+  const float* colpart;  // [views][tiles_r][cols]
+  float* colfac;         // [views][cols]
+  int64_t cols, views, tiles_r;
+  int64_t elem_begin;    // prefix over views*cols
+};
+constexpr int kMaxColFinJobs = 96;
+struct ColFinParams {
+  ColFinJob jobs[kMaxColFinJobs];
+  int32_t njobs;
+  int64_t total;
+  float plus_eps;
+};
+
+// Per-view ||Q||_F^2 from the prologue's per-tile partials, one warp per view.
+struct NormJob {
+  const double* tile_ss;  // this tensor's first tile partial
+  double* sumsq;          // this tensor's first view
+  int64_t tiles_per_view, views;
+  int64_t view_begin;
+};
+constexpr int kMaxNormJobs = 96;
+struct NormParams {
+  NormJob jobs[kMaxNormJobs];
+  int32_t njobs;
+  int64_t total_views;
+};
+
+cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_row_finalize(const RowFinParams& p, cudaStream_t s);
+cudaError_t launch_col_finalize(const ColFinParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Grouped Newton-Schulz GEMM stage: one persistent launch covers every view
+// of up to kMaxClasses shape classes.
+// ---------------------------------------------------------------------------
+constexpr int kBM = 128;  // tile rows (TMEM lanes)
+constexpr int kBN = 256;  // tile cols (MMA N)
+constexpr int kBK = 64;   // k per stage: one 128-byte swizzle atom of bf16
+constexpr int kStages = 4;
+constexpr int kMaxClasses = 8;
+constexpr int kGemmThreads = 256;
+
+enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_APPLY = 2 };
+
+struct GemmClass {
+  CUtensorMap tmA;         // operand A: rows of X (gram), A (poly), P (apply); box 64 x 128
+  CUtensorMap tmB;         // operand B: rows of X (gram), A (poly) box 64 x 256;
+                           //            X as MN-major (apply) box 64 x 64
+  bf16* out;               // output base (first view of the class)
+  const bf16* aux;         // poly: A (b*A term); apply: X (a*X term)
+  const double* sumsq;     // per view sum of squares of Q (first iteration only)
+  int64_t out_view_stride, aux_view_stride;  // elements
+  int64_t ld_out, ld_aux;                     // elements
+  int32_t m, n;            // Newton-Schulz orientation (m <= n)
+  int32_t views;
+  int32_t tiles_m, tiles_n, tiles_per_view;
+  int32_t K;               // contraction length
+  int64_t tile_begin;      // first global tile index of this class
+};
+
+struct GemmParams {
+  GemmClass cls[kMaxClasses];
+  int32_t num_classes;
+  int32_t kind;            // GemmKind
+  int32_t first_iter;      // fold the Frobenius normalisation in
+  int64_t total_tiles;
+  float a, b, c, eps;
+  int* status;             // device status word (bounded-wait timeouts)
+};
+
+size_t gemm_smem_bytes();
+cudaError_t launch_ns_gemm(const GemmParams& p, int grid, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// AdamW
+// ---------------------------------------------------------------------------
+constexpr int kMaxAdamJobs = 160;
+constexpr int64_t kAdamChunk = 16384;  // elements per work item
+
+struct AdamJob {
+  void* param;
+  const void* grad;
+  float* m;
+  float* v;
+  int64_t numel;
+  int64_t chunk_begin;
+  int32_t pdt, gdt;
+  int32_t vec;  // all four pointers 16-byte aligned
+  float lr, wd;  // lr already multiplied by lr_mult
+};
+
+struct AdamParams {
+  AdamJob jobs[kMaxAdamJobs];
+  int32_t njobs;
+  int64_t total_chunks;
+  float beta1, beta2, eps;
+  float inv_bc1, inv_sqrt_bc2;  // 1/(1-b1^t), 1/sqrt(1-b2^t)
+};
+
+cudaError_t launch_adamw(const AdamParams& p, int num_sms, cudaStream_t s);
+
+}  // namespace mh

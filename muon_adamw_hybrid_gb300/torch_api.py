@@ -1,0 +1,240 @@
+"""Marshalling from torch tensors to the C ABI, and an optimizer facade.
+
+PyTorch supplies device memory and streams; every arithmetic step of the
+optimizer runs in libmuonhybrid's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import _lib
+from ._lib import MH_BF16, MH_F32, AdamwTensor, MuonHparams, MuonTensor, NsProblem
+
+# Speedtronic docs "v2 optimizers", "Newton-Schulz": coefficients, steps, eps.
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+NS_STEPS = 5
+NS_EPS = 1e-7
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    """fp32 -> MH_F32, bf16 -> MH_BF16; sparse, complex and other dtypes raise."""
+    if t.layout != torch.strided:
+        raise TypeError(f"sparse tensors are not supported (layout {t.layout})")
+    if t.is_complex():
+        raise TypeError(f"complex tensors are not supported (dtype {t.dtype})")
+    if t.dtype == torch.float32:
+        return MH_F32
+    if t.dtype == torch.bfloat16:
+        return MH_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: only float32 and bfloat16")
+
+
+def _dev_ptr(t: torch.Tensor, what: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_STEPS,
+                 coeffs=NS_COEFFS, normuon=False, beta2=0.95, muon_plus=False, plus_eps=NS_EPS,
+                 cautious=0) -> MuonHparams:
+    a, b, c = coeffs
+    return MuonHparams(lr=lr, momentum=momentum, nesterov=int(bool(nesterov)), eps=eps,
+                       ns_steps=ns_steps, a=a, b=b, c=c, normuon=int(bool(normuon)), beta2=beta2,
+                       muon_plus=int(bool(muon_plus)), plus_eps=plus_eps, cautious=int(cautious))
+
+
+def _view_dims(param: torch.Tensor, views: int, rows: int | None = None):
+    if param.dim() < 2:
+        raise ValueError("a Muon parameter must have at least 2 dimensions")
+    cols = param.shape[-1]
+    numel = param.numel()
+    if rows is None:
+        if views < 1 or numel % (views * cols):
+            raise ValueError(f"shape {tuple(param.shape)} cannot be split into {views} views")
+        rows = numel // (views * cols)
+    if views * rows * cols != numel:
+        raise ValueError(f"views*rows*cols != numel for shape {tuple(param.shape)}")
+    return views, rows, cols
+
+
+def muon_tensor(param: torch.Tensor, grad: torch.Tensor, momentum: torch.Tensor, views: int = 1,
+                normuon_sm: torch.Tensor | None = None, lr_mult: float = 1.0,
+                wd: float = 0.0, rows: int | None = None) -> MuonTensor:
+    """One Muon-routed tensor: ``views`` independent matrices of rows x cols.
+
+    ``param`` is (views*rows, cols) or (views, rows, cols), contiguous.
+    """
+    v, r, c = _view_dims(param, views, rows)
+    if grad.numel() != param.numel() or momentum.numel() != param.numel():
+        raise ValueError("grad and momentum must have the parameter's number of elements")
+    if momentum.dtype != torch.float32:
+        raise TypeError("the momentum buffer must be float32")
+    sm = 0
+    if normuon_sm is not None:
+        if normuon_sm.dtype != torch.float32 or normuon_sm.numel() != v * r:
+            raise ValueError("normuon_sm must be float32 with views*rows elements")
+        sm = _dev_ptr(normuon_sm, "normuon_sm")
+    return MuonTensor(param=_dev_ptr(param, "param"), grad=_dev_ptr(grad, "grad"),
+                      momentum=_dev_ptr(momentum, "momentum"), normuon_sm=sm,
+                      param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), views=v,
+                      rows=r, cols=c, lr_mult=lr_mult, wd=wd)
+
+
+def adamw_tensor(param, grad, exp_avg, exp_avg_sq, lr_mult: float = 1.0,
+                 wd: float = 0.0) -> AdamwTensor:
+    n = param.numel()
+    if grad.numel() != n or exp_avg.numel() != n or exp_avg_sq.numel() != n:
+        raise ValueError("grad and moments must have the parameter's number of elements")
+    if exp_avg.dtype != torch.float32 or exp_avg_sq.dtype != torch.float32:
+        raise TypeError("AdamW moments must be float32")
+    return AdamwTensor(param=_dev_ptr(param, "param"), grad=_dev_ptr(grad, "grad"),
+                       exp_avg=_dev_ptr(exp_avg, "exp_avg"),
+                       exp_avg_sq=_dev_ptr(exp_avg_sq, "exp_avg_sq"),
+                       param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), numel=n,
+                       lr_mult=lr_mult, wd=wd)
+
+
+def ns_problem(x: torch.Tensor, out: torch.Tensor, views: int = 1) -> NsProblem:
+    v, r, c = _view_dims(x, views)
+    if out.numel() != x.numel():
+        raise ValueError("out must have x's number of elements")
+    return NsProblem(x=_dev_ptr(x, "x"), out=_dev_ptr(out, "out"), in_dtype=dtype_code(x),
+                     out_dtype=dtype_code(out), views=v, rows=r, cols=c)
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """Caller-owned workspace (PyTorch allocations are 512-byte aligned)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def newton_schulz(xs, outs=None, views=None, steps: int = NS_STEPS, coeffs=NS_COEFFS,
+                  eps: float = NS_EPS, workspace: torch.Tensor | None = None, stream=None):
+    """U = NS(X) for a list of matrices (or stacks of views); returns the outputs."""
+    xs = list(xs)
+    if outs is None:
+        outs = [torch.empty_like(x) for x in xs]
+    views = views or [1] * len(xs)
+    probs = [ns_problem(x, o, v) for x, o, v in zip(xs, outs, views)]
+    need = _lib.ns_workspace_bytes(probs)
+    if workspace is None or workspace.numel() < need:
+        workspace = alloc_workspace(need, xs[0].device)
+    a, b, c = coeffs
+    _lib.newton_schulz_batched(probs, steps, a, b, c, eps, workspace.data_ptr(), workspace.numel(),
+                               _stream_ptr(stream))
+    return outs
+
+
+@dataclass
+class MuonGroupEntry:
+    param: torch.Tensor
+    views: int = 1
+    lr_mult: float = 1.0
+    wd: float = 0.0
+
+
+@dataclass
+class AdamGroupEntry:
+    param: torch.Tensor
+    lr_mult: float = 1.0
+    wd: float = 0.0
+
+
+class HybridMuonAdamW:
+    """Owns the optimizer state of a hybrid Muon + AdamW step and calls the library.
+
+    Muon state: one fp32 momentum buffer per routed tensor (views share it),
+    plus the NorMuon second moment when enabled. AdamW state: fp32 exp_avg and
+    exp_avg_sq. The state dict holds exactly these tensors and the AdamW step
+    count (Speedtronic "Scheduler and checkpoint behavior": Adam moments and
+    Muon momentum buffers; the cautious variants add no state).
+    """
+
+    def __init__(self, muon_params, adamw_params, lr=0.02, momentum=0.95, nesterov=True,
+                 ns_steps=NS_STEPS, coeffs=NS_COEFFS, eps=NS_EPS, normuon=False,
+                 normuon_beta2=0.95, muon_plus=False, plus_eps=NS_EPS, cautious=0,
+                 adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8):
+        self.muon = [e if isinstance(e, MuonGroupEntry) else MuonGroupEntry(**e) for e in muon_params]
+        self.adam = [e if isinstance(e, AdamGroupEntry) else AdamGroupEntry(**e) for e in adamw_params]
+        self.hp = make_hparams(lr, momentum, nesterov, eps, ns_steps, coeffs, normuon,
+                               normuon_beta2, muon_plus, plus_eps, cautious)
+        self.adam_lr, self.adam_betas, self.adam_eps = adam_lr, adam_betas, adam_eps
+        self.step_count = 0
+        self.momentum = [torch.zeros(e.param.shape, dtype=torch.float32, device=e.param.device)
+                         for e in self.muon]
+        self.normuon_sm = []
+        for e in self.muon:
+            if normuon:
+                v, r, _ = _view_dims(e.param, e.views)
+                self.normuon_sm.append(torch.zeros(v * r, dtype=torch.float32, device=e.param.device))
+            else:
+                self.normuon_sm.append(None)
+        self.exp_avg = [torch.zeros(e.param.shape, dtype=torch.float32, device=e.param.device)
+                        for e in self.adam]
+        self.exp_avg_sq = [torch.zeros_like(m) for m in self.exp_avg]
+        self._ws = None
+
+    @property
+    def lr(self) -> float:
+        return self.hp.lr
+
+    @lr.setter
+    def lr(self, value: float) -> None:
+        self.hp.lr = value
+
+    def _muon_structs(self, grads):
+        return [muon_tensor(e.param, g, m, e.views, sm, e.lr_mult, e.wd)
+                for e, g, m, sm in zip(self.muon, grads, self.momentum, self.normuon_sm)]
+
+    def _adam_structs(self, grads):
+        return [adamw_tensor(e.param, g, m, v, e.lr_mult, e.wd)
+                for e, g, m, v in zip(self.adam, grads, self.exp_avg, self.exp_avg_sq)]
+
+    def workspace_bytes(self) -> int:
+        return _lib.muon_workspace_bytes(self._muon_structs([e.param for e in self.muon]), self.hp)
+
+    def step(self, muon_grads=None, adam_grads=None, stream=None) -> None:
+        """One hybrid step. Gradients default to each parameter's ``.grad``."""
+        muon_grads = muon_grads if muon_grads is not None else [e.param.grad for e in self.muon]
+        adam_grads = adam_grads if adam_grads is not None else [e.param.grad for e in self.adam]
+        s = _stream_ptr(stream)
+        self.step_count += 1
+        if self.muon:
+            ts = self._muon_structs(muon_grads)
+            need = _lib.muon_workspace_bytes(ts, self.hp)
+            if self._ws is None or self._ws.numel() < need:
+                self._ws = alloc_workspace(need, self.muon[0].param.device)
+            _lib.muon_step_batched(ts, self.hp, self._ws.data_ptr(), self._ws.numel(), s)
+        if self.adam:
+            b1, b2 = self.adam_betas
+            _lib.adamw_step(self._adam_structs(adam_grads), self.adam_lr, b1, b2, self.adam_eps,
+                            self.step_count, s)
+
+    def state_dict(self) -> dict:
+        return {"step": self.step_count,
+                "momentum": [m.clone() for m in self.momentum],
+                "normuon_sm": [None if s is None else s.clone() for s in self.normuon_sm],
+                "exp_avg": [m.clone() for m in self.exp_avg],
+                "exp_avg_sq": [v.clone() for v in self.exp_avg_sq]}
+
+    def load_state_dict(self, sd: dict) -> None:
+        self.step_count = int(sd["step"])
+        for dst, src in zip(self.momentum, sd["momentum"]):
+            dst.copy_(src)
+        for dst, src in zip(self.normuon_sm, sd["normuon_sm"]):
+            if dst is not None:
+                dst.copy_(src)
+        for dst, src in zip(self.exp_avg, sd["exp_avg"]):
+            dst.copy_(src)
+        for dst, src in zip(self.exp_avg_sq, sd["exp_avg_sq"]):
+            dst.copy_(src)

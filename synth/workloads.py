@@ -1,0 +1,228 @@
+"""Synthetic workloads: tensor shapes, dtypes, seeds and input scales.
+
+Inputs only; no optimizer arithmetic. Shared by the tests (oracle side and
+GPU side) and the benchmark so both run on the same seeded data.
+
+Shapes follow the five benchmark configurations the optimizer is measured
+on. Where the description leaves a value open, the reading used is stated
+next to it (and in the design notes):
+  * parameter init std 0.02 where unstated;
+  * Muon lr 0.02, wd 0.01, momentum 0.95 (Nesterov) in every configuration;
+  * AdamW lr 3e-4 (the Speedtronic "Configuration" example), betas 0.9/0.95,
+    eps 1e-8, wd 0.1 on every AdamW tensor;
+  * "N(0,1e-3)" means std 1e-3; "lognormal(0,1) per tensor" is one factor
+    exp(z) per tensor, z drawn from the generator.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import lognormal_factor
+
+SEED = 0
+
+KIND_W, KIND_G, KIND_AW, KIND_AG = 0, 1, 2, 3
+
+
+def tensor_id(kind: int, index: int, step: int = 0) -> int:
+    """Generator stream of (kind, tensor index, step)."""
+    return (index << 24) | (kind << 16) | step
+
+
+@dataclass
+class MuonSpec:
+    name: str
+    views: int
+    rows: int
+    cols: int
+    param_dtype: str = "bf16"
+    grad_dtype: str = "bf16"
+    w_std: float = 0.02
+    g_std: float = 1e-3
+    lognormal: bool = False
+    lr_mult: float = 1.0
+    wd: float = 0.01
+
+    @property
+    def numel(self) -> int:
+        return self.views * self.rows * self.cols
+
+    @property
+    def shape(self):
+        return (self.views * self.rows, self.cols)
+
+
+@dataclass
+class AdamSpec:
+    name: str
+    shape: tuple
+    param_dtype: str = "bf16"
+    grad_dtype: str = "bf16"
+    w_std: float = 0.02
+    g_std: float = 1e-3
+    lognormal: bool = False
+    lr_mult: float = 1.0
+    wd: float = 0.1
+    w_const: float | None = None  # norms start at a constant (1.0)
+
+    @property
+    def numel(self) -> int:
+        return int(np.prod(self.shape))
+
+
+@dataclass
+class Workload:
+    name: str
+    muon: list = field(default_factory=list)
+    adamw: list = field(default_factory=list)
+    muon_hp: dict = field(default_factory=dict)
+    adam_hp: dict = field(default_factory=dict)
+    steps: int = 1
+    seed: int = SEED
+
+    def grad_std(self, kind: int, index: int) -> np.float32:
+        spec = (self.muon if kind == KIND_G else self.adamw)[index]
+        std = np.float32(spec.g_std)
+        if spec.lognormal:
+            std = np.float32(std * lognormal_factor(self.seed, tensor_id(kind, index)))
+        return std
+
+    @property
+    def muon_elems(self) -> int:
+        return sum(s.numel for s in self.muon)
+
+    @property
+    def adam_elems(self) -> int:
+        return sum(s.numel for s in self.adamw)
+
+
+MUON_HP = dict(lr=0.02, momentum=0.95, nesterov=True, eps=1e-7, ns_steps=5,
+               coeffs=(3.4445, -4.7750, 2.0315))
+ADAM_HP = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8)
+
+
+def single_matrix() -> Workload:
+    """256 x 1024 fp32, W and G ~ N(0, 1), zero momentum, one step."""
+    return Workload(
+        name="single_256x1024_fp32",
+        muon=[MuonSpec("W", 1, 256, 1024, "f32", "f32", w_std=1.0, g_std=1.0)],
+        muon_hp=dict(MUON_HP), adam_hp=dict(ADAM_HP), steps=1)
+
+
+def gpt124m() -> Workload:
+    """d=768, 12 layers: Q/K/V/O 768^2, gate_up (2, 2048, 768), down 768 x 2048
+    on Muon; embedding 50304 x 768 and two RMSNorm vectors per layer on
+    AdamW. bf16 params and grads, grads N(0,1e-3) * lognormal per tensor."""
+    muon, adamw = [], []
+    for l in range(12):
+        for nm in ("q", "k", "v", "o"):
+            muon.append(MuonSpec(f"l{l}.{nm}", 1, 768, 768, lognormal=True))
+        muon.append(MuonSpec(f"l{l}.gate_up", 2, 2048, 768, lognormal=True))
+        muon.append(MuonSpec(f"l{l}.down", 1, 768, 2048, lognormal=True))
+    adamw.append(AdamSpec("embed", (50304, 768), lognormal=True))
+    for l in range(12):
+        for k in range(2):
+            adamw.append(AdamSpec(f"l{l}.norm{k}", (768,), lognormal=True, w_const=1.0))
+    return Workload("gpt124m_d768_l12", muon, adamw, dict(MUON_HP), dict(ADAM_HP), steps=10)
+
+
+def llama7b() -> Workload:
+    """d=4096, 32 layers, GQA: Q/O 4096^2, K/V 1024 x 4096, gate_up
+    (2, 14336, 4096), down 4096 x 14336 on Muon; untied embedding and head
+    128256 x 4096 plus 65 norms on AdamW; bf16 params/grads, fp32 state."""
+    muon, adamw = [], []
+    for l in range(32):
+        muon.append(MuonSpec(f"l{l}.q", 1, 4096, 4096))
+        muon.append(MuonSpec(f"l{l}.k", 1, 1024, 4096))
+        muon.append(MuonSpec(f"l{l}.v", 1, 1024, 4096))
+        muon.append(MuonSpec(f"l{l}.o", 1, 4096, 4096))
+        muon.append(MuonSpec(f"l{l}.gate_up", 2, 14336, 4096))
+        muon.append(MuonSpec(f"l{l}.down", 1, 4096, 14336))
+    adamw.append(AdamSpec("embed", (128256, 4096)))
+    adamw.append(AdamSpec("head", (128256, 4096)))
+    for k in range(65):
+        adamw.append(AdamSpec(f"norm{k}", (4096,), w_const=1.0))
+    return Workload("llama7b_d4096_l32", muon, adamw, dict(MUON_HP), dict(ADAM_HP), steps=1)
+
+
+def moe_mla() -> Workload:
+    """One MoE layer with 64 experts (gate_up (2, 1408, 2048) as two wide
+    views, down 2048 x 1408 tall) and the MLA kv up-projection, 32 heads x
+    (128 K + 128 V rows) x 512, as 64 views of 128 x 512. NorMuon (beta2 0.95),
+    Muon+ row_col and cautious weight decay on."""
+    muon = []
+    for e in range(64):
+        muon.append(MuonSpec(f"e{e}.gate_up", 2, 1408, 2048))
+        muon.append(MuonSpec(f"e{e}.down", 1, 2048, 1408))
+    muon.append(MuonSpec("mla.kv_b", 64, 128, 512))
+    hp = dict(MUON_HP, normuon=True, beta2=0.95, muon_plus=True, cautious=1)
+    return Workload("moe64_mla_all_variants", muon, [], hp, dict(ADAM_HP), steps=1)
+
+
+def ns_sweep_shapes():
+    """Newton-Schulz-only sweep: square n x n, wide n x 4n and tall 4n x n for
+    n in {512 .. 8192}, batch counts 1..256 capped at 64 GB of operand X."""
+    out = []
+    for n in (512, 1024, 2048, 4096, 8192):
+        for aspect, (r, c) in (("1:1", (n, n)), ("1:4", (n, 4 * n)), ("4:1", (4 * n, n))):
+            for batch in (1, 4, 16, 64, 256):
+                if batch * r * c * 2 > 64 * 2 ** 30:
+                    continue
+                out.append((aspect, n, batch, r, c))
+    return out
+
+
+def adamw_2p30() -> Workload:
+    """AdamW alone on 2^30 fp32 elements (HBM roofline case)."""
+    return Workload("adamw_2p30_fp32", [], [AdamSpec("flat", (1 << 30,), "f32", "f32",
+                                                     w_std=1.0, g_std=1e-3)],
+                    dict(MUON_HP), dict(ADAM_HP), steps=1)
+
+
+WORKLOADS = {
+    "single": single_matrix,
+    "gpt124m": gpt124m,
+    "llama7b": llama7b,
+    "moe_mla": moe_mla,
+    "adamw_2p30": adamw_2p30,
+}
+
+
+# ---- materialisation -----------------------------------------------------------
+
+def host_tensor(wl: Workload, kind: int, index: int, step: int = 0, offset: int = 0,
+                count: int | None = None) -> np.ndarray:
+    """Float64 copy (exact values of the stored dtype) of a tensor's inputs,
+    or of ``count`` elements from flat ``offset``."""
+    spec = (wl.muon if kind in (KIND_W, KIND_G) else wl.adamw)[index]
+    n = spec.numel if count is None else count
+    if kind in (KIND_W, KIND_AW):
+        dt, std = spec.param_dtype, np.float32(spec.w_std)
+        if getattr(spec, "w_const", None) is not None:
+            return np.full(n, spec.w_const, dtype=np.float64)
+    else:
+        dt, std = spec.grad_dtype, wl.grad_std(kind, index)
+    from . import normal
+    return normal(wl.seed, tensor_id(kind, index, step if kind in (KIND_G, KIND_AG) else 0),
+                  (n,), std=std, dtype=dt, offset=offset).astype(np.float64)
+
+
+def device_tensor(wl: Workload, kind: int, index: int, step: int = 0, device="cuda"):
+    """The same tensor created on the GPU by the CUDA generator."""
+    import torch
+    from .gpu import fill_normal
+    spec = (wl.muon if kind in (KIND_W, KIND_G) else wl.adamw)[index]
+    shape = spec.shape
+    if kind in (KIND_W, KIND_AW):
+        dt = spec.param_dtype
+        tdt = torch.float32 if dt == "f32" else torch.bfloat16
+        if getattr(spec, "w_const", None) is not None:
+            return torch.full(shape, spec.w_const, dtype=tdt, device=device)
+        t = torch.empty(shape, dtype=tdt, device=device)
+        return fill_normal(t, wl.seed, tensor_id(kind, index), np.float32(spec.w_std))
+    dt = spec.grad_dtype
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    t = torch.empty(shape, dtype=tdt, device=device)
+    return fill_normal(t, wl.seed, tensor_id(kind, index, step), wl.grad_std(kind, index))

@@ -1,0 +1,180 @@
+"""The C ABI library on a machine without a GPU: it loads, exports every
+declared entry point, its structs match the header's layout, and the host-side
+argument checks reject bad calls before anything touches a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import muon_adamw_hybrid_gb300 as mh
+from muon_adamw_hybrid_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", "muonhybrid.h"), os.path.join(ROOT, "include", "mhsynth.h")]
+
+
+def _declared(header):
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:mh|synth)_[a-z_0-9]+)\s*\(", text)))
+
+
+def _exports(lib_path):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True,
+                         check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if line.strip()}
+
+
+def test_library_exports_every_declared_symbol():
+    declared = _declared(HEADERS[0])
+    assert set(_lib.EXPORTED) <= set(declared) | set(_lib.EXPORTED)
+    exports = _exports(_lib.LIB_PATH)
+    for name in declared:
+        assert name in exports, name
+        assert hasattr(_lib.LIB, name)
+
+
+def test_synth_library_exports():
+    path = os.path.join(ROOT, "synth", "libmhsynth.so")
+    exports = _exports(path)
+    for name in _declared(HEADERS[1]):
+        assert name in exports, name
+
+
+def test_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "sizes.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "muonhybrid.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(mh_muon_tensor),"
+        " sizeof(mh_muon_hparams), sizeof(mh_ns_problem), sizeof(mh_adamw_tensor),"
+        " offsetof(mh_muon_tensor, views), offsetof(mh_muon_hparams, cautious),"
+        " offsetof(mh_adamw_tensor, numel)); return 0;}\n")
+    exe = tmp_path / "sizes"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True,
+                                       check=True).stdout.split()))
+    want = [ctypes.sizeof(mh.MuonTensor), ctypes.sizeof(mh.MuonHparams),
+            ctypes.sizeof(mh.NsProblem), ctypes.sizeof(mh.AdamwTensor),
+            mh.MuonTensor.views.offset, mh.MuonHparams.cautious.offset,
+            mh.AdamwTensor.numel.offset]
+    assert got == want
+
+
+def _tensor(**kw):
+    base = dict(param=256, grad=512, momentum=768, normuon_sm=0, param_dtype=0, grad_dtype=0,
+                views=1, rows=4, cols=6, lr_mult=1.0, wd=0.0)
+    base.update(kw)
+    return mh.MuonTensor(**base)
+
+
+def _step(tensors, hp=None, ws=0, wsb=0):
+    hp = hp or mh.make_hparams()
+    arr = (mh.MuonTensor * max(1, len(tensors)))(*tensors)
+    return _lib.LIB.mh_muon_step_batched(arr, len(tensors), ctypes.byref(hp), ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(param_dtype=5), _lib.MH_EDTYPE),     # complex / other dtypes
+    (dict(grad_dtype=-1), _lib.MH_EDTYPE),
+    (dict(param=0), _lib.MH_EINVAL),
+    (dict(momentum=0), _lib.MH_EINVAL),
+    (dict(rows=-3), _lib.MH_ESHAPE),
+    (dict(cols=1 << 25), _lib.MH_ESHAPE),
+    (dict(rows=40000, cols=40000), _lib.MH_EUNSUPPORTED),
+    (dict(lr_mult=float("nan")), _lib.MH_EINVAL),
+])
+def test_muon_rejects_bad_tensor(kw, code):
+    assert _step([_tensor(**kw)]) == code
+    assert mh.last_error() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(momentum=1.0), dict(momentum=-0.1), dict(eps=0.0),
+                                dict(ns_steps=17), dict(ns_steps=-1), dict(cautious=3),
+                                dict(coeffs=(float("inf"), 0, 0)),
+                                dict(normuon=True, beta2=1.0)])
+def test_muon_rejects_bad_hparams(kw):
+    assert _step([_tensor()], hp=mh.make_hparams(**kw)) == _lib.MH_EINVAL
+
+
+def test_normuon_requires_state():
+    assert _step([_tensor()], hp=mh.make_hparams(normuon=True)) == _lib.MH_EINVAL
+    assert "normuon_sm" in mh.last_error()
+
+
+def test_workspace_checks_happen_before_any_device_work():
+    t = [_tensor()]
+    need = mh.muon_workspace_bytes(t, mh.make_hparams())
+    assert need > 0
+    assert _step(t, ws=0, wsb=need) == _lib.MH_EWORKSPACE
+    assert _step(t, ws=4096 + 16, wsb=need) == _lib.MH_EWORKSPACE      # misaligned
+    assert _step(t, ws=4096, wsb=need - 1) == _lib.MH_EWORKSPACE        # too small
+    assert "too small" in mh.last_error()
+
+
+def test_empty_calls_are_noops():
+    assert _step([]) == _lib.MH_OK
+    assert _step([_tensor(rows=0)]) == _lib.MH_OK
+    assert _step([_tensor(views=0, param=0, grad=0, momentum=0)]) == _lib.MH_OK
+    arr = (mh.AdamwTensor * 1)(mh.AdamwTensor(numel=0))
+    assert _lib.LIB.mh_adamw_step(arr, 1, 1e-3, 0.9, 0.95, 1e-8, 1, None) == _lib.MH_OK
+
+
+def test_workspace_bytes_layout():
+    # One 256 x 1024 view: 256-byte status header, sumsq (one double, padded
+    # to 256 B), per-tile norm partials (8 x 8 tiles of 32 x 128, doubles),
+    # rounded up to 1 KiB; then X0 and X1 (256 x 1024 bf16 each) and A and P
+    # (256 x 256 bf16 each).
+    need = mh.muon_workspace_bytes([_tensor(rows=256, cols=1024)], mh.make_hparams())
+    assert need == 1024 + 2 * 256 * 1024 * 2 + 2 * 256 * 256 * 2
+    # A tall view shares the transposed class: (1024 x 256) and (256 x 1024)
+    # need one class with two slots; the statistics region grows to 2 KiB.
+    two = mh.muon_workspace_bytes([_tensor(rows=256, cols=1024), _tensor(rows=1024, cols=256)],
+                                  mh.make_hparams())
+    assert two == 2048 + 2 * (2 * 256 * 1024 * 2 + 2 * 256 * 256 * 2)
+    # Ragged sizes pad the leading dimensions to multiples of 8 (5 x 16 and
+    # 5 x 8 bf16 per buffer, each rounded to 1 KiB).
+    rag = mh.muon_workspace_bytes([_tensor(rows=5, cols=13)], mh.make_hparams())
+    assert rag == 1024 + 2 * 1024 + 2 * 1024
+    # NorMuon and Muon+ add row and column statistics.
+    more = mh.muon_workspace_bytes([_tensor(rows=256, cols=1024, normuon_sm=1024)],
+                                   mh.make_hparams(normuon=True, muon_plus=True))
+    assert more > need
+
+
+def test_adamw_rejects_bad_args():
+    good = mh.AdamwTensor(param=256, grad=512, exp_avg=768, exp_avg_sq=1024, numel=10)
+    arr = (mh.AdamwTensor * 1)(good)
+    L = _lib.LIB
+    assert L.mh_adamw_step(arr, 1, 1e-3, 0.9, 0.95, 1e-8, 0, None) == _lib.MH_EINVAL  # step 0
+    assert L.mh_adamw_step(arr, 1, 1e-3, 1.0, 0.95, 1e-8, 1, None) == _lib.MH_EINVAL
+    assert L.mh_adamw_step(arr, -1, 1e-3, 0.9, 0.95, 1e-8, 1, None) == _lib.MH_EINVAL
+    bad = (mh.AdamwTensor * 1)(mh.AdamwTensor(param=256, grad=512, exp_avg=0, exp_avg_sq=1024,
+                                              numel=10))
+    assert L.mh_adamw_step(bad, 1, 1e-3, 0.9, 0.95, 1e-8, 1, None) == _lib.MH_EINVAL
+    cplx = (mh.AdamwTensor * 1)(mh.AdamwTensor(param=256, grad=512, exp_avg=768, exp_avg_sq=1024,
+                                               numel=10, grad_dtype=9))
+    assert L.mh_adamw_step(cplx, 1, 1e-3, 0.9, 0.95, 1e-8, 1, None) == _lib.MH_EDTYPE
+
+
+def test_ns_rejects_bad_args():
+    p = mh.NsProblem(x=256, out=512, in_dtype=0, out_dtype=0, views=1, rows=8, cols=8)
+    arr = (mh.NsProblem * 1)(p)
+    L = _lib.LIB
+    assert L.mh_newton_schulz_batched(arr, 1, 17, 1.0, 0.0, 0.0, 1e-7, None, 0, None) == _lib.MH_EINVAL
+    assert L.mh_newton_schulz_batched(arr, 1, 5, 1.0, 0.0, 0.0, 0.0, None, 0, None) == _lib.MH_EINVAL
+    assert L.mh_newton_schulz_batched(arr, 1, 5, 1.0, 0.0, 0.0, 1e-7, None, 0, None) == _lib.MH_EWORKSPACE
+
+
+def test_torch_marshalling_rejects_sparse_and_complex():
+    import torch
+    with pytest.raises(TypeError):
+        mh.dtype_code(torch.zeros(2, 2).to_sparse())
+    with pytest.raises(TypeError):
+        mh.dtype_code(torch.zeros(2, 2, dtype=torch.complex64))
+    with pytest.raises(TypeError):
+        mh.dtype_code(torch.zeros(2, 2, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        mh.muon_tensor(torch.zeros(4, 4), torch.zeros(4, 4), torch.zeros(4, 4))  # not CUDA
