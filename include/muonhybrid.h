@@ -139,6 +139,32 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
                              float b, float c, float eps, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Size of the fixed scratch array behind mh_newton_schulz_batched_noalloc. */
+#define MH_NS_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* mh_newton_schulz_batched for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that have no way to provide a workspace -- for example a plugin that its
+ * host application gives only input and output buffers, or a program whose
+ * device memory is already fully reserved by its own pool -- and so can
+ * neither call cudaMalloc nor keep a scratch buffer between calls.
+ * Same problems, arguments and results as mh_newton_schulz_batched, with the
+ * workspace taken from a file-scope device array of
+ * MH_NS_STATIC_SCRATCH_BYTES (64 MiB) inside the library instead of from
+ * the caller; the call allocates nothing.
+ *   - Requests whose mh_ns_workspace_bytes exceeds that size return
+ *     MH_EWORKSPACE (with a message) before anything is enqueued.
+ *   - Each GPU that loads the library holds its own array until exit.
+ *   - All calls on one device share its array, which keeps the last call's
+ *     contents (nothing stale is ever read: the status word is cleared and
+ *     every other byte is written before use). Calls whose GPU work overlaps,
+ *     e.g. on two unordered streams, race on the array: serialise them.
+ *   - The first call on each device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture on the device. */
+int mh_newton_schulz_batched_noalloc(const mh_ns_problem* problems, int32_t n, int32_t steps,
+                                     float a, float b, float c, float eps, void* stream);
+
 /* One AdamW-routed tensor, treated as a flat array of numel elements. */
 typedef struct {
   void* param;            /* numel, param_dtype, updated in place */

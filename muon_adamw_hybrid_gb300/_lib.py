@@ -20,7 +20,9 @@ MH_CAUTIOUS_OFF, MH_CAUTIOUS_WD, MH_CAUTIOUS_UPDATE = 0, 1, 2
 
 EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_bytes",
             "mh_newton_schulz_batched", "mh_adamw_step", "mh_workspace_status", "mh_last_error",
-            "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read")
+            "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read",
+            "mh_newton_schulz_batched_noalloc")
+NS_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class MuonTensor(ctypes.Structure):
@@ -77,6 +79,9 @@ def _load() -> ctypes.CDLL:
                                              c_float, c_float, c_float, c_void_p, c_size_t,
                                              c_void_p]
     lib.mh_newton_schulz_batched.restype = c_int
+    lib.mh_newton_schulz_batched_noalloc.argtypes = [POINTER(NsProblem), c_int32, c_int32,
+                                                     c_float, c_float, c_float, c_float, c_void_p]
+    lib.mh_newton_schulz_batched_noalloc.restype = c_int
     lib.mh_adamw_step.argtypes = [POINTER(AdamwTensor), c_int32, c_float, c_float, c_float,
                                   c_float, c_int64, c_void_p]
     lib.mh_adamw_step.restype = c_int
@@ -142,6 +147,14 @@ def newton_schulz_batched(problems, steps: int, a: float, b: float, c: float, ep
     arr, n = _array(NsProblem, problems)
     _check(LIB.mh_newton_schulz_batched(arr, n, steps, a, b, c, eps, workspace, workspace_bytes,
                                         stream))
+
+
+def newton_schulz_batched_noalloc(problems, steps: int, a: float, b: float, c: float, eps: float,
+                                  stream: int) -> None:
+    """mh_newton_schulz_batched without a workspace argument: the scratch is a
+    fixed 64 MiB array inside the library, for callers that cannot allocate."""
+    arr, n = _array(NsProblem, problems)
+    _check(LIB.mh_newton_schulz_batched_noalloc(arr, n, steps, a, b, c, eps, stream))
 
 
 def adamw_step(tensors, lr: float, beta1: float, beta2: float, eps: float, step: int,

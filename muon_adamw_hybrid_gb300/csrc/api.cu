@@ -563,6 +563,9 @@ int check_workspace(const Plan& P, const void* ws, size_t bytes) {
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
 }  // namespace mh
 
 using namespace mh;

@@ -188,4 +188,7 @@ struct AdamParams {
 
 cudaError_t launch_adamw(const AdamParams& p, int num_sms, cudaStream_t s);
 
+// Sets the calling thread's message returned by mh_last_error().
+void set_last_error(const char* msg);
+
 }  // namespace mh
