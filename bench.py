@@ -52,7 +52,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama7b")
+    ap.add_argument("--workload", default="llama7b",
+                    help="llama7b (default), gpt124m, moe_mla, single, adamw_2p30, or ns "
+                         "(Newton-Schulz only, see --ns-n/--ns-aspect/--ns-batch)")
+    ap.add_argument("--ns-n", type=int, default=4096)
+    ap.add_argument("--ns-aspect", default="1:1", choices=["1:1", "1:4", "4:1"])
+    ap.add_argument("--ns-batch", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -428,9 +433,80 @@ def config_dict(wl, world):
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
+def run_ns_only(args):
+    """Newton-Schulz alone on a batch of n x n, n x 4n or 4n x n matrices
+    (entries N(0,1), bf16 in and out), timed like the full step."""
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+    from synth.gpu import fill_normal
+    world, rank, local = dist_setup(args)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = load_peaks()
+    n = args.ns_n
+    r, c = {"1:1": (n, n), "1:4": (n, 4 * n), "4:1": (4 * n, n)}[args.ns_aspect]
+    b = args.ns_batch
+    x = torch.empty(b * r, c, dtype=torch.bfloat16, device=device)
+    fill_normal(x, 0, 5000 + n, 1.0)
+    out = torch.empty_like(x)
+    probs = [mh.ns_problem(x, out, b)]
+    need = mh.ns_workspace_bytes(probs)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    a_, b_, c_ = 3.4445, -4.7750, 2.0315
+
+    def call():
+        mh.newton_schulz_batched(probs, 5, a_, b_, c_, 1e-7, ws.data_ptr(), need, stream.cuda_stream)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    mh.profiler_reset()
+    mh.profiler_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    mh.profiler_enable(False)
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    ks = mh.profiler_read()
+    m_, n_ = min(r, c), max(r, c)
+    flops = b * 5 * (4.0 * m_ * m_ * n_ + 2.0 * m_ ** 3)
+    g = ks.get("ns_gemm", {"total_ms": 0.0, "flops": 0.0, "flops_executed": 0.0, "launches": 0})
+    peak = peaks["bf16_tflops"]
+    ach = g["flops"] / (g["total_ms"] * 1e-3) / 1e12 if g["total_ms"] else 0.0
+    if rank == 0:
+        print(json.dumps({
+            "metric": "Newton-Schulz TFLOP/s (nominal 4m^2n+2m^3 per iteration)",
+            "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"ns_{args.ns_aspect}_n{n}_batch{b}", "rows": r, "cols": c,
+                       "batch": b, "l2": "X operand " + ("larger" if b * r * c * 2 > 129e6
+                                                         else "smaller") + " than L2"},
+            "roofline": {"kernel": "ns_gemm", "bound": "tensor", "achieved": round(ach, 1),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                         "traffic": None, "peak_source": f"bf16 burst, of {peak_src}",
+                         "executed_tflops": round(g["flops_executed"] / (g["total_ms"] * 1e-3) / 1e12, 1)
+                         if g["total_ms"] else None},
+            "kernels": {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3)}
+                        for k, v in ks.items()},
+            "gpu_launches": sum(v["launches"] for v in ks.values()), "clocks": clk}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from synth import workloads as W
+    if args.workload == "ns":
+        return run_ns_only(args)
     if args.workload not in W.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(W.WORKLOADS)}")
     wl = W.WORKLOADS[args.workload]()
