@@ -351,13 +351,13 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           G.n = static_cast<int32_t>(C.n);
           G.views = static_cast<int32_t>(C.count);
           G.sumsq = sumsq + class_first[k];
-          G.tiles_m = static_cast<int32_t>(ceil_div(C.m, kBM));
+          // Work units are 256 x 256 blocks, one per CTA pair (2 x 128 rows).
+          G.tiles_m = static_cast<int32_t>(ceil_div(C.m, 2 * kBM));
           int rc;
           if (kind == GEMM_GRAM || kind == GEMM_POLY) {
+            // Upper block triangle: row block pm holds column blocks pm..T-1.
             G.tiles_n = static_cast<int32_t>(ceil_div(C.m, kBN));
-            int64_t per = 0;
-            for (int tm = 0; tm < G.tiles_m; ++tm) per += G.tiles_n - (tm >> 1);
-            G.tiles_per_view = static_cast<int32_t>(per);
+            G.tiles_per_view = G.tiles_n * (G.tiles_n + 1) / 2;
             G.out = kind == GEMM_GRAM ? A : Pm;
             G.out_view_stride = C.m * C.lda;
             G.ld_out = C.lda;
@@ -367,14 +367,14 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
               G.aux_view_stride = C.m * C.ldx;
               G.ld_aux = C.ldx;
               if ((rc = make_tmap(&G.tmA, X, C.n, C.m, C.count, C.ldx, kBM)) != MH_OK) return rc;
-              if ((rc = make_tmap(&G.tmB, X, C.n, C.m, C.count, C.ldx, kBN)) != MH_OK) return rc;
+              G.tmB = G.tmA;  // each CTA of a pair loads 128 of the 256 B rows
             } else {
               G.K = static_cast<int32_t>(C.m);
               G.aux = A;
               G.aux_view_stride = C.m * C.lda;
               G.ld_aux = C.lda;
               if ((rc = make_tmap(&G.tmA, A, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
-              if ((rc = make_tmap(&G.tmB, A, C.m, C.m, C.count, C.lda, kBN)) != MH_OK) return rc;
+              G.tmB = G.tmA;
             }
           } else {
             G.tiles_n = static_cast<int32_t>(ceil_div(C.n, kBN));
@@ -402,7 +402,7 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           const double m = G.m, nn = G.n, v = G.views;
           flops += v * (kind == GEMM_POLY ? 2.0 * m * m * m : 2.0 * m * m * nn);
           const double kpad = std::ceil(G.K / double(kBK)) * kBK;
-          fexec += double(G.tiles_per_view) * v * 2.0 * kBM * kBN * kpad;
+          fexec += double(G.tiles_per_view) * v * 2.0 * (2.0 * kBM) * kBN * kpad;
           // operands read once and the output written once (bf16)
           if (kind == GEMM_GRAM) bytes += v * 2.0 * (m * nn + m * m);
           else if (kind == GEMM_POLY) bytes += v * 2.0 * (m * m + m * m);

@@ -133,7 +133,8 @@ enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_APPLY = 2 };
 
 struct GemmClass {
   CUtensorMap tmA;         // operand A: rows of X (gram), A (poly), P (apply); box 64 x 128
-  CUtensorMap tmB;         // operand B: rows of X (gram), A (poly) box 64 x 256;
+  CUtensorMap tmB;         // operand B: rows of X (gram), A (poly) box 64 x 128 (half
+                           //            of the 256 B rows per CTA of a pair);
                            //            X as MN-major (apply) box 64 x 64
   bf16* out;               // output base (first view of the class)
   const bf16* aux;         // poly: A (b*A term); apply: X (a*X term)
@@ -142,9 +143,9 @@ struct GemmClass {
   int64_t ld_out, ld_aux;                     // elements
   int32_t m, n;            // Newton-Schulz orientation (m <= n)
   int32_t views;
-  int32_t tiles_m, tiles_n, tiles_per_view;
+  int32_t tiles_m, tiles_n, tiles_per_view;  // in 256 x 256 pair blocks
   int32_t K;               // contraction length
-  int64_t tile_begin;      // first global tile index of this class
+  int64_t tile_begin;      // first global pair-block index of this class
 };
 
 struct GemmParams {
@@ -158,7 +159,9 @@ struct GemmParams {
 };
 
 size_t gemm_smem_bytes();
-cudaError_t launch_ns_gemm(const GemmParams& p, int grid, cudaStream_t s);
+// Launches one persistent grid of CTA pairs (clusters of two), at most one
+// pair per two SMs that can hold a cluster.
+cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // AdamW

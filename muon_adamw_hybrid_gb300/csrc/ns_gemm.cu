@@ -1,5 +1,6 @@
 // Grouped Newton-Schulz GEMM stage on sm_103a tensor cores (tcgen05 + TMEM,
-// operands staged by TMA with 128-byte swizzle).
+// operands staged by TMA with 128-byte swizzle, CTA pairs sharing operands by
+// TMA multicast).
 //
 // One quintic step (Speedtronic "v2 optimizers", "Newton-Schulz"; flaxchat
 // "Optimizer", "Muon Algorithm" step 2) is three launches of this kernel:
@@ -16,16 +17,27 @@
 // the gram epilogue scales by s^2 and the apply epilogue by s, so the
 // prologue never has to re-read Q to normalise it.
 //
-// Layout: every view of every shape class is one problem; a persistent CTA
-// (one per SM) walks a static list of 128 x 256 output tiles spanning all
-// classes. Warp roles: warp 0 issues TMA loads into a 4-stage ring, warp 1
-// issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators,
-// warp 2 owns the TMEM allocation, warps 4-7 drain an accumulator with
-// tcgen05.ld, apply the stage's epilogue in fp32 and store bf16, while the
-// MMA warp already fills the other accumulator.
+// Work unit: a 256 x 256 output block computed by a cluster of two CTAs, CTA
+// rank k taking rows 128k..128k+127 (one tcgen05.mma M=128 N=256 K=16 per
+// 16 of k). Both CTAs need the same 256 B-rows per k-step: each loads half of
+// them and multicasts it to both, so every CTA fetches 32 KB per 64-deep k
+// step from L2 instead of 48 KB. A CTA frees a pipeline stage only when the
+// MMAs of both CTAs have read it (the MMA completion is multicast to both
+// "empty" barriers).
+//
+// Warp roles per CTA: warp 0 issues TMA loads into a 4-stage ring, warp 1
+// issues tcgen05.mma into one of two TMEM accumulators, warp 2 owns the TMEM
+// allocation, warps 4-7 drain an accumulator with tcgen05.ld, apply the
+// stage's epilogue in fp32 and store bf16 while the MMA warp fills the other
+// accumulator. Mirrored halves of the symmetric outputs are transposed in
+// shared memory so that they are written as 64-byte row segments.
 //
 // Every mbarrier wait is bounded; on timeout the CTA records a status code in
-// the workspace, drains what it has in flight, frees TMEM and exits.
+// the workspace, raises the abort flag of both CTAs of its pair, drains what
+// it has in flight, frees TMEM and exits.
+#include <map>
+#include <mutex>
+
 #include "mh_internal.h"
 #include "mh_ptx.cuh"
 
@@ -34,14 +46,20 @@ namespace {
 
 constexpr uint32_t kStageABytes = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kStageBBytes = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kHalfBBytes = kStageBBytes / 2;
 constexpr uint32_t kTmemCols = 2 * kBN;           // two fp32 accumulators
 constexpr uint32_t kApplyChunkBytes = kBK * 64 * 2;  // one 64-col MN-major box: 8 KB
+constexpr int kTPitch = 40;                        // bf16 pitch of the mirror-transpose tile
+constexpr uint32_t kTBytes = 32 * kTPitch * 2;     // per epilogue warp
+constexpr uint16_t kPairMask = 0x3;
 
 struct TileCoord {
   int cls, view, tm, tn;
 };
 
-__device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t) {
+// Maps a pair-tile index to (class, view, 256-row block pm, 256-col block tn)
+// and returns this CTA's 128-row tile tm = 2 pm + rank.
+__device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t, uint32_t rank) {
   int c = 0;
   while (c + 1 < p.num_classes && t >= p.cls[c + 1].tile_begin) ++c;
   const GemmClass& C = p.cls[c];
@@ -50,22 +68,22 @@ __device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t) {
   tc.cls = c;
   tc.view = static_cast<int>(local / C.tiles_per_view);
   int w = static_cast<int>(local - static_cast<int64_t>(tc.view) * C.tiles_per_view);
+  int pm;
   if (p.kind == GEMM_APPLY) {
-    tc.tm = w % C.tiles_m;
+    pm = w % C.tiles_m;
     tc.tn = w / C.tiles_m;
   } else {
-    // Row tm of 128 holds the 256-wide column tiles tn >= tm/2 (those that
-    // reach the diagonal or lie above it).
-    int tm = 0;
+    // Row block pm holds the column blocks tn >= pm (upper block triangle).
+    pm = 0;
     while (true) {
-      const int cnt = C.tiles_n - (tm >> 1);
+      const int cnt = C.tiles_n - pm;
       if (w < cnt) break;
       w -= cnt;
-      ++tm;
+      ++pm;
     }
-    tc.tm = tm;
-    tc.tn = (tm >> 1) + w;
+    tc.tn = pm + w;
   }
+  tc.tm = 2 * pm + static_cast<int>(rank);
   return tc;
 }
 
@@ -102,13 +120,21 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&x)[32]) {
   }
 }
 
+// Raises the abort flag of both CTAs of the pair.
+__device__ __forceinline__ void abort_pair(volatile int* abort_flag) {
+  *abort_flag = 1;
+  st_cluster_s32(abort_flag, 0, 1);
+  st_cluster_s32(abort_flag, 1, 1);
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kStageBBytes);
+  uint8_t* sT = sB + kStages * kStageBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sT + 4 * kTBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -119,11 +145,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t pair = blockIdx.x >> 1;
+  const int64_t npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // released by the MMAs of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -144,7 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barrier inits of both CTAs visible before any remote traffic
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const bool apply = p.kind == GEMM_APPLY;
@@ -154,11 +183,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t inflight = 0;             // stages with a load issued
-      uint32_t inflight_par = 0;         // parity of that load's phase
+      uint32_t inflight = 0;     // stages with a load issued
+      uint32_t inflight_par = 0; // parity of that load's phase
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
-        const TileCoord tc = map_tile(p, t);
+      for (int64_t t = pair; ok && t < p.total_tiles; t += npairs) {
+        const TileCoord tc = map_tile(p, t, rank);
         const GemmClass& C = p.cls[tc.cls];
         const int nk = (C.K + kBK - 1) / kBK;
         for (int kb = 0; kb < nk; ++kb) {
@@ -171,12 +200,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                       tc.view);
           uint8_t* b_dst = sB + stage * kStageBBytes;
           if (apply) {
+            // This CTA's two 64-column chunks of the 256-column X block.
 #pragma unroll
-            for (int j = 0; j < kBN / 64; ++j)
-              tma_load_3d(b_dst + j * kApplyChunkBytes, &C.tmB, &full[stage], tc.tn * kBN + j * 64,
-                          kb * kBK, tc.view);
+            for (int j = 2 * static_cast<int>(rank); j < 2 * static_cast<int>(rank) + 2; ++j)
+              tma_load_3d_mc(b_dst + j * kApplyChunkBytes, &C.tmB, &full[stage],
+                             tc.tn * kBN + j * 64, kb * kBK, tc.view, kPairMask);
           } else {
-            tma_load_3d(b_dst, &C.tmB, &full[stage], kb * kBK, tc.tn * kBN, tc.view);
+            // This CTA's 128 of the 256 B rows.
+            tma_load_3d_mc(b_dst + rank * kHalfBBytes, &C.tmB, &full[stage], kb * kBK,
+                           tc.tn * kBN + static_cast<int>(rank) * kBM, tc.view, kPairMask);
           }
           inflight |= 1u << stage;
           inflight_par = (inflight_par & ~(1u << stage)) | (phase << stage);
@@ -186,8 +218,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
         }
       }
+      if (ok) {
+        // Wait until both CTAs' MMAs have released every stage this CTA
+        // filled: after this, no arrive from the peer can still be on its way
+        // to this CTA's barriers.
+        for (int i = 0; i < kStages; ++i) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_TMA)) {
+            ok = false;
+            break;
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
       if (!ok) {
-        // Let every issued copy land before the CTA's shared memory goes away.
+        abort_pair(abort_flag);
+        // Let every copy into this CTA's shared memory land before it exits.
         for (int s = 0; s < kStages; ++s)
           if (inflight & (1u << s)) mbar_wait_drain(&full[s], (inflight_par >> s) & 1u);
       }
@@ -201,8 +249,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
-      for (int64_t t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
-        const TileCoord tc = map_tile(p, t);
+      for (int64_t t = pair; ok && t < p.total_tiles; t += npairs) {
+        const TileCoord tc = map_tile(p, t, rank);
         const GemmClass& C = p.cls[tc.cls];
         const int nk = (C.K + kBK - 1) / kBK;
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
@@ -230,7 +278,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          tc_commit(&empty[stage]);
+          tc_commit_mc(&empty[stage], kPairMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -241,6 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
+      if (!ok) abort_pair(abort_flag);
       if (!ok && issued) {
         tc_commit(drain);
         mbar_wait_drain(drain, 0);
@@ -249,15 +298,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
     const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
+    bf16* tbuf = reinterpret_cast<bf16*>(sT + ew * kTBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-      const TileCoord tc = map_tile(p, t);
+    for (int64_t t = pair; t < p.total_tiles; t += npairs) {
+      const TileCoord tc = map_tile(p, t, rank);
       const GemmClass& C = p.cls[tc.cls];
-      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPI)) break;
+      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPI)) {
+        abort_pair(abort_flag);
+        break;
+      }
       tc_fence_after();
 
-      const int r = tc.tm * kBM + ew * 32 + lane;
+      const int r0 = tc.tm * kBM + ew * 32;  // first row of this warp
+      const int r = r0 + lane;
       const int n_out = apply ? C.n : C.m;
       float sc = 1.0f;
       if (p.first_iter) {
@@ -293,47 +347,68 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
               for (int j = 0; j < 32; ++j) v[j] = sc * (p.a * x[j] + v[j]);
               store_bf16x32(out + off, v);
             } else {
-              for (int j = 0; j < n_out - c0; ++j)
-                out[off + j] = __float2bfloat16_rn(sc * (p.a * __bfloat162float(aux[aoff + j]) + v[j]));
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (c0 + j < n_out)
+                  out[off + j] =
+                      __float2bfloat16_rn(sc * (p.a * __bfloat162float(aux[aoff + j]) + v[j]));
+            }
+          }
+          continue;
+        }
+
+        // Symmetric output: element (r, c) with c >= r is stored at (r, c)
+        // and, when c > r, mirrored to (c, r).
+        if (p.kind == GEMM_POLY) {
+          if (row_ok) {
+            const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
+            if (full_cols) {
+              float x[32];
+              load_bf16x32(aux + aoff, x);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = p.b * x[j] + p.c * v[j];
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (c0 + j < n_out) v[j] = p.b * __bfloat162float(aux[aoff + j]) + p.c * v[j];
             }
           }
         } else {
-          // Symmetric output: element (r, c) with c >= r is stored at (r, c)
-          // and, when c > r, mirrored to (c, r).
-          if (p.kind == GEMM_POLY) {
-            if (row_ok) {
-              const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
-              if (full_cols) {
-                float x[32];
-                load_bf16x32(aux + aoff, x);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = p.b * x[j] + p.c * v[j];
-              } else {
-                for (int j = 0; j < 32; ++j)
-                  if (c0 + j < n_out) v[j] = p.b * __bfloat162float(aux[aoff + j]) + p.c * v[j];
-              }
-            }
+          for (int j = 0; j < 32; ++j) v[j] *= sc;
+        }
+        if (row_ok) {
+          const int64_t off = static_cast<int64_t>(r) * C.ld_out + c0;
+          if (full_cols && c0 >= r) {
+            store_bf16x32(out + off, v);
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] *= sc;
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < n_out && c0 + j >= r) out[off + j] = __float2bfloat16_rn(v[j]);
           }
-          if (row_ok) {
-            const int64_t off = static_cast<int64_t>(r) * C.ld_out + c0;
-            if (full_cols && c0 >= r) {
-              store_bf16x32(out + off, v);
-            } else {
-              for (int j = 0; j < 32; ++j) {
-                const int c = c0 + j;
-                if (c < n_out && c >= r) out[off + j] = __float2bfloat16_rn(v[j]);
-              }
-            }
+        }
+        if (c0 + 31 > r0) {  // some element of the chunk lies above the diagonal (warp-uniform)
+          // Transpose the 32 x 32 chunk in shared memory: lane L then owns
+          // output row c0 + L and writes columns r0 .. r0+31 of it.
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int c = c0 + j;
-              if (c < n_out && c > r)
-                out[static_cast<int64_t>(c) * C.ld_out + r] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 32; ++j) tbuf[j * kTPitch + lane] = __float2bfloat16_rn(v[j]);
+          __syncwarp();
+          const int c = c0 + lane;
+          if (c < n_out) {
+            bf16* dst = out + static_cast<int64_t>(c) * C.ld_out + r0;
+            const bf16* src = tbuf + lane * kTPitch;
+            if (r0 + 32 <= c && r0 + 32 <= C.m) {
+              const uint4* s4 = reinterpret_cast<const uint4*>(src);
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) d4[q] = s4[q];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (r0 + i < c && r0 + i < C.m) dst[i] = src[i];
             }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -343,8 +418,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
   }
 
+  // Neither CTA of the pair leaves while the other may still multicast into
+  // its shared memory or arrive on its barriers.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -354,10 +431,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 }  // namespace
 
 size_t gemm_smem_bytes() {
-  return 1024 + kStages * (kStageABytes + kStageBBytes) + (2 * kStages + 5) * sizeof(uint64_t) + 16;
+  return 1024 + kStages * (kStageABytes + kStageBBytes) + 4 * kTBytes +
+         (2 * kStages + 5) * sizeof(uint64_t) + 16;
 }
 
-cudaError_t launch_ns_gemm(const GemmParams& p, int grid, cudaStream_t s) {
+// Maximum number of co-resident CTA pairs on the current device (GPCs with an
+// odd number of free SMs leave one SM out), cached per device.
+int gemm_max_pairs(int dev, int num_sms) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, ns_gemm_kernel, &cfg) != cudaSuccess ||
+      clusters <= 0) {
+    (void)cudaGetLastError();
+    clusters = num_sms / 2;
+  }
+  cache[dev] = clusters;
+  return clusters;
+}
+
+cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
   const size_t smem = gemm_smem_bytes();
   static thread_local int configured_device = -1;
@@ -370,8 +477,22 @@ cudaError_t launch_ns_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int g = static_cast<int>(p.total_tiles < grid ? p.total_tiles : grid);
-  ns_gemm_kernel<<<g, kGemmThreads, smem, s>>>(p);
+  const int64_t max_pairs = gemm_max_pairs(dev, num_sms);
+  const int64_t pairs = p.total_tiles < max_pairs ? p.total_tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
