@@ -219,6 +219,19 @@ class DeviceWorkload:
             self.mh.workspace_status(self.ws.data_ptr(), stream.cuda_stream)
 
 
+def family_stats(stats: dict) -> dict:
+    """Merges the library's per-stage records ("ns_gemm.gram", ...) into
+    kernel families ("ns_gemm")."""
+    out = {}
+    for name, v in stats.items():
+        fam = name.split(".")[0]
+        a = out.setdefault(fam, {"launches": 0, "total_ms": 0.0, "bytes": 0.0, "flops": 0.0,
+                                 "flops_executed": 0.0})
+        for k in a:
+            a[k] += v[k]
+    return out
+
+
 def ns_flops(wl) -> float:
     steps = wl.muon_hp["ns_steps"]
     tot = 0.0
@@ -475,7 +488,7 @@ def run_ns_only(args):
     mh.profiler_enable(False)
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-    ks = mh.profiler_read()
+    ks = family_stats(mh.profiler_read())
     m_, n_ = min(r, c), max(r, c)
     flops = b * 5 * (4.0 * m_ * m_ * n_ + 2.0 * m_ ** 3)
     g = ks.get("ns_gemm", {"total_ms": 0.0, "flops": 0.0, "flops_executed": 0.0, "launches": 0})
@@ -546,8 +559,9 @@ def main():
     clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
     ms_step = max_over_ranks(ms_total / args.steps, world)
-    kstats = mh.profiler_read()
+    stage_stats = mh.profiler_read()
     dw.check_status(stream)
+    kstats = family_stats(stage_stats)
     launches = sum(v["launches"] for v in kstats.values())
 
     # ---- roofline of the dominant kernel and of the top HBM-bound kernel -------------
@@ -591,6 +605,9 @@ def main():
                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
                         "peak_source": f"HBM copy, of {peak_src}"}
+    stages = {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
+                  "tflops_executed": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)}
+              for k, v in stage_stats.items() if "." in k and v["total_ms"] > 0}
     nsf = ns_flops(wl)
     ns_ms = kstats.get("ns_gemm", {}).get("total_ms", 0.0) / max(args.steps, 1)
 
@@ -644,6 +661,7 @@ def main():
             "ns_tflops": round(nsf / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
             "ns_ms_per_step": round(ns_ms, 3),
             "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,
+            "ns_stages": stages,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "resident_gb": round(dw.resident_bytes / 1e9, 1),
         }

@@ -14,6 +14,8 @@
 //   [0, 256)        device status word (bounded-wait timeouts)
 //   sumsq           double per view: ||Q||_F^2
 //   tile_ss         double per prologue tile: partial ||Q||_F^2
+//   vrec            per view: parameter/gradient pointers, shape, lr, wd (the
+//                   last Newton-Schulz apply updates parameters directly)
 //   rowpart         float per (view, column tile, stored row)   (NorMuon / Muon+)
 //   rowfac          float per (view, stored row)                 (NorMuon / Muon+)
 //   colpart         float per (view, row tile, stored col)       (Muon+)
@@ -86,8 +88,8 @@ struct Plan {
   std::vector<TensorInfo> tensors;
   int64_t total_views = 0, total_tiles = 0;
   int64_t n_rowpart = 0, n_rowfac = 0, n_colpart = 0, n_colfac = 0;
-  size_t off_sumsq = 0, off_tile_ss = 0, off_rowpart = 0, off_rowfac = 0, off_colpart = 0,
-         off_colfac = 0;
+  size_t off_sumsq = 0, off_tile_ss = 0, off_vrec = 0, off_rowpart = 0, off_rowfac = 0,
+         off_colpart = 0, off_colfac = 0;
   size_t bytes = 0;
 };
 
@@ -154,6 +156,8 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
   off = align_up(off + sizeof(double) * static_cast<size_t>(P.total_views), 256);
   P.off_tile_ss = off;
   off = align_up(off + sizeof(double) * static_cast<size_t>(P.total_tiles), 256);
+  P.off_vrec = off;
+  off = align_up(off + sizeof(ViewRec) * static_cast<size_t>(P.total_views), 256);
   if (need_rows) {
     P.off_rowpart = off;
     off = align_up(off + sizeof(float) * static_cast<size_t>(P.n_rowpart), 256);
@@ -316,8 +320,11 @@ class ProfScope {
 
 // ---- Newton-Schulz stages --------------------------------------------------------
 
+// Launches the 3 * steps grouped GEMM stages. When `final_update` is set, the
+// last apply stage writes the parameter update (from the per-view records)
+// instead of the last X.
 int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, float eps, int sms,
-           cudaStream_t stream, int* final_buf) {
+           cudaStream_t stream, int* final_buf, bool final_update = false, int cautious = 0) {
   int cur = 0;
   const int nclass = static_cast<int>(P.classes.size());
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
@@ -338,6 +345,9 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
         gp.c = c;
         gp.eps = eps;
         gp.status = status;
+        const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
+        gp.final_update = fused ? 1 : 0;
+        gp.cautious = cautious;
         int64_t tiles = 0;
         int nc = 0;
         for (int k = c0; k < nclass && nc < kMaxClasses; ++k, ++nc) {
@@ -351,6 +361,7 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           G.n = static_cast<int32_t>(C.n);
           G.views = static_cast<int32_t>(C.count);
           G.sumsq = sumsq + class_first[k];
+          G.vrec = reinterpret_cast<const ViewRec*>(ws + P.off_vrec) + class_first[k];
           // Work units are 256 x 256 blocks, one per CTA pair (2 x 128 rows).
           G.tiles_m = static_cast<int32_t>(ceil_div(C.m, 2 * kBM));
           int rc;
@@ -406,9 +417,12 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           // operands read once and the output written once (bf16)
           if (kind == GEMM_GRAM) bytes += v * 2.0 * (m * nn + m * m);
           else if (kind == GEMM_POLY) bytes += v * 2.0 * (m * m + m * m);
-          else bytes += v * 2.0 * (m * m + 2.0 * m * nn);
+          else if (!fused) bytes += v * 2.0 * (m * m + 2.0 * m * nn);
+          else bytes += v * (2.0 * (m * m + m * nn) + 2.0 * 2.0 * m * nn);  // + W read/write (bf16)
         }
-        ProfScope ps(stream, "ns_gemm", bytes, flops, fexec);
+        static const char* kNames[4] = {"ns_gemm.gram", "ns_gemm.poly", "ns_gemm.apply",
+                                         "ns_gemm.apply_update"};
+        ProfScope ps(stream, kNames[fused ? 3 : kind], bytes, flops, fexec);
         cudaError_t e = launch_ns_gemm(gp, sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
       }
@@ -602,7 +616,11 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   float* rowfac = reinterpret_cast<float*>(ws + P.off_rowfac);
   float* colpart = reinterpret_cast<float*>(ws + P.off_colpart);
   float* colfac = reinterpret_cast<float*>(ws + P.off_colfac);
+  ViewRec* vrec = reinterpret_cast<ViewRec*>(ws + P.off_vrec);
   const bool need_rows = hp->normuon || hp->muon_plus;
+  // Without NorMuon / Muon+ the update needs nothing beyond U itself, so the
+  // last Newton-Schulz apply stage writes the parameters directly.
+  const bool fuse_update = !need_rows && hp->ns_steps >= 1;
 
   EwParams proto;
   std::memset(&proto, 0, sizeof(proto));
@@ -636,6 +654,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     J.xf = xb;
     J.sumsq = sumsq + T.view_slot;
     J.tile_ss = tile_ss + T.tile_off;
+    J.vrec = vrec + T.view_slot;
     if (need_rows) {
       J.rowpart = rowpart + T.rowpart_off;
       J.rowfac = rowfac + T.rowfac_off;
@@ -653,8 +672,10 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
               sms, stream);
   if (rc != MH_OK) return rc;
   if ((rc = run_view_norm(P, tile_ss, sumsq, stream)) != MH_OK) return rc;
-  rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf);
+  rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf,
+              fuse_update, hp->cautious);
   if (rc != MH_OK) return rc;
+  if (fuse_update) return MH_OK;
   auto fill_final = [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, final_buf); };
   if (need_rows) {
     rc = run_ew(EW_ROWSQ, P, proto, fill_final, sms, stream);

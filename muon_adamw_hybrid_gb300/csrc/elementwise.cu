@@ -180,6 +180,22 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
     const int nvalid = ncol >= 4 ? 4 : (ncol > 0 ? static_cast<int>(ncol) : 0);
 
     if constexpr (KIND == EW_PROLOGUE) {
+      if (J.vrec != nullptr && threadIdx.x == 0 && t.r0 == 0 && t.c0 == 0) {
+        ViewRec rec;
+        rec.param = J.dst;
+        rec.grad = J.src;
+        rec.elem0 = view_elem0;
+        rec.rows = J.rows;
+        rec.cols = J.cols;
+        rec.lr = J.lr;
+        rec.wd = J.wd;
+        rec.shape_scale = J.shape_scale;
+        rec.pdt = J.dst_dtype;
+        rec.gdt = J.src_dtype;
+        rec.tall = J.tall;
+        rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
+        J.vrec[t.v] = rec;
+      }
       float ss = 0.0f;
       bf16* xv = J.x0 + t.v * J.x_view_stride;
 #pragma unroll

@@ -24,6 +24,19 @@ constexpr int kEwTileC = 128;  // tile cols (stored orientation)
 constexpr int kEwThreads = 256;
 constexpr int kMaxJobs = 40;   // tensors per elementwise launch (param space)
 
+// Per-view record written by the prologue and read by the final Newton-Schulz
+// apply when it applies the parameter update itself (no NorMuon / Muon+).
+struct ViewRec {
+  void* param;          // tensor base
+  const void* grad;     // tensor base
+  int64_t elem0;        // first element of this view
+  int64_t rows, cols;   // stored view
+  float lr, wd, shape_scale;
+  int32_t pdt, gdt;
+  int32_t tall;
+  int32_t vec;          // param and grad 16-byte aligned and cols % 8 == 0
+};
+
 struct EwJob {
   const void* src;       // prologue: gradient (Muon) or input x (NS only)
   float* mom;            // Muon momentum (fp32), null for NS only
@@ -37,6 +50,7 @@ struct EwJob {
   bf16* x0;              // NS input buffer: first view of this tensor
   const bf16* xf;        // NS output buffer: first view of this tensor
   const double* sumsq;   // per view ||Q||_F^2 (first view of this tensor)
+  ViewRec* vrec;         // per view record (first view of this tensor), or null
   int64_t rows, cols, views;
   int64_t ldx;           // leading dimension of the X buffers (elements)
   int64_t x_view_stride; // elements between views in the X buffers
@@ -139,6 +153,7 @@ struct GemmClass {
   bf16* out;               // output base (first view of the class)
   const bf16* aux;         // poly: A (b*A term); apply: X (a*X term)
   const double* sumsq;     // per view sum of squares of Q (first iteration only)
+  const ViewRec* vrec;     // per view records (final update only)
   int64_t out_view_stride, aux_view_stride;  // elements
   int64_t ld_out, ld_aux;                     // elements
   int32_t m, n;            // Newton-Schulz orientation (m <= n)
@@ -153,6 +168,8 @@ struct GemmParams {
   int32_t num_classes;
   int32_t kind;            // GemmKind
   int32_t first_iter;      // fold the Frobenius normalisation in
+  int32_t final_update;    // apply: update the parameters instead of writing X'
+  int32_t cautious;        // MH_CAUTIOUS_* for the final update
   int64_t total_tiles;
   float a, b, c, eps;
   int* status;             // device status word (bounded-wait timeouts)

@@ -40,6 +40,7 @@
 
 #include "mh_internal.h"
 #include "mh_ptx.cuh"
+#include "muonhybrid.h"
 
 namespace mh {
 namespace {
@@ -50,7 +51,8 @@ constexpr uint32_t kHalfBBytes = kStageBBytes / 2;
 constexpr uint32_t kTmemCols = 2 * kBN;           // two fp32 accumulators
 constexpr uint32_t kApplyChunkBytes = kBK * 64 * 2;  // one 64-col MN-major box: 8 KB
 constexpr int kTPitch = 40;                        // bf16 pitch of the mirror-transpose tile
-constexpr uint32_t kTBytes = 32 * kTPitch * 2;     // per epilogue warp
+constexpr int kUPitch = 36;                        // fp32 pitch of the update-transpose tile
+constexpr uint32_t kTBytes = 32 * kUPitch * 4;     // per epilogue warp (holds either)
 constexpr uint16_t kPairMask = 0x3;
 
 struct TileCoord {
@@ -118,6 +120,88 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&x)[32]) {
     u.w = pack_bf16x2(x[q * 8 + 6], x[q * 8 + 7]);
     d[q] = u;
   }
+}
+
+__device__ __forceinline__ void load_f32x32(const void* base, int dt, int64_t off, int nvalid,
+                                            bool vec, float (&x)[32]) {
+  if (vec) {
+    if (dt == MH_F32) {
+      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 t = s[q];
+        x[4 * q] = t.x; x[4 * q + 1] = t.y; x[4 * q + 2] = t.z; x[4 * q + 3] = t.w;
+      }
+    } else {
+      load_bf16x32(static_cast<const bf16*>(base) + off, x);
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < nvalid)
+      x[j] = dt == MH_F32 ? static_cast<const float*>(base)[off + j]
+                          : __bfloat162float(static_cast<const bf16*>(base)[off + j]);
+    else
+      x[j] = 0.0f;
+  }
+}
+
+__device__ __forceinline__ void store_f32x32(void* base, int dt, int64_t off, int nvalid, bool vec,
+                                             const float (&x)[32]) {
+  if (vec) {
+    if (dt == MH_F32) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        d[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else {
+      store_bf16x32(static_cast<bf16*>(base) + off, x);
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < nvalid) {
+      if (dt == MH_F32)
+        static_cast<float*>(base)[off + j] = x[j];
+      else
+        static_cast<bf16*>(base)[off + j] = __float2bfloat16_rn(x[j]);
+    }
+  }
+}
+
+// The parameter update of Speedtronic "Muon update" (decoupled decay and
+// max(1, rows/cols)^0.5 scale), or one of the cautious forms (flaxchat step
+// 4; Speedtronic "Cautious updates"), on 32 consecutive elements of one
+// stored row starting at element `off`; u holds the Newton-Schulz output.
+__device__ __forceinline__ void update_w32(const ViewRec& R, int64_t off, int nvalid,
+                                           const float (&u)[32], int cautious) {
+  const bool vec = R.vec && nvalid == 32;
+  float w[32];
+  load_f32x32(R.param, R.pdt, off, nvalid, vec, w);
+  const float lr = R.lr, wd = R.wd, sc = R.shape_scale;
+  if (cautious == MH_CAUTIOUS_OFF) {
+    const float decay = 1.0f - lr * wd;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) w[j] = decay * w[j] - (lr * sc) * u[j];
+  } else if (cautious == MH_CAUTIOUS_WD) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float g = sc * u[j];
+      const float mask = (g * w[j] >= 0.0f) ? 1.0f : 0.0f;
+      w[j] = w[j] - lr * (g + wd * w[j] * mask);
+    }
+  } else {
+    float gr[32];
+    load_f32x32(R.grad, R.gdt, off, nvalid, vec, gr);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float delta = lr * wd * w[j] + (lr * sc) * u[j];
+      if (delta * gr[j] > 0.0f) w[j] = w[j] - delta;
+    }
+  }
+  store_f32x32(R.param, R.pdt, off, nvalid, vec, w);
 }
 
 // Raises the abort flag of both CTAs of the pair.
@@ -336,6 +420,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         const bool row_ok = r < C.m;
         const bool full_cols = c0 + 32 <= n_out;
 
+        if (apply && p.final_update) {
+          // Last Newton-Schulz step: U = sc (a X + P X) goes straight into
+          // the parameter update; X' is not stored.
+          float u[32];
+          if (row_ok) {
+            const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
+            if (full_cols) {
+              float x[32];
+              load_bf16x32(aux + aoff, x);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) u[j] = sc * (p.a * x[j] + v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                u[j] = c0 + j < n_out ? sc * (p.a * __bfloat162float(aux[aoff + j]) + v[j]) : 0.0f;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) u[j] = 0.0f;
+          }
+          const ViewRec R = C.vrec[tc.view];
+          if (!R.tall) {
+            if (row_ok) {
+              const int nvalid = n_out - c0 < 32 ? n_out - c0 : 32;
+              update_w32(R, R.elem0 + static_cast<int64_t>(r) * R.cols + c0, nvalid, u,
+                         p.cautious);
+            }
+          } else {
+            // Tall view: X row r is stored column r. Transpose the 32 x 32
+            // chunk so lane L updates stored row c0 + L, columns r0..r0+31.
+            float* tb = reinterpret_cast<float*>(tbuf);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tb[j * kUPitch + lane] = u[j];
+            __syncwarp();
+            const int wrow = c0 + lane;
+            if (wrow < n_out) {
+              float ut[32];
+              const float4* s4 = reinterpret_cast<const float4*>(tb + lane * kUPitch);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 t4 = s4[q];
+                ut[4 * q] = t4.x; ut[4 * q + 1] = t4.y; ut[4 * q + 2] = t4.z; ut[4 * q + 3] = t4.w;
+              }
+              const int nvalid = C.m - r0 < 32 ? C.m - r0 : 32;
+              update_w32(R, R.elem0 + static_cast<int64_t>(wrow) * R.cols + r0, nvalid, ut,
+                         p.cautious);
+            }
+            __syncwarp();
+          }
+          continue;
+        }
         if (apply) {
           if (row_ok) {
             const int64_t off = static_cast<int64_t>(r) * C.ld_out + c0;
