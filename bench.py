@@ -244,25 +244,20 @@ def ns_flops(wl) -> float:
 # ---- host buffers for the end-to-end measurement -------------------------------------
 
 class PinnedMirror:
-    """One page-locked host buffer mirroring a list of device tensors."""
+    """One page-locked host buffer (a single torch pinned allocation) mirroring
+    a list of device tensors."""
 
     def __init__(self, tensors):
-        import numpy as np
         import torch
         self.tensors = tensors
         self.nbytes = sum(t.numel() * t.element_size() for t in tensors)
-        self.buf = np.empty(max(self.nbytes, 1), dtype=np.uint8)
-        err = torch.cuda.cudart().cudaHostRegister(self.buf.ctypes.data, self.buf.nbytes, 0)
-        try:
-            self.registered = int(getattr(err, "value", err)) == 0
-        except (TypeError, ValueError):
-            self.registered = False
+        self.buf = torch.empty(max(self.nbytes, 1), dtype=torch.uint8, pin_memory=True)
+        self.registered = bool(self.buf.is_pinned())
         self.host = []
         off = 0
-        base = torch.from_numpy(self.buf)
         for t in tensors:
             nb = t.numel() * t.element_size()
-            self.host.append(base[off:off + nb].view(t.dtype).view(t.shape))
+            self.host.append(self.buf[off:off + nb].view(t.dtype).view(t.shape))
             off += nb
 
     def fill_from_device(self):
@@ -278,9 +273,8 @@ class PinnedMirror:
             h.copy_(t, non_blocking=True)
 
     def close(self):
-        import torch
-        if self.registered:
-            torch.cuda.cudart().cudaHostUnregister(self.buf.ctypes.data)
+        self.host = []
+        self.buf = None
 
 
 # ---- oracle (CPU baseline / reference arm) ------------------------------------------------
@@ -624,18 +618,23 @@ def main():
             gin.h2d(); dw.step(stream); pout.d2h()
         torch.cuda.synchronize()
         barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            ev[k][0].record(stream)
             gin.h2d()
+            ev[k][1].record(stream)
             dw.step(stream)
+            ev[k][2].record(stream)
             pout.d2h()
-        e1.record(stream)
+            ev[k][3].record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        e2e_ms = max_over_ranks(ev[0][0].elapsed_time(ev[-1][3]) / args.steps, world)
+        h2d_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        d2h_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
         e2e = {"value": round(e2e_ms, 3), "unit": "ms/step", "h2d_bytes_per_step": gin.nbytes,
-               "d2h_bytes_per_step": pout.nbytes,
+               "d2h_bytes_per_step": pout.nbytes, "h2d_ms": round(h2d_ms, 2),
+               "d2h_ms": round(d2h_ms, 2),
                "path": "C ABI calls with gradients copied in from pinned host memory and "
                        "updated parameters copied back each step",
                "pinned": bool(gin.registered and pout.registered)}
@@ -645,7 +644,7 @@ def main():
     # ---- CPU oracle baseline (rank 0, one GPU) -------------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        views, adam = oracle_sample_plan(wl, muon_flop_budget=4.0e12, adam_elems=1 << 24)
+        views, adam = oracle_sample_plan(wl, muon_flop_budget=1.2e13, adam_elems=1 << 24)
         ms_muon, ms_adam = OracleSample(wl, views, adam).run()
         cpu_ms = oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam)
         cpu = {"value": round(cpu_ms, 1), "unit": "ms/step", "cores": blas_threads(),

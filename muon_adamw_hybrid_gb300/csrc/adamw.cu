@@ -14,6 +14,9 @@
 #include "muonhybrid.h"
 
 namespace mh {
+
+static_assert(sizeof(AdamParams) <= 32000, "AdamParams exceeds the kernel parameter space");
+
 namespace {
 
 struct F8 {

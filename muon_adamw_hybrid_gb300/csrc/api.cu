@@ -13,7 +13,7 @@
 // Workspace (256-byte aligned base):
 //   [0, 256)        device status word (bounded-wait timeouts)
 //   sumsq           double per view: ||Q||_F^2
-//   tile_ss         double per prologue tile: partial ||Q||_F^2
+//   tile_ss         float per prologue tile and warp: partial ||Q||_F^2
 //   vrec            per view: parameter/gradient pointers, shape, lr, wd (the
 //                   last Newton-Schulz apply updates parameters directly)
 //   rowpart         float per (view, column tile, stored row)   (NorMuon / Muon+)
@@ -77,7 +77,8 @@ struct TensorInfo {
   int64_t class_slot = 0;  // slot of the first view within its class
   int64_t view_slot = 0;   // global view index (sumsq)
   int64_t tile_off = 0;    // first prologue tile (tile_ss index)
-  int64_t tiles_r = 0, tiles_c = 0;
+  int64_t tiles_r = 0, tiles_c = 0;  // 32 x 128 tiles of the statistics/apply passes
+  int64_t ptiles_c = 0;              // 32 x 256 tiles of the prologue
   int64_t rowpart_off = 0, rowfac_off = 0;  // elements
   int64_t colpart_off = 0, colfac_off = 0;  // elements
   bool tall = false;
@@ -140,8 +141,9 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
     T.view_slot = class_first[T.cls] + T.class_slot;
     T.tiles_r = ceil_div(T.rows, kEwTileR);
     T.tiles_c = ceil_div(T.cols, kEwTileC);
+    T.ptiles_c = ceil_div(T.cols, kProTileC);
     T.tile_off = P.total_tiles;
-    P.total_tiles += T.views * T.tiles_r * T.tiles_c;
+    P.total_tiles += T.views * T.tiles_r * T.ptiles_c;
     T.rowpart_off = P.n_rowpart;
     T.rowfac_off = P.n_rowfac;
     T.colpart_off = P.n_colpart;
@@ -155,7 +157,7 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
   P.off_sumsq = off;
   off = align_up(off + sizeof(double) * static_cast<size_t>(P.total_views), 256);
   P.off_tile_ss = off;
-  off = align_up(off + sizeof(double) * static_cast<size_t>(P.total_tiles), 256);
+  off = align_up(off + sizeof(float) * (kEwThreads / 32) * static_cast<size_t>(P.total_tiles), 256);
   P.off_vrec = off;
   off = align_up(off + sizeof(ViewRec) * static_cast<size_t>(P.total_views), 256);
   if (need_rows) {
@@ -483,11 +485,15 @@ int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms
       J.cols = T.cols;
       J.views = T.views;
       J.tall = T.tall ? 1 : 0;
-      J.tiles_r = static_cast<int32_t>(ceil_div(T.rows, kEwTileR));
-      J.tiles_c = static_cast<int32_t>(ceil_div(T.cols, kEwTileC));
+      J.tiles_r = static_cast<int32_t>(T.tiles_r);
+      J.tiles_c = static_cast<int32_t>(kind == EW_PROLOGUE ? T.ptiles_c : T.tiles_c);
       J.tile_begin = tiles;
       tiles += static_cast<int64_t>(J.tiles_r) * J.tiles_c * T.views;
       fill(T, J);
+      if (kind == EW_PROLOGUE && (T.cols % 8) != 0) {
+        // the prologue moves 8 consecutive elements per access
+        J.src_vec = J.dst_vec = J.mom_vec = 0;
+      }
     }
     ep.total_tiles = tiles;
     double bytes = 0.0;
@@ -499,7 +505,7 @@ int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms
   return MH_OK;
 }
 
-int run_view_norm(const Plan& P, double* tile_ss, double* sumsq, cudaStream_t stream) {
+int run_view_norm(const Plan& P, float* tile_ss, double* sumsq, cudaStream_t stream) {
   for (size_t t0 = 0; t0 < P.tensors.size(); t0 += kMaxNormJobs) {
     NormParams np;
     std::memset(&np, 0, sizeof(np));
@@ -507,9 +513,9 @@ int run_view_norm(const Plan& P, double* tile_ss, double* sumsq, cudaStream_t st
     for (size_t t = t0; t < P.tensors.size() && np.njobs < kMaxNormJobs; ++t) {
       const TensorInfo& T = P.tensors[t];
       NormJob& J = np.jobs[np.njobs++];
-      J.tile_ss = tile_ss + T.tile_off;
+      J.tile_ss = tile_ss + T.tile_off * (kEwThreads / 32);
       J.sumsq = sumsq + T.view_slot;
-      J.tiles_per_view = T.tiles_r * T.tiles_c;
+      J.tiles_per_view = T.tiles_r * T.ptiles_c;
       J.views = T.views;
       J.view_begin = views;
       views += T.views;
@@ -544,6 +550,8 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
     const mh_muon_tensor& T = t[i];
     int rc = check_shape(T.views, T.rows, T.cols, i, "tensors");
     if (rc != MH_OK) return rc;
+    if (T.views * ceil_div(T.rows, kEwTileR) * ceil_div(T.cols, kEwTileC) >= (int64_t(1) << 31))
+      return fail(MH_EUNSUPPORTED, "tensors[%d]: too many elements for one tensor", i);
     if (!valid_dtype(T.param_dtype) || !valid_dtype(T.grad_dtype))
       return fail(MH_EDTYPE,
                   "tensors[%d]: only fp32 and bf16 dense tensors are supported (sparse and complex "
@@ -611,7 +619,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
 
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
-  double* tile_ss = reinterpret_cast<double*>(ws + P.off_tile_ss);
+  float* tile_ss = reinterpret_cast<float*>(ws + P.off_tile_ss);
   float* rowpart = reinterpret_cast<float*>(ws + P.off_rowpart);
   float* rowfac = reinterpret_cast<float*>(ws + P.off_rowfac);
   float* colpart = reinterpret_cast<float*>(ws + P.off_colpart);
@@ -653,7 +661,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     J.x0 = xb;
     J.xf = xb;
     J.sumsq = sumsq + T.view_slot;
-    J.tile_ss = tile_ss + T.tile_off;
+    J.tile_ss = tile_ss + T.tile_off * (kEwThreads / 32);
     J.vrec = vrec + T.view_slot;
     if (need_rows) {
       J.rowpart = rowpart + T.rowpart_off;
@@ -763,6 +771,8 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
     const mh_ns_problem& p = problems[i];
     int rc = check_shape(p.views, p.rows, p.cols, i, "problems");
     if (rc != MH_OK) return rc;
+    if (p.views * ceil_div(p.rows, kEwTileR) * ceil_div(p.cols, kEwTileC) >= (int64_t(1) << 31))
+      return fail(MH_EUNSUPPORTED, "problems[%d]: too many elements for one problem", i);
     if (!valid_dtype(p.in_dtype) || !valid_dtype(p.out_dtype))
       return fail(MH_EDTYPE, "problems[%d]: only fp32 and bf16 dense matrices are supported", i);
     if (p.views * p.rows * p.cols > 0 && (!p.x || !p.out))
@@ -780,7 +790,7 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
   cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
-  double* tile_ss = reinterpret_cast<double*>(ws + P.off_tile_ss);
+  float* tile_ss = reinterpret_cast<float*>(ws + P.off_tile_ss);
 
   EwParams proto;
   std::memset(&proto, 0, sizeof(proto));
@@ -804,7 +814,7 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
     J.x0 = xb;
     J.xf = xb;
     J.sumsq = sumsq + T.view_slot;
-    J.tile_ss = tile_ss + T.tile_off;
+    J.tile_ss = tile_ss + T.tile_off * (kEwThreads / 32);
   };
   rc = run_ew(EW_PROLOGUE, P, proto, [&](const TensorInfo& T, EwJob& J) { fill(T, J, 0); }, sms,
               stream);

@@ -23,6 +23,13 @@
 #include "muonhybrid.h"
 
 namespace mh {
+
+// Kernel parameters live in the 32 KB (32764-byte) parameter space.
+static_assert(sizeof(EwParams) <= 32000, "EwParams exceeds the kernel parameter space");
+static_assert(sizeof(RowFinParams) <= 32000, "RowFinParams exceeds the kernel parameter space");
+static_assert(sizeof(ColFinParams) <= 32000, "ColFinParams exceeds the kernel parameter space");
+static_assert(sizeof(NormParams) <= 32000, "NormParams exceeds the kernel parameter space");
+
 namespace {
 
 constexpr int kSqPad = 2;  // bf16 padding of the shared transpose tiles
@@ -164,105 +171,225 @@ __device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t,
   }
 }
 
+__device__ __forceinline__ void load8(const void* base, int dt, int64_t off, int nvalid, bool vec,
+                                      float (&o)[8]) {
+  if (vec && nvalid == 8) {
+    if (dt == MH_F32) {
+      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+      const float4 a = __ldcs(s), b = __ldcs(s + 1);
+      o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+      o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    } else {
+      const uint4 t = __ldcs(reinterpret_cast<const uint4*>(static_cast<const bf16*>(base) + off));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(h[k]);
+        o[2 * k] = f.x;
+        o[2 * k + 1] = f.y;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (k < nvalid)
+      o[k] = dt == MH_F32 ? static_cast<const float*>(base)[off + k]
+                          : __bfloat162float(static_cast<const bf16*>(base)[off + k]);
+    else
+      o[k] = 0.0f;
+  }
+}
+
+__device__ __forceinline__ void store8(void* base, int dt, int64_t off, int nvalid, bool vec,
+                                       const float (&x)[8]) {
+  if (vec && nvalid == 8) {
+    if (dt == MH_F32) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+      __stcs(d, make_float4(x[0], x[1], x[2], x[3]));
+      __stcs(d + 1, make_float4(x[4], x[5], x[6], x[7]));
+    } else {
+      uint4 t;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&t);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+      __stcs(reinterpret_cast<uint4*>(static_cast<bf16*>(base) + off), t);
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (k < nvalid) {
+      if (dt == MH_F32)
+        static_cast<float*>(base)[off + k] = x[k];
+      else
+        static_cast<bf16*>(base)[off + k] = __float2bfloat16_rn(x[k]);
+    }
+  }
+}
+
+constexpr int kProPitch = kProTileC + kSqPad;  // bf16 pitch of the transpose tile
+
+// Momentum, Nesterov lerp, ||Q||_F^2 partials and bf16(Q) in Newton-Schulz
+// orientation, over 32 x 256 tiles (each thread: 4 rows x 8 columns, all
+// loads issued before any store). Tile indices use 32-bit arithmetic (the
+// host rejects tensors with 2^31 or more tiles).
+__global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_constant__ EwParams p) {
+  __shared__ __align__(16) bf16 sQ[kEwTileR][kProPitch];
+  __shared__ __align__(16) EwJob sJ;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int cur_job = -1;
+
+  for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    const int jb = find_job(p, tile);
+    if (jb != cur_job) {  // block-uniform
+      __syncthreads();
+      constexpr int kWords = sizeof(EwJob) / 4;
+      if (threadIdx.x < kWords)
+        reinterpret_cast<uint32_t*>(&sJ)[threadIdx.x] =
+            reinterpret_cast<const uint32_t*>(&p.jobs[jb])[threadIdx.x];
+      __syncthreads();
+      cur_job = jb;
+    }
+    const EwJob& J = sJ;
+    const uint32_t local = static_cast<uint32_t>(tile - J.tile_begin);
+    const uint32_t tc_n = static_cast<uint32_t>(J.tiles_c);
+    const uint32_t per_view = static_cast<uint32_t>(J.tiles_r) * tc_n;
+    const uint32_t v32 = local / per_view;
+    const uint32_t w = local - v32 * per_view;
+    const uint32_t trow = w / tc_n;
+    const int64_t v = v32;
+    const int64_t r0 = static_cast<int64_t>(trow) * kEwTileR;
+    const int64_t c0 = static_cast<int64_t>(w - trow * tc_n) * kProTileC;
+    const int64_t view_elem0 = v * J.rows * J.cols;
+    const int64_t col = c0 + lane * 8;
+    const int64_t ncol = J.cols - col;
+    const int nvalid = ncol >= 8 ? 8 : (ncol > 0 ? static_cast<int>(ncol) : 0);
+
+    if (J.vrec != nullptr && threadIdx.x == 0 && r0 == 0 && c0 == 0) {
+      ViewRec rec;
+      rec.param = J.dst;
+      rec.grad = J.src;
+      rec.elem0 = view_elem0;
+      rec.rows = J.rows;
+      rec.cols = J.cols;
+      rec.lr = J.lr;
+      rec.wd = J.wd;
+      rec.shape_scale = J.shape_scale;
+      rec.pdt = J.dst_dtype;
+      rec.gdt = J.src_dtype;
+      rec.tall = J.tall;
+      rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
+      J.vrec[v] = rec;
+    }
+
+    bf16* xv = J.x0 + v * J.x_view_stride;
+    float g[4][8], b[4][8];
+    bool ok[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + warp * 4 + i;
+      ok[i] = row < J.rows && nvalid > 0;
+      if (ok[i]) {
+        const int64_t off = view_elem0 + row * J.cols + col;
+        load8(J.src, J.src_dtype, off, nvalid, J.src_vec, g[i]);
+        if (p.use_momentum) load8(J.mom, MH_F32, off, nvalid, J.mom_vec, b[i]);
+      }
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (!ok[i]) continue;
+      const int lr = warp * 4 + i;
+      const int64_t row = r0 + lr;
+      const int64_t off = view_elem0 + row * J.cols + col;
+      float q[8];
+      if (p.use_momentum) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          b[i][k] = p.mu * b[i][k] + (1.0f - p.mu) * g[i][k];
+          q[k] = p.nesterov ? g[i][k] + p.mu * (b[i][k] - g[i][k]) : b[i][k];
+        }
+        store8(J.mom, MH_F32, off, nvalid, J.mom_vec, b[i]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = g[i][k];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss += q[k] * q[k];  // q[k] == 0 beyond nvalid
+      if (!J.tall) {
+        store8(xv + row * J.ldx, MH_BF16, col, nvalid, true, q);
+      } else {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sQ[lr][lane * 8]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(q[2 * k], q[2 * k + 1]);
+          dst[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      }
+    }
+    // ||Q||_F^2 of this warp's 4 x 256 block: one partial per warp, summed in
+    // a fixed order by the view-norm kernel, so wide tiles need no block-wide
+    // barrier.
+    ss = warp_sum(ss);
+    if (lane == 0) J.tile_ss[static_cast<int64_t>(local) * (kEwThreads / 32) + warp] = ss;
+    if (J.tall) {
+      __syncthreads();
+      // Write the transpose: X row = stored col c0 + cc, X cols = stored rows.
+#pragma unroll
+      for (int rep = 0; rep < 4; ++rep) {
+        const int task = threadIdx.x + rep * kEwThreads;
+        const int cc = task >> 2, seg = task & 3;
+        const int64_t xr = c0 + cc;
+        const int64_t xc0 = r0 + seg * 8;
+        if (xr >= J.cols) continue;
+        bf16* dst = xv + xr * J.ldx + xc0;
+        const int64_t nval = J.rows - xc0;
+        if (nval >= 8) {
+          uint4 q;
+          bf16* h = reinterpret_cast<bf16*>(&q);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) h[k] = sQ[seg * 8 + k][cc];
+          *reinterpret_cast<uint4*>(dst) = q;
+        } else {
+          for (int k = 0; k < nval; ++k) dst[k] = sQ[seg * 8 + k][cc];
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ EwParams p) {
-  __shared__ __align__(16) bf16 sQ[kEwTileR][kEwTileC + kSqPad];     // prologue, tall
   __shared__ __align__(16) bf16 sU[kEwTileC][kEwTileR + kSqPad];     // U loads, tall
   __shared__ float sRed[kEwThreads / 32][kEwTileC];
+  // The tile's job record, copied once per tile from the parameter space:
+  // indexing a large parameter table per access would keep missing the small
+  // constant cache.
+  __shared__ __align__(16) EwJob sJ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int cur_job = -1;
 
   for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
     const TileInfo t = tile_info(p, tile);
-    const EwJob& J = p.jobs[t.job];
+    if (t.job != cur_job) {  // block-uniform
+      __syncthreads();
+      constexpr int kWords = sizeof(EwJob) / 4;
+      static_assert(sizeof(EwJob) % 4 == 0, "EwJob must be a whole number of words");
+      if (threadIdx.x < kWords)
+        reinterpret_cast<uint32_t*>(&sJ)[threadIdx.x] =
+            reinterpret_cast<const uint32_t*>(&p.jobs[t.job])[threadIdx.x];
+      __syncthreads();
+      cur_job = t.job;
+    }
+    const EwJob& J = sJ;
     const int64_t view_elem0 = t.v * J.rows * J.cols;
     const int64_t col = t.c0 + lane * 4;
     const int64_t ncol = J.cols - col;
     const int nvalid = ncol >= 4 ? 4 : (ncol > 0 ? static_cast<int>(ncol) : 0);
 
-    if constexpr (KIND == EW_PROLOGUE) {
-      if (J.vrec != nullptr && threadIdx.x == 0 && t.r0 == 0 && t.c0 == 0) {
-        ViewRec rec;
-        rec.param = J.dst;
-        rec.grad = J.src;
-        rec.elem0 = view_elem0;
-        rec.rows = J.rows;
-        rec.cols = J.cols;
-        rec.lr = J.lr;
-        rec.wd = J.wd;
-        rec.shape_scale = J.shape_scale;
-        rec.pdt = J.dst_dtype;
-        rec.gdt = J.src_dtype;
-        rec.tall = J.tall;
-        rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
-        J.vrec[t.v] = rec;
-      }
-      float ss = 0.0f;
-      bf16* xv = J.x0 + t.v * J.x_view_stride;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int lr = warp * 4 + i;
-        const int64_t row = t.r0 + lr;
-        if (row >= J.rows || nvalid == 0) continue;
-        const int64_t off = view_elem0 + row * J.cols + col;
-        float g[4], q[4];
-        load4(J.src, J.src_dtype, off, nvalid, J.src_vec, g);
-        if (p.use_momentum) {
-          float b[4];
-          load4(J.mom, MH_F32, off, nvalid, J.mom_vec, b);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            b[k] = p.mu * b[k] + (1.0f - p.mu) * g[k];
-            q[k] = p.nesterov ? g[k] + p.mu * (b[k] - g[k]) : b[k];
-          }
-          store4(J.mom, MH_F32, off, nvalid, J.mom_vec, b);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) q[k] = g[k];
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ss += q[k] * q[k];  // q[k] == 0 beyond nvalid
-        if (!J.tall) {
-          store4(xv + row * J.ldx, MH_BF16, col, nvalid, true, q);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) sQ[lr][lane * 4 + k] = __float2bfloat16_rn(q[k]);
-        }
-      }
-      // ||Q||_F^2 of this tile, summed in a fixed order; the per-view total
-      // is formed from these partials by the view-norm kernel.
-      ss = warp_sum(ss);
-      if (lane == 0) sRed[warp][0] = ss;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        double tot = 0.0;
-#pragma unroll
-        for (int w = 0; w < kEwThreads / 32; ++w) tot += static_cast<double>(sRed[w][0]);
-        J.tile_ss[tile - J.tile_begin] = tot;
-      }
-      if (J.tall) {
-        // Write the transpose: X row = stored col (c0+cc), X cols = stored rows.
-#pragma unroll
-        for (int rep = 0; rep < 2; ++rep) {
-          const int task = threadIdx.x + rep * kEwThreads;
-          const int cc = task >> 2, seg = task & 3;
-          const int64_t xr = t.c0 + cc;
-          const int64_t xc0 = t.r0 + seg * 8;
-          if (xr >= J.cols) continue;
-          bf16* dst = xv + xr * J.ldx + xc0;
-          const int64_t nval = J.rows - xc0;
-          if (nval >= 8) {
-            uint4 q;
-            bf16* h = reinterpret_cast<bf16*>(&q);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] = sQ[seg * 8 + k][cc];
-            *reinterpret_cast<uint4*>(dst) = q;
-          } else {
-            for (int k = 0; k < nval; ++k) dst[k] = sQ[seg * 8 + k][cc];
-          }
-        }
-      }
-      __syncthreads();
-    } else {
+    {
       float u[4][4];
       load_u_block(J, t, sU, u);
 
@@ -435,13 +562,11 @@ __global__ void __launch_bounds__(256) col_finalize_kernel(const __grid_constant
   }
 }
 
-// One warp per view: ||Q||_F^2 = sum of the view's per-tile partials, each
-// lane summing a fixed stride of tiles, then a fixed butterfly.
+// One block per view: ||Q||_F^2 = the sum of the view's per-warp partials,
+// each thread summing a fixed stride of them, then a fixed-order tree.
 __global__ void __launch_bounds__(256) view_norm_kernel(const __grid_constant__ NormParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_global = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t vv = warp_global; vv < p.total_views; vv += nwarps) {
+  __shared__ double red[256];
+  for (int64_t vv = blockIdx.x; vv < p.total_views; vv += gridDim.x) {
     int lo = 0, hi = p.njobs - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -449,12 +574,19 @@ __global__ void __launch_bounds__(256) view_norm_kernel(const __grid_constant__ 
     }
     const NormJob& J = p.jobs[lo];
     const int64_t v = vv - J.view_begin;
-    const double* part = J.tile_ss + v * J.tiles_per_view;
+    const int64_t n = J.tiles_per_view * (kEwThreads / 32);
+    const float* part = J.tile_ss + v * n;
     double s = 0.0;
-    for (int64_t k = lane; k < J.tiles_per_view; k += 32) s += part[k];
+    for (int64_t k = threadIdx.x; k < n; k += 256) s += static_cast<double>(part[k]);
+    red[threadIdx.x] = s;
+    __syncthreads();
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) J.sumsq[v] = s;
+    for (int w = 128; w > 0; w >>= 1) {
+      if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) J.sumsq[v] = red[0];
+    __syncthreads();
   }
 }
 
@@ -470,17 +602,42 @@ cudaError_t launch_col_finalize(const ColFinParams& p, int num_sms, cudaStream_t
 
 cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s) {
   if (p.total_views <= 0) return cudaSuccess;
-  const int64_t blocks = (p.total_views + 7) / 8;
-  view_norm_kernel<<<static_cast<int>(blocks < 1024 ? blocks : 1024), 256, 0, s>>>(p);
+  const int64_t blocks = p.total_views;
+  view_norm_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+// Resident blocks per SM of each elementwise kernel (queried once per kind),
+// so that the persistent grids are exactly one wave.
+int blocks_per_sm(EwKind kind, const void* kernel) {
+  static int cached[5] = {0, 0, 0, 0, 0};
+  if (cached[kind] == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kEwThreads, 0) != cudaSuccess ||
+        b <= 0) {
+      (void)cudaGetLastError();
+      b = 2;
+    }
+    cached[kind] = b;
+  }
+  return cached[kind];
 }
 
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  const int64_t want = static_cast<int64_t>(num_sms) * 4;
+  const void* fn = nullptr;
+  switch (kind) {
+    case EW_PROLOGUE: fn = reinterpret_cast<const void*>(prologue_kernel); break;
+    case EW_ROWSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_ROWSQ>); break;
+    case EW_COLSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_COLSQ>); break;
+    case EW_APPLY: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY>); break;
+    case EW_COPYOUT: fn = reinterpret_cast<const void*>(ew_kernel<EW_COPYOUT>); break;
+  }
+  const int per_sm = blocks_per_sm(kind, fn);
+  const int64_t want = static_cast<int64_t>(num_sms) * per_sm;
   const int grid = static_cast<int>(p.total_tiles < want ? p.total_tiles : want);
   switch (kind) {
-    case EW_PROLOGUE: ew_kernel<EW_PROLOGUE><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_PROLOGUE: prologue_kernel<<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;

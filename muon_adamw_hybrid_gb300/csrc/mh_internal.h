@@ -21,8 +21,9 @@ typedef __nv_bfloat16 bf16;
 // ---------------------------------------------------------------------------
 constexpr int kEwTileR = 32;   // tile rows (stored orientation)
 constexpr int kEwTileC = 128;  // tile cols (stored orientation)
+constexpr int kProTileC = 256; // prologue tile cols: 8 per lane
 constexpr int kEwThreads = 256;
-constexpr int kMaxJobs = 40;   // tensors per elementwise launch (param space)
+constexpr int kMaxJobs = 64;   // tensors per elementwise launch (param space)
 
 // Per-view record written by the prologue and read by the final Newton-Schulz
 // apply when it applies the parameter update itself (no NorMuon / Muon+).
@@ -42,7 +43,7 @@ struct EwJob {
   float* mom;            // Muon momentum (fp32), null for NS only
   void* dst;             // apply: parameter; copy-out: NS output
   float* sm;             // NorMuon second moment (views*rows)
-  double* tile_ss;       // per prologue tile: partial ||Q||^2 (this tensor's first tile)
+  float* tile_ss;        // per prologue tile and warp: partial ||Q||^2 (this tensor's first)
   float* rowpart;        // [views][tiles_c][rows] partial row sums of U^2
   float* colpart;        // [views][tiles_r][cols] partial col sums of (f U)^2
   float* rowfac;         // [views][rows] final row factor
@@ -115,7 +116,7 @@ struct ColFinParams {
 
 // Per-view ||Q||_F^2 from the prologue's per-tile partials, one warp per view.
 struct NormJob {
-  const double* tile_ss;  // this tensor's first tile partial
+  const float* tile_ss;   // this tensor's first per-warp partial
   double* sumsq;          // this tensor's first view
   int64_t tiles_per_view, views;
   int64_t view_begin;

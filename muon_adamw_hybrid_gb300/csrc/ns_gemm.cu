@@ -43,6 +43,9 @@
 #include "muonhybrid.h"
 
 namespace mh {
+
+static_assert(sizeof(GemmParams) <= 32000, "GemmParams exceeds the kernel parameter space");
+
 namespace {
 
 constexpr uint32_t kStageABytes = kBM * kBK * 2;  // 16 KB
