@@ -63,6 +63,44 @@ def parse_args():
     return ap.parse_args()
 
 
+# Kernel family -> the sources that define it. A DRAM-traffic record in
+# profiles/ is used only while these files still hash to the digest it was
+# taken on; once a kernel changes, its traffic is reported as null.
+KERNEL_SOURCES = {
+    "ns_gemm": ["ns_gemm.cu", "mh_ptx.cuh", "mh_internal.h"],
+    "muon_prologue": ["elementwise.cu", "mh_internal.h"],
+    "adamw": ["adamw.cu", "mh_internal.h"],
+}
+
+
+def sources_digest(family: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(family, []):
+        with open(os.path.join(ROOT, "muon_adamw_hybrid_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_records(workload: str) -> dict:
+    """bytes_per_launch of each kernel family from `traffic-record:` lines of
+    profiles/dram_<workload>.md, kept only if the sources still match."""
+    path = os.path.join(ROOT, "profiles", f"dram_{workload}.md")
+    out = {}
+    try:
+        with open(path) as f:
+            for line in f:
+                if not line.startswith("traffic-record:"):
+                    continue
+                kv = dict(tok.split("=", 1) for tok in line.split()[1:])
+                fam = kv["kernel"]
+                if fam in KERNEL_SOURCES and kv.get("sources") == sources_digest(fam):
+                    out[fam] = float(kv["bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return out
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -570,6 +608,7 @@ def main():
             kernels[name]["tflops_executed"] = round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)
         if v["bytes"] > 0:
             kernels[name]["gbs"] = round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1)
+    traffic = traffic_records(args.workload)
     roofline = None
     if kstats:
         top = max(kstats, key=lambda k: kstats[k]["total_ms"])
@@ -578,16 +617,19 @@ def main():
             peak = peaks["bf16_tflops_sustained"]
             ach = v["flops"] / (v["total_ms"] * 1e-3) / 1e12
             roofline = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
-                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                        "traffic": traffic.get(top),
                         "peak_source": f"bf16 sustained, of {peak_src}",
                         "achieved_basis": "nominal NS FLOPs (2m^2n gram, 2m^3 poly, 2m^2n apply "
                                           "per view) / event time",
-                        "executed_tflops": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)}
+                        "executed_tflops": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1),
+                        "executed_frac": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12 / peak, 4),
+                        "traffic_unit": "DRAM bytes per launch (ncu, profiles/)"}
         else:
             peak = peaks["hbm_gbs"]
             ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
             roofline = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
-                        "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic.get(top),
                         "peak_source": f"HBM copy, of {peak_src}"}
     hbm = {k: v for k, v in kstats.items() if v["flops"] == 0 and v["bytes"] > 0}
     roofline_hbm = None
@@ -597,7 +639,8 @@ def main():
         ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
         roofline_hbm = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                        "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic.get(top),
+                        "algorithmic_bytes_per_launch": hbm[top]["bytes"] / max(hbm[top]["launches"], 1),
                         "peak_source": f"HBM copy, of {peak_src}"}
     stages = {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
                   "tflops_executed": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)}
