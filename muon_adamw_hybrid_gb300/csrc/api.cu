@@ -79,6 +79,8 @@ struct TensorInfo {
   int64_t tile_off = 0;    // first prologue tile (tile_ss index)
   int64_t tiles_r = 0, tiles_c = 0;  // 32 x 128 tiles of the statistics/apply passes
   int64_t ptiles_c = 0;              // 32 x 256 tiles of the prologue
+  bool flat = false;                 // prologue streams the view as contiguous chunks
+  int64_t pro_tiles_per_view = 0;    // prologue work items per view
   int64_t rowpart_off = 0, rowfac_off = 0;  // elements
   int64_t colpart_off = 0, colfac_off = 0;  // elements
   bool tall = false;
@@ -142,8 +144,12 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
     T.tiles_r = ceil_div(T.rows, kEwTileR);
     T.tiles_c = ceil_div(T.cols, kEwTileC);
     T.ptiles_c = ceil_div(T.cols, kProTileC);
+    // A wide view whose row pitch in X equals its cols is laid out exactly as
+    // stored: the prologue streams it in contiguous chunks.
+    T.flat = !T.tall && (T.cols % 8) == 0;
+    T.pro_tiles_per_view = T.flat ? ceil_div(T.rows * T.cols, kProChunk) : T.tiles_r * T.ptiles_c;
     T.tile_off = P.total_tiles;
-    P.total_tiles += T.views * T.tiles_r * T.ptiles_c;
+    P.total_tiles += T.views * T.pro_tiles_per_view;
     T.rowpart_off = P.n_rowpart;
     T.rowfac_off = P.n_rowfac;
     T.colpart_off = P.n_colpart;
@@ -444,6 +450,7 @@ double ew_bytes(EwKind kind, const EwParams& p, const EwJob& J) {
   const double e = double(J.rows) * J.cols * J.views;
   switch (kind) {
     case EW_PROLOGUE:
+    case EW_PROLOGUE_FLAT:
       return e * (dsize(J.src_dtype) + (p.use_momentum ? 8.0 : 0.0) + 2.0);
     case EW_ROWSQ:
       return e * 2.0;
@@ -460,7 +467,8 @@ double ew_bytes(EwKind kind, const EwParams& p, const EwJob& J) {
 
 const char* ew_name(EwKind kind, bool muon) {
   switch (kind) {
-    case EW_PROLOGUE: return muon ? "muon_prologue" : "ns_prologue";
+    case EW_PROLOGUE:
+    case EW_PROLOGUE_FLAT: return muon ? "muon_prologue" : "ns_prologue";
     case EW_ROWSQ: return "muon_rowstats";
     case EW_COLSQ: return "muon_colstats";
     case EW_APPLY: return "muon_apply";
@@ -469,16 +477,19 @@ const char* ew_name(EwKind kind, bool muon) {
   return "elementwise";
 }
 
-template <typename Fill>
-int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms,
-           cudaStream_t stream) {
-  const size_t nt = P.tensors.size();
+template <typename Fill, typename Sel>
+int run_ew_sel(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms,
+               cudaStream_t stream, Sel sel) {
+  std::vector<size_t> idx;
+  for (size_t t = 0; t < P.tensors.size(); ++t)
+    if (sel(P.tensors[t])) idx.push_back(t);
+  const size_t nt = idx.size();
   for (size_t t0 = 0; t0 < nt; t0 += kMaxJobs) {
     EwParams ep = proto;
     ep.njobs = 0;
     int64_t tiles = 0;
-    for (size_t t = t0; t < nt && ep.njobs < kMaxJobs; ++t) {
-      const TensorInfo& T = P.tensors[t];
+    for (size_t q = t0; q < nt && ep.njobs < kMaxJobs; ++q) {
+      const TensorInfo& T = P.tensors[idx[q]];
       EwJob& J = ep.jobs[ep.njobs++];
       std::memset(&J, 0, sizeof(J));
       J.rows = T.rows;
@@ -486,11 +497,16 @@ int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms
       J.views = T.views;
       J.tall = T.tall ? 1 : 0;
       J.tiles_r = static_cast<int32_t>(T.tiles_r);
-      J.tiles_c = static_cast<int32_t>(kind == EW_PROLOGUE ? T.ptiles_c : T.tiles_c);
+      J.tiles_c = static_cast<int32_t>(T.tiles_c);
+      if (kind == EW_PROLOGUE || kind == EW_PROLOGUE_FLAT) {
+        J.flat = T.flat ? 1 : 0;
+        J.tiles_r = T.flat ? 1 : static_cast<int32_t>(T.tiles_r);
+        J.tiles_c = static_cast<int32_t>(T.flat ? T.pro_tiles_per_view : T.ptiles_c);
+      }
       J.tile_begin = tiles;
       tiles += static_cast<int64_t>(J.tiles_r) * J.tiles_c * T.views;
       fill(T, J);
-      if (kind == EW_PROLOGUE && (T.cols % 8) != 0) {
+      if ((kind == EW_PROLOGUE || kind == EW_PROLOGUE_FLAT) && (T.cols % 8) != 0) {
         // the prologue moves 8 consecutive elements per access
         J.src_vec = J.dst_vec = J.mom_vec = 0;
       }
@@ -505,6 +521,20 @@ int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms
   return MH_OK;
 }
 
+template <typename Fill>
+int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms,
+           cudaStream_t stream) {
+  if (kind == EW_PROLOGUE) {
+    // Wide views stored like X are streamed by their own kernel.
+    int rc = run_ew_sel(EW_PROLOGUE_FLAT, P, proto, fill, sms, stream,
+                        [](const TensorInfo& T) { return T.flat; });
+    if (rc != MH_OK) return rc;
+    return run_ew_sel(EW_PROLOGUE, P, proto, fill, sms, stream,
+                      [](const TensorInfo& T) { return !T.flat; });
+  }
+  return run_ew_sel(kind, P, proto, fill, sms, stream, [](const TensorInfo&) { return true; });
+}
+
 int run_view_norm(const Plan& P, float* tile_ss, double* sumsq, cudaStream_t stream) {
   for (size_t t0 = 0; t0 < P.tensors.size(); t0 += kMaxNormJobs) {
     NormParams np;
@@ -515,7 +545,7 @@ int run_view_norm(const Plan& P, float* tile_ss, double* sumsq, cudaStream_t str
       NormJob& J = np.jobs[np.njobs++];
       J.tile_ss = tile_ss + T.tile_off * (kEwThreads / 32);
       J.sumsq = sumsq + T.view_slot;
-      J.tiles_per_view = T.tiles_r * T.ptiles_c;
+      J.tiles_per_view = T.pro_tiles_per_view;
       J.views = T.views;
       J.view_begin = views;
       views += T.views;

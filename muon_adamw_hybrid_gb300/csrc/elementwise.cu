@@ -230,6 +230,83 @@ __device__ __forceinline__ void store8(void* base, int dt, int64_t off, int nval
 
 constexpr int kProPitch = kProTileC + kSqPad;  // bf16 pitch of the transpose tile
 
+// Prologue of wide views whose X layout equals their stored layout (cols a
+// multiple of 8): a plain contiguous stream, like AdamW. One work item is a
+// kProChunk-element chunk of one view; each thread handles 8 consecutive
+// elements per step, the block 2048 per step, four steps per chunk. One
+// ||Q||_F^2 partial per warp and chunk.
+__global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __grid_constant__ EwParams p) {
+  __shared__ __align__(16) EwJob sJ;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int cur_job = -1;
+  for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    const int jb = find_job(p, tile);
+    if (jb != cur_job) {  // block-uniform
+      __syncthreads();
+      constexpr int kWords = sizeof(EwJob) / 4;
+      if (threadIdx.x < kWords)
+        reinterpret_cast<uint32_t*>(&sJ)[threadIdx.x] =
+            reinterpret_cast<const uint32_t*>(&p.jobs[jb])[threadIdx.x];
+      __syncthreads();
+      cur_job = jb;
+    }
+    const EwJob& J = sJ;
+    const uint32_t local = static_cast<uint32_t>(tile - J.tile_begin);
+    const uint32_t per_view = static_cast<uint32_t>(J.tiles_c);
+    const uint32_t v32 = local / per_view;
+    const int64_t v = v32;
+    const int64_t w = local - v32 * per_view;
+    const int64_t view_elem0 = v * J.rows * J.cols;
+    const int64_t vsz = J.rows * J.cols;
+    const int64_t base = w * kProChunk;
+    if (J.vrec != nullptr && threadIdx.x == 0 && w == 0) {
+      ViewRec rec;
+      rec.param = J.dst;
+      rec.grad = J.src;
+      rec.elem0 = view_elem0;
+      rec.rows = J.rows;
+      rec.cols = J.cols;
+      rec.lr = J.lr;
+      rec.wd = J.wd;
+      rec.shape_scale = J.shape_scale;
+      rec.pdt = J.dst_dtype;
+      rec.gdt = J.src_dtype;
+      rec.tall = J.tall;
+      rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
+      J.vrec[v] = rec;
+    }
+    bf16* xv = J.x0 + v * J.x_view_stride;
+    float ss = 0.0f;
+#pragma unroll 1
+    for (int i = 0; i < kProChunk / (8 * kEwThreads); ++i) {
+      const int64_t off = base + i * (8 * kEwThreads) + warp * 256 + lane * 8;
+      const int64_t rem = vsz - off;
+      const int nv = rem >= 8 ? 8 : (rem > 0 ? static_cast<int>(rem) : 0);
+      if (nv == 0) continue;
+      float g[8], q[8];
+      load8(J.src, J.src_dtype, view_elem0 + off, nv, J.src_vec, g);
+      if (p.use_momentum) {
+        float b[8];
+        load8(J.mom, MH_F32, view_elem0 + off, nv, J.mom_vec, b);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          b[k] = p.mu * b[k] + (1.0f - p.mu) * g[k];
+          q[k] = p.nesterov ? g[k] + p.mu * (b[k] - g[k]) : b[k];
+        }
+        store8(J.mom, MH_F32, view_elem0 + off, nv, J.mom_vec, b);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = g[k];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss += q[k] * q[k];  // q[k] == 0 beyond nv
+      store8(xv, MH_BF16, off, nv, true, q);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) J.tile_ss[static_cast<int64_t>(local) * (kEwThreads / 32) + warp] = ss;
+  }
+}
+
 // Momentum, Nesterov lerp, ||Q||_F^2 partials and bf16(Q) in Newton-Schulz
 // orientation, over 32 x 256 tiles (each thread: 4 rows x 8 columns, all
 // loads issued before any store). Tile indices use 32-bit arithmetic (the
@@ -257,11 +334,12 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
     const uint32_t per_view = static_cast<uint32_t>(J.tiles_r) * tc_n;
     const uint32_t v32 = local / per_view;
     const uint32_t w = local - v32 * per_view;
-    const uint32_t trow = w / tc_n;
     const int64_t v = v32;
+    const int64_t view_elem0 = v * J.rows * J.cols;
+
+    const uint32_t trow = w / tc_n;
     const int64_t r0 = static_cast<int64_t>(trow) * kEwTileR;
     const int64_t c0 = static_cast<int64_t>(w - trow * tc_n) * kProTileC;
-    const int64_t view_elem0 = v * J.rows * J.cols;
     const int64_t col = c0 + lane * 8;
     const int64_t ncol = J.cols - col;
     const int nvalid = ncol >= 8 ? 8 : (ncol > 0 ? static_cast<int>(ncol) : 0);
@@ -610,7 +688,7 @@ cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s) {
 // Resident blocks per SM of each elementwise kernel (queried once per kind),
 // so that the persistent grids are exactly one wave.
 int blocks_per_sm(EwKind kind, const void* kernel) {
-  static int cached[5] = {0, 0, 0, 0, 0};
+  static int cached[6] = {0, 0, 0, 0, 0, 0};
   if (cached[kind] == 0) {
     int b = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kEwThreads, 0) != cudaSuccess ||
@@ -628,6 +706,7 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
   const void* fn = nullptr;
   switch (kind) {
     case EW_PROLOGUE: fn = reinterpret_cast<const void*>(prologue_kernel); break;
+    case EW_PROLOGUE_FLAT: fn = reinterpret_cast<const void*>(prologue_flat_kernel); break;
     case EW_ROWSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_ROWSQ>); break;
     case EW_COLSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_COLSQ>); break;
     case EW_APPLY: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY>); break;
@@ -638,6 +717,7 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
   const int grid = static_cast<int>(p.total_tiles < want ? p.total_tiles : want);
   switch (kind) {
     case EW_PROLOGUE: prologue_kernel<<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_PROLOGUE_FLAT: prologue_flat_kernel<<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;

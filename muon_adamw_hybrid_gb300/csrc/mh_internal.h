@@ -22,6 +22,7 @@ typedef __nv_bfloat16 bf16;
 constexpr int kEwTileR = 32;   // tile rows (stored orientation)
 constexpr int kEwTileC = 128;  // tile cols (stored orientation)
 constexpr int kProTileC = 256; // prologue tile cols: 8 per lane
+constexpr int kProChunk = 8192;  // prologue chunk of a flat (wide) view: 32 per thread
 constexpr int kEwThreads = 256;
 constexpr int kMaxJobs = 64;   // tensors per elementwise launch (param space)
 
@@ -58,6 +59,8 @@ struct EwJob {
   int64_t tile_begin;    // first global tile index of this tensor
   int32_t tiles_r, tiles_c;
   int32_t tall;          // rows > cols: X holds the transpose
+  int32_t flat;          // prologue: wide view stored like X (cols % 8 == 0): streamed
+                         // as contiguous kProChunk-element chunks, tiles_r = 1
   int32_t src_dtype, dst_dtype;
   int32_t src_vec, dst_vec, mom_vec;  // 16-byte aligned and cols % 4 == 0
   float lr, wd, shape_scale;
@@ -77,7 +80,14 @@ struct EwParams {
   int32_t u_scale_from_sumsq;  // ns_steps == 0: U = X0 / (||Q|| + eps)
 };
 
-enum EwKind { EW_PROLOGUE = 0, EW_ROWSQ = 1, EW_COLSQ = 2, EW_APPLY = 3, EW_COPYOUT = 4 };
+enum EwKind {
+  EW_PROLOGUE = 0,       // transposing 32 x 256 tiles (tall views, ragged wide views)
+  EW_ROWSQ = 1,
+  EW_COLSQ = 2,
+  EW_APPLY = 3,
+  EW_COPYOUT = 4,
+  EW_PROLOGUE_FLAT = 5   // contiguous chunks (wide views with cols % 8 == 0)
+};
 
 // Row finalisation (NorMuon state, NorMuon norm restore, Muon+ row factor):
 // one CTA per view. Every reduction sums per-tile partials in a fixed order,
