@@ -4,10 +4,12 @@
 // include/muonhybrid.h.
 //
 // Plan. Every view is a Newton-Schulz problem of size m x n (m = min(rows,
-// cols), n = max(rows, cols); tall views, rows > cols, are transposed by the
-// prologue as the Speedtronic "Newton-Schulz" section prescribes). Views with
-// the same (m, n) form a shape class whose buffers are stacked in the
-// workspace, so one 3-D tensor map covers a whole class and one grouped
+// cols), n = max(rows, cols)); for a tall view (rows > cols) the iteration
+// runs on the transpose, as the Speedtronic "Newton-Schulz" section
+// prescribes. No data is transposed: a tall view's X is kept in its stored
+// (n x m) layout and the GEMM stages read it with transposed operands. Views
+// with the same (m, n, tall) form a shape class whose buffers are stacked in
+// the workspace, so one 3-D tensor map covers a whole class and one grouped
 // launch per Newton-Schulz stage covers every class.
 //
 // Workspace (256-byte aligned base):
@@ -20,7 +22,8 @@
 //   rowfac          float per (view, stored row)                 (NorMuon / Muon+)
 //   colpart         float per (view, row tile, stored col)       (Muon+)
 //   colfac          float per (view, stored col)                 (Muon+)
-//   per class       X0, X1 (bf16, m x ldx per view), A, P (bf16, m x lda)
+//   per class       X0, X1 (bf16, per view m x ldx, or n x ldx for tall views),
+//                   A, P (bf16, m x lda)
 // Every reduction is a sum of per-tile partials taken in a fixed order, so a
 // step's results do not depend on scheduling.
 #include <cmath>
@@ -67,6 +70,8 @@ bool valid_dtype(int32_t d) { return d == MH_F32 || d == MH_BF16; }
 
 struct ClassInfo {
   int64_t m = 0, n = 0, ldx = 0, lda = 0, count = 0;
+  bool tstore = false;       // X kept in the stored (n x m) layout of tall views
+  int64_t xrows = 0;         // rows of one view's X buffer: m, or n when tstore
   size_t off_x[2] = {0, 0}, off_a = 0, off_p = 0;
 };
 
@@ -103,7 +108,7 @@ struct Shape {
 // Groups views by Newton-Schulz shape and lays out the workspace.
 Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols) {
   Plan P;
-  std::map<std::pair<int64_t, int64_t>, int> cls_of;
+  std::map<std::pair<std::pair<int64_t, int64_t>, bool>, int> cls_of;
   for (size_t i = 0; i < shapes.size(); ++i) {
     const Shape& s = shapes[i];
     if (s.views == 0 || s.rows == 0 || s.cols == 0) continue;
@@ -115,13 +120,16 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
     T.tall = s.rows > s.cols;
     const int64_t m = T.tall ? s.cols : s.rows;
     const int64_t n = T.tall ? s.rows : s.cols;
-    auto key = std::make_pair(m, n);
+    // Tall views keep X in their stored layout; the GEMMs read it transposed.
+    auto key = std::make_pair(std::make_pair(m, n), T.tall);
     auto it = cls_of.find(key);
     if (it == cls_of.end()) {
       ClassInfo C;
       C.m = m;
       C.n = n;
-      C.ldx = (n + 7) / 8 * 8;
+      C.tstore = T.tall;
+      C.xrows = T.tall ? n : m;
+      C.ldx = ((T.tall ? m : n) + 7) / 8 * 8;
       C.lda = (m + 7) / 8 * 8;
       it = cls_of.emplace(key, static_cast<int>(P.classes.size())).first;
       P.classes.push_back(C);
@@ -144,9 +152,9 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
     T.tiles_r = ceil_div(T.rows, kEwTileR);
     T.tiles_c = ceil_div(T.cols, kEwTileC);
     T.ptiles_c = ceil_div(T.cols, kProTileC);
-    // A wide view whose row pitch in X equals its cols is laid out exactly as
-    // stored: the prologue streams it in contiguous chunks.
-    T.flat = !T.tall && (T.cols % 8) == 0;
+    // X holds every view in its stored layout; when the row pitch equals the
+    // stored cols the prologue streams the view in contiguous chunks.
+    T.flat = (T.cols % 8) == 0;
     T.pro_tiles_per_view = T.flat ? ceil_div(T.rows * T.cols, kProChunk) : T.tiles_r * T.ptiles_c;
     T.tile_off = P.total_tiles;
     P.total_tiles += T.views * T.pro_tiles_per_view;
@@ -180,7 +188,7 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
   }
   off = align_up(off, 1024);
   for (ClassInfo& C : P.classes) {
-    const size_t xb = static_cast<size_t>(C.count) * C.m * C.ldx * sizeof(bf16);
+    const size_t xb = static_cast<size_t>(C.count) * C.xrows * C.ldx * sizeof(bf16);
     const size_t ab = static_cast<size_t>(C.count) * C.m * C.lda * sizeof(bf16);
     C.off_x[0] = off; off = align_up(off + xb, 1024);
     C.off_x[1] = off; off = align_up(off + xb, 1024);
@@ -343,96 +351,120 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
 
   for (int it = 0; it < steps; ++it) {
     for (int kind = GEMM_GRAM; kind <= GEMM_APPLY; ++kind) {
-      for (int c0 = 0; c0 < nclass; c0 += kMaxClasses) {
-        GemmParams gp;
-        std::memset(&gp, 0, sizeof(gp));
-        gp.kind = kind;
-        gp.first_iter = it == 0 ? 1 : 0;
-        gp.a = a;
-        gp.b = b;
-        gp.c = c;
-        gp.eps = eps;
-        gp.status = status;
-        const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
-        gp.final_update = fused ? 1 : 0;
-        gp.cautious = cautious;
-        int64_t tiles = 0;
-        int nc = 0;
-        for (int k = c0; k < nclass && nc < kMaxClasses; ++k, ++nc) {
-          const ClassInfo& C = P.classes[k];
-          GemmClass& G = gp.cls[nc];
-          bf16* X = reinterpret_cast<bf16*>(ws + C.off_x[cur]);
-          bf16* Xn = reinterpret_cast<bf16*>(ws + C.off_x[cur ^ 1]);
-          bf16* A = reinterpret_cast<bf16*>(ws + C.off_a);
-          bf16* Pm = reinterpret_cast<bf16*>(ws + C.off_p);
-          G.m = static_cast<int32_t>(C.m);
-          G.n = static_cast<int32_t>(C.n);
-          G.views = static_cast<int32_t>(C.count);
-          G.sumsq = sumsq + class_first[k];
-          G.vrec = reinterpret_cast<const ViewRec*>(ws + P.off_vrec) + class_first[k];
-          // Work units are 256 x 256 blocks, one per CTA pair (2 x 128 rows).
-          G.tiles_m = static_cast<int32_t>(ceil_div(C.m, 2 * kBM));
-          int rc;
-          if (kind == GEMM_GRAM || kind == GEMM_POLY) {
-            // Upper block triangle: row block pm holds column blocks pm..T-1.
-            G.tiles_n = static_cast<int32_t>(ceil_div(C.m, kBN));
-            G.tiles_per_view = G.tiles_n * (G.tiles_n + 1) / 2;
-            G.out = kind == GEMM_GRAM ? A : Pm;
-            G.out_view_stride = C.m * C.lda;
-            G.ld_out = C.lda;
-            if (kind == GEMM_GRAM) {
-              G.K = static_cast<int32_t>(C.n);
-              G.aux = X;
-              G.aux_view_stride = C.m * C.ldx;
-              G.ld_aux = C.ldx;
-              if ((rc = make_tmap(&G.tmA, X, C.n, C.m, C.count, C.ldx, kBM)) != MH_OK) return rc;
-              G.tmB = G.tmA;  // each CTA of a pair loads 128 of the 256 B rows
+      // One launch (or more, kMaxClasses at a time) per operand mode.
+      for (int mode = 0; mode < kGemmModes; ++mode) {
+        std::vector<int> ids;
+        for (int k = 0; k < nclass; ++k)
+          if (gemm_mode(kind, P.classes[k].tstore) == mode) ids.push_back(k);
+        const int nids = static_cast<int>(ids.size());
+        for (int c0 = 0; c0 < nids; c0 += kMaxClasses) {
+          GemmParams gp;
+          std::memset(&gp, 0, sizeof(gp));
+          gp.kind = kind;
+          gp.mode = mode;
+          gp.first_iter = it == 0 ? 1 : 0;
+          gp.a = a;
+          gp.b = b;
+          gp.c = c;
+          gp.eps = eps;
+          gp.status = status;
+          const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
+          gp.final_update = fused ? 1 : 0;
+          gp.cautious = cautious;
+          int64_t tiles = 0;
+          int nc = 0;
+          for (; c0 + nc < nids && nc < kMaxClasses; ++nc) {
+            const int k = ids[c0 + nc];
+            const ClassInfo& C = P.classes[k];
+            GemmClass& G = gp.cls[nc];
+            bf16* X = reinterpret_cast<bf16*>(ws + C.off_x[cur]);
+            bf16* Xn = reinterpret_cast<bf16*>(ws + C.off_x[cur ^ 1]);
+            bf16* A = reinterpret_cast<bf16*>(ws + C.off_a);
+            bf16* Pm = reinterpret_cast<bf16*>(ws + C.off_p);
+            G.m = static_cast<int32_t>(C.m);
+            G.n = static_cast<int32_t>(C.n);
+            G.tstore = C.tstore ? 1 : 0;
+            G.out_rows = static_cast<int32_t>(C.tstore ? C.n : C.m);
+            G.out_cols = static_cast<int32_t>(C.tstore ? C.m : C.n);
+            G.views = static_cast<int32_t>(C.count);
+            G.sumsq = sumsq + class_first[k];
+            G.vrec = reinterpret_cast<const ViewRec*>(ws + P.off_vrec) + class_first[k];
+            // Work units are 256 x 256 blocks, one per CTA pair (2 x 128 rows).
+            G.tiles_m = static_cast<int32_t>(ceil_div(C.m, 2 * kBM));
+            int rc;
+            if (kind == GEMM_GRAM || kind == GEMM_POLY) {
+              // Upper block triangle: row block pm holds column blocks pm..T-1.
+              G.tiles_n = static_cast<int32_t>(ceil_div(C.m, kBN));
+              G.tiles_per_view = G.tiles_n * (G.tiles_n + 1) / 2;
+              G.out = kind == GEMM_GRAM ? A : Pm;
+              G.out_view_stride = C.m * C.lda;
+              G.ld_out = C.lda;
+              if (kind == GEMM_GRAM) {
+                G.K = static_cast<int32_t>(C.n);
+                G.aux = X;
+                G.aux_view_stride = C.xrows * C.ldx;
+                G.ld_aux = C.ldx;
+                if (C.tstore) {
+                  // T is n x m: both operands are 64 x 64 MN-major chunks of T.
+                  if ((rc = make_tmap(&G.tmA, X, C.m, C.n, C.count, C.ldx, 64)) != MH_OK) return rc;
+                } else {
+                  if ((rc = make_tmap(&G.tmA, X, C.n, C.m, C.count, C.ldx, kBM)) != MH_OK) return rc;
+                }
+                G.tmB = G.tmA;  // each CTA of a pair loads 128 of the 256 B rows
+              } else {
+                G.K = static_cast<int32_t>(C.m);
+                G.aux = A;
+                G.aux_view_stride = C.m * C.lda;
+                G.ld_aux = C.lda;
+                if ((rc = make_tmap(&G.tmA, A, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
+                G.tmB = G.tmA;
+              }
             } else {
+              G.tiles_m = static_cast<int32_t>(ceil_div(G.out_rows, 2 * kBM));
+              G.tiles_n = static_cast<int32_t>(ceil_div(G.out_cols, kBN));
+              G.tiles_per_view = G.tiles_m * G.tiles_n;
               G.K = static_cast<int32_t>(C.m);
-              G.aux = A;
-              G.aux_view_stride = C.m * C.lda;
-              G.ld_aux = C.lda;
-              if ((rc = make_tmap(&G.tmA, A, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
-              G.tmB = G.tmA;
+              G.out = Xn;
+              G.out_view_stride = C.xrows * C.ldx;
+              G.ld_out = C.ldx;
+              G.aux = X;
+              G.aux_view_stride = C.xrows * C.ldx;
+              G.ld_aux = C.ldx;
+              if (C.tstore) {
+                // T' = a T + T P: rows of T and rows of P, both K-major.
+                if ((rc = make_tmap(&G.tmA, X, C.m, C.n, C.count, C.ldx, kBM)) != MH_OK) return rc;
+                if ((rc = make_tmap(&G.tmB, Pm, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
+              } else {
+                if ((rc = make_tmap(&G.tmA, Pm, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
+                if ((rc = make_tmap(&G.tmB, X, C.n, C.m, C.count, C.ldx, 64)) != MH_OK) return rc;
+              }
             }
-          } else {
-            G.tiles_n = static_cast<int32_t>(ceil_div(C.n, kBN));
-            G.tiles_per_view = G.tiles_m * G.tiles_n;
-            G.K = static_cast<int32_t>(C.m);
-            G.out = Xn;
-            G.out_view_stride = C.m * C.ldx;
-            G.ld_out = C.ldx;
-            G.aux = X;
-            G.aux_view_stride = C.m * C.ldx;
-            G.ld_aux = C.ldx;
-            if ((rc = make_tmap(&G.tmA, Pm, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
-            if ((rc = make_tmap(&G.tmB, X, C.n, C.m, C.count, C.ldx, 64)) != MH_OK) return rc;
+            G.tile_begin = tiles;
+            tiles += static_cast<int64_t>(G.tiles_per_view) * C.count;
           }
-          G.tile_begin = tiles;
-          tiles += static_cast<int64_t>(G.tiles_per_view) * C.count;
+          gp.num_classes = nc;
+          gp.total_tiles = tiles;
+          if (tiles >= (int64_t(1) << 31))
+            return fail(MH_EUNSUPPORTED, "too many GEMM tiles in one stage (%lld)", (long long)tiles);
+          double flops = 0.0, fexec = 0.0, bytes = 0.0;
+          for (int k = 0; k < nc; ++k) {
+            const GemmClass& G = gp.cls[k];
+            const double m = G.m, nn = G.n, v = G.views;
+            flops += v * (kind == GEMM_POLY ? 2.0 * m * m * m : 2.0 * m * m * nn);
+            const double kpad = std::ceil(G.K / double(kBK)) * kBK;
+            fexec += double(G.tiles_per_view) * v * 2.0 * (2.0 * kBM) * kBN * kpad;
+            // operands read once and the output written once (bf16)
+            if (kind == GEMM_GRAM) bytes += v * 2.0 * (m * nn + m * m);
+            else if (kind == GEMM_POLY) bytes += v * 2.0 * (m * m + m * m);
+            else if (!fused) bytes += v * 2.0 * (m * m + 2.0 * m * nn);
+            else bytes += v * (2.0 * (m * m + m * nn) + 2.0 * 2.0 * m * nn);  // + W read/write (bf16)
+          }
+          static const char* kNames[4] = {"ns_gemm.gram", "ns_gemm.poly", "ns_gemm.apply",
+                                           "ns_gemm.apply_update"};
+          ProfScope ps(stream, kNames[fused ? 3 : kind], bytes, flops, fexec);
+          cudaError_t e = launch_ns_gemm(gp, sms, stream);
+          if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
         }
-        gp.num_classes = nc;
-        gp.total_tiles = tiles;
-        if (tiles >= (int64_t(1) << 31))
-          return fail(MH_EUNSUPPORTED, "too many GEMM tiles in one stage (%lld)", (long long)tiles);
-        double flops = 0.0, fexec = 0.0, bytes = 0.0;
-        for (int k = 0; k < nc; ++k) {
-          const GemmClass& G = gp.cls[k];
-          const double m = G.m, nn = G.n, v = G.views;
-          flops += v * (kind == GEMM_POLY ? 2.0 * m * m * m : 2.0 * m * m * nn);
-          const double kpad = std::ceil(G.K / double(kBK)) * kBK;
-          fexec += double(G.tiles_per_view) * v * 2.0 * (2.0 * kBM) * kBN * kpad;
-          // operands read once and the output written once (bf16)
-          if (kind == GEMM_GRAM) bytes += v * 2.0 * (m * nn + m * m);
-          else if (kind == GEMM_POLY) bytes += v * 2.0 * (m * m + m * m);
-          else if (!fused) bytes += v * 2.0 * (m * m + 2.0 * m * nn);
-          else bytes += v * (2.0 * (m * m + m * nn) + 2.0 * 2.0 * m * nn);  // + W read/write (bf16)
-        }
-        static const char* kNames[4] = {"ns_gemm.gram", "ns_gemm.poly", "ns_gemm.apply",
-                                         "ns_gemm.apply_update"};
-        ProfScope ps(stream, kNames[fused ? 3 : kind], bytes, flops, fexec);
-        cudaError_t e = launch_ns_gemm(gp, sms, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
       }
     }
     cur ^= 1;
@@ -495,7 +527,7 @@ int run_ew_sel(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int
       J.rows = T.rows;
       J.cols = T.cols;
       J.views = T.views;
-      J.tall = T.tall ? 1 : 0;
+      J.tall = 0;  // X of a tall view is kept in its stored layout
       J.tiles_r = static_cast<int32_t>(T.tiles_r);
       J.tiles_c = static_cast<int32_t>(T.tiles_c);
       if (kind == EW_PROLOGUE || kind == EW_PROLOGUE_FLAT) {
@@ -686,8 +718,8 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     J.dst_vec = cols4 && aligned16(U.param);
     J.mom_vec = cols4 && aligned16(U.momentum);
     J.ldx = C.ldx;
-    J.x_view_stride = C.m * C.ldx;
-    bf16* xb = reinterpret_cast<bf16*>(ws + C.off_x[xbuf]) + T.class_slot * C.m * C.ldx;
+    J.x_view_stride = C.xrows * C.ldx;
+    bf16* xb = reinterpret_cast<bf16*>(ws + C.off_x[xbuf]) + T.class_slot * C.xrows * C.ldx;
     J.x0 = xb;
     J.xf = xb;
     J.sumsq = sumsq + T.view_slot;
@@ -839,8 +871,8 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
     J.src_vec = cols4 && aligned16(p.x);
     J.dst_vec = cols4 && aligned16(p.out);
     J.ldx = C.ldx;
-    J.x_view_stride = C.m * C.ldx;
-    bf16* xb = reinterpret_cast<bf16*>(ws + C.off_x[xbuf]) + T.class_slot * C.m * C.ldx;
+    J.x_view_stride = C.xrows * C.ldx;
+    bf16* xb = reinterpret_cast<bf16*>(ws + C.off_x[xbuf]) + T.class_slot * C.xrows * C.ldx;
     J.x0 = xb;
     J.xf = xb;
     J.sumsq = sumsq + T.view_slot;

@@ -2,9 +2,9 @@
 // stored (rows x cols) layout of each view in 32 x 128 tiles:
 //
 //   EW_PROLOGUE  B <- mu B + (1-mu) G;  Q = lerp(G, B, mu) (or B);
-//                writes B (fp32), bf16(Q) into the Newton-Schulz buffer in NS
-//                orientation (transposed through shared memory for tall
-//                views), and accumulates ||Q||_F^2 per view from fp32 Q.
+//                writes B (fp32) and bf16(Q) into the Newton-Schulz buffer
+//                (every view in its stored layout; the GEMMs read tall views
+//                transposed), and per-warp partials of ||Q||_F^2 from fp32 Q.
 //                Speedtronic "v2 optimizers", "Muon update" / "Newton-Schulz";
 //                flaxchat "Optimizer", "Muon Algorithm" step 1.
 //   EW_ROWSQ     per stored row and column tile: sum_j U_ij^2 (NorMuon
@@ -12,8 +12,8 @@
 //   EW_COLSQ     per stored col and row tile: sum_i (f_i U_ij)^2 (Muon+
 //                columns), likewise.
 //   EW_APPLY     W <- (1 - lr wd) W - lr s U, or a cautious form, with
-//                U_ij = f_i h_j X_ji (tall) / X_ij (wide), f from NorMuon and
-//                Muon+ rows, h from Muon+ columns. Speedtronic "Muon update",
+//                U_ij = f_i h_j X_ij, f from NorMuon and Muon+ rows, h from
+//                Muon+ columns. Speedtronic "Muon update",
 //                "Muon+", "Cautious updates"; flaxchat step 4.
 //   EW_COPYOUT   Newton-Schulz-only output U in the caller's dtype.
 //
@@ -32,7 +32,6 @@ static_assert(sizeof(NormParams) <= 32000, "NormParams exceeds the kernel parame
 
 namespace {
 
-constexpr int kSqPad = 2;  // bf16 padding of the shared transpose tiles
 
 __device__ __forceinline__ int find_job(const EwParams& p, int64_t tile) {
   int lo = 0, hi = p.njobs - 1;
@@ -120,53 +119,22 @@ __device__ __forceinline__ TileInfo tile_info(const EwParams& p, int64_t tile) {
 }
 
 // Loads this thread's 4 x 4 block of U (rows r0+4*warp+i, cols c0+4*lane+k)
-// from the Newton-Schulz output buffer. Tall views are stored transposed, so
-// the tile is staged through shared memory. Must be called by the whole CTA.
-__device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t,
-                                             bf16 (*sU)[kEwTileR + kSqPad], float u[4][4]) {
+// from the Newton-Schulz output buffer, which holds every view in its stored
+// layout (row pitch ldx).
+__device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t, float u[4][4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bf16* xv = J.xf + t.v * J.x_view_stride;
-  if (J.tall) {
-    // X rows are stored columns c0..c0+127; X columns are stored rows r0..r0+31.
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int task = threadIdx.x + rep * kEwThreads;
-      const int cc = task >> 2, seg = task & 3;
-      const int64_t xr = t.c0 + cc;
-      const int64_t xc0 = t.r0 + seg * 8;
-      if (xr < J.cols) {
-        const bf16* src = xv + xr * J.ldx + xc0;
-        const int64_t nval = J.rows - xc0;
-        if (nval >= 8) {
-          const uint4 q = *reinterpret_cast<const uint4*>(src);
-          const bf16* h = reinterpret_cast<const bf16*>(&q);
+  for (int i = 0; i < 4; ++i) {
+    const int64_t row = t.r0 + warp * 4 + i;
+    const int64_t col = t.c0 + lane * 4;
+    const int64_t nv = J.cols - col;
+    const int nvalid = nv >= 4 ? 4 : (nv > 0 ? static_cast<int>(nv) : 0);
+    if (row < J.rows && nvalid > 0) {
+      load4(xv + row * J.ldx, MH_BF16, col, nvalid, true, u[i]);
+    } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) sU[cc][seg * 8 + k] = h[k];
-        } else {
-          for (int k = 0; k < 8; ++k)
-            sU[cc][seg * 8 + k] = k < nval ? src[k] : __float2bfloat16_rn(0.0f);
-        }
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) u[i][k] = __bfloat162float(sU[lane * 4 + k][warp * 4 + i]);
-    __syncthreads();
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t row = t.r0 + warp * 4 + i;
-      const int64_t col = t.c0 + lane * 4;
-      const int64_t nv = J.cols - col;
-      const int nvalid = nv >= 4 ? 4 : (nv > 0 ? static_cast<int>(nv) : 0);
-      if (row < J.rows && nvalid > 0) {
-        load4(xv + row * J.ldx, MH_BF16, col, nvalid, true, u[i]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) u[i][k] = 0.0f;
-      }
+      for (int k = 0; k < 4; ++k) u[i][k] = 0.0f;
     }
   }
 }
@@ -228,9 +196,7 @@ __device__ __forceinline__ void store8(void* base, int dt, int64_t off, int nval
   }
 }
 
-constexpr int kProPitch = kProTileC + kSqPad;  // bf16 pitch of the transpose tile
-
-// Prologue of wide views whose X layout equals their stored layout (cols a
+// Prologue of views whose X layout equals their stored layout (cols a
 // multiple of 8): a plain contiguous stream, like AdamW. One work item is a
 // kProChunk-element chunk of one view; each thread handles 8 consecutive
 // elements per step, the block 2048 per step, four steps per chunk. One
@@ -271,7 +237,7 @@ __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __gr
       rec.shape_scale = J.shape_scale;
       rec.pdt = J.dst_dtype;
       rec.gdt = J.src_dtype;
-      rec.tall = J.tall;
+      rec.tall = 0;
       rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
       J.vrec[v] = rec;
     }
@@ -307,12 +273,12 @@ __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __gr
   }
 }
 
-// Momentum, Nesterov lerp, ||Q||_F^2 partials and bf16(Q) in Newton-Schulz
-// orientation, over 32 x 256 tiles (each thread: 4 rows x 8 columns, all
-// loads issued before any store). Tile indices use 32-bit arithmetic (the
-// host rejects tensors with 2^31 or more tiles).
+// Momentum, Nesterov lerp, ||Q||_F^2 partials and bf16(Q) for views whose X
+// row pitch differs from their cols (cols not a multiple of 8), over 32 x 256
+// tiles (each thread: 4 rows x 8 columns, all loads issued before any
+// store). Tile indices use 32-bit arithmetic (the host rejects tensors with
+// 2^31 or more tiles).
 __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_constant__ EwParams p) {
-  __shared__ __align__(16) bf16 sQ[kEwTileR][kProPitch];
   __shared__ __align__(16) EwJob sJ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int cur_job = -1;
@@ -356,7 +322,7 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
       rec.shape_scale = J.shape_scale;
       rec.pdt = J.dst_dtype;
       rec.gdt = J.src_dtype;
-      rec.tall = J.tall;
+      rec.tall = 0;
       rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
       J.vrec[v] = rec;
     }
@@ -395,52 +361,18 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) ss += q[k] * q[k];  // q[k] == 0 beyond nvalid
-      if (!J.tall) {
-        store8(xv + row * J.ldx, MH_BF16, col, nvalid, true, q);
-      } else {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sQ[lr][lane * 8]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(q[2 * k], q[2 * k + 1]);
-          dst[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-      }
+      store8(xv + row * J.ldx, MH_BF16, col, nvalid, true, q);
     }
     // ||Q||_F^2 of this warp's 4 x 256 block: one partial per warp, summed in
     // a fixed order by the view-norm kernel, so wide tiles need no block-wide
     // barrier.
     ss = warp_sum(ss);
     if (lane == 0) J.tile_ss[static_cast<int64_t>(local) * (kEwThreads / 32) + warp] = ss;
-    if (J.tall) {
-      __syncthreads();
-      // Write the transpose: X row = stored col c0 + cc, X cols = stored rows.
-#pragma unroll
-      for (int rep = 0; rep < 4; ++rep) {
-        const int task = threadIdx.x + rep * kEwThreads;
-        const int cc = task >> 2, seg = task & 3;
-        const int64_t xr = c0 + cc;
-        const int64_t xc0 = r0 + seg * 8;
-        if (xr >= J.cols) continue;
-        bf16* dst = xv + xr * J.ldx + xc0;
-        const int64_t nval = J.rows - xc0;
-        if (nval >= 8) {
-          uint4 q;
-          bf16* h = reinterpret_cast<bf16*>(&q);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) h[k] = sQ[seg * 8 + k][cc];
-          *reinterpret_cast<uint4*>(dst) = q;
-        } else {
-          for (int k = 0; k < nval; ++k) dst[k] = sQ[seg * 8 + k][cc];
-        }
-      }
-      __syncthreads();
-    }
   }
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ EwParams p) {
-  __shared__ __align__(16) bf16 sU[kEwTileC][kEwTileR + kSqPad];     // U loads, tall
   __shared__ float sRed[kEwThreads / 32][kEwTileC];
   // The tile's job record, copied once per tile from the parameter space:
   // indexing a large parameter table per access would keep missing the small
@@ -469,7 +401,7 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
 
     {
       float u[4][4];
-      load_u_block(J, t, sU, u);
+      load_u_block(J, t, u);
 
       if constexpr (KIND == EW_ROWSQ) {
 #pragma unroll

@@ -58,7 +58,7 @@ struct EwJob {
   int64_t x_view_stride; // elements between views in the X buffers
   int64_t tile_begin;    // first global tile index of this tensor
   int32_t tiles_r, tiles_c;
-  int32_t tall;          // rows > cols: X holds the transpose
+  int32_t tall;          // unused by the kernels (X is always in stored layout)
   int32_t flat;          // prologue: wide view stored like X (cols % 8 == 0): streamed
                          // as contiguous kProChunk-element chunks, tiles_r = 1
   int32_t src_dtype, dst_dtype;
@@ -156,11 +156,25 @@ constexpr int kGemmThreads = 256;
 
 enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_APPLY = 2 };
 
+// Operand major-ness of one launch (A, B): K-major (K) or MN-major (M). The
+// gram of a tall view reads both operands as MN-major chunks of T; the apply
+// reads X MN-major as B, except for tall views (T P: both K-major); every
+// other stage is K-major. Each launch covers classes of one mode, so the
+// kernel is specialised on it.
+enum GemmMode { GEMM_MODE_KK = 0, GEMM_MODE_KM = 1, GEMM_MODE_MM = 2 };
+constexpr int kGemmModes = 3;
+inline int gemm_mode(int kind, bool tstore) {
+  if (kind == GEMM_GRAM) return tstore ? GEMM_MODE_MM : GEMM_MODE_KK;
+  if (kind == GEMM_APPLY) return tstore ? GEMM_MODE_KK : GEMM_MODE_KM;
+  return GEMM_MODE_KK;
+}
+
 struct GemmClass {
-  CUtensorMap tmA;         // operand A: rows of X (gram), A (poly), P (apply); box 64 x 128
-  CUtensorMap tmB;         // operand B: rows of X (gram), A (poly) box 64 x 128 (half
-                           //            of the 256 B rows per CTA of a pair);
-                           //            X as MN-major (apply) box 64 x 64
+  CUtensorMap tmA;         // operand A: rows of X (gram), A (poly), P or T (apply);
+                           //   K-major box 64 x 128, or MN-major 64 x 64 chunks of T (gram, tstore)
+  CUtensorMap tmB;         // operand B: 128 of the 256 B rows per CTA of a pair: X (gram),
+                           //   A (poly), P (apply, tstore) K-major; X (apply) or T
+                           //   (gram, tstore) as MN-major 64 x 64 chunks
   bf16* out;               // output base (first view of the class)
   const bf16* aux;         // poly: A (b*A term); apply: X (a*X term)
   const double* sumsq;     // per view sum of squares of Q (first iteration only)
@@ -168,6 +182,10 @@ struct GemmClass {
   int64_t out_view_stride, aux_view_stride;  // elements
   int64_t ld_out, ld_aux;                     // elements
   int32_t m, n;            // Newton-Schulz orientation (m <= n)
+  int32_t tstore;          // X is kept in its stored (n x m) layout T = X^T: the gram
+                           // reads T with MN-major operands (A = T^T T) and the apply
+                           // computes T' = a T + T P
+  int32_t out_rows, out_cols;  // apply output (m x n, or n x m when tstore)
   int32_t views;
   int32_t tiles_m, tiles_n, tiles_per_view;  // in 256 x 256 pair blocks
   int32_t K;               // contraction length
@@ -178,6 +196,7 @@ struct GemmParams {
   GemmClass cls[kMaxClasses];
   int32_t num_classes;
   int32_t kind;            // GemmKind
+  int32_t mode;            // GemmMode shared by every class of the launch
   int32_t first_iter;      // fold the Frobenius normalisation in
   int32_t final_update;    // apply: update the parameters instead of writing X'
   int32_t cautious;        // MH_CAUTIOUS_* for the final update

@@ -13,6 +13,11 @@
 //                                      triangle scheme; b A read in the epilogue)
 //   GEMM_APPLY  X' = a X + P X        (B operand = X read MN-major)
 //
+// A tall view (rows > cols) keeps its Newton-Schulz matrix in the stored
+// layout T = X^T (n x m); for such shape classes the gram reads T with
+// MN-major A and B operands (A = T^T T) and the apply computes T' = a T + T P
+// with K-major operands (P is symmetric), so no pass ever transposes data.
+//
 // On the first step the Frobenius normalisation 1/(||Q||_F + eps) is folded in:
 // the gram epilogue scales by s^2 and the apply epilogue by s, so the
 // prologue never has to re-read Q to normalise it.
@@ -54,8 +59,7 @@ constexpr uint32_t kHalfBBytes = kStageBBytes / 2;
 constexpr uint32_t kTmemCols = 2 * kBN;           // two fp32 accumulators
 constexpr uint32_t kApplyChunkBytes = kBK * 64 * 2;  // one 64-col MN-major box: 8 KB
 constexpr int kTPitch = 40;                        // bf16 pitch of the mirror-transpose tile
-constexpr int kUPitch = 36;                        // fp32 pitch of the update-transpose tile
-constexpr uint32_t kTBytes = 32 * kUPitch * 4;     // per epilogue warp (holds either)
+constexpr uint32_t kTBytes = 32 * kTPitch * 2;     // per epilogue warp
 constexpr uint16_t kPairMask = 0x3;
 
 struct TileCoord {
@@ -64,6 +68,7 @@ struct TileCoord {
 
 // Maps a pair-tile index to (class, view, 256-row block pm, 256-col block tn)
 // and returns this CTA's 128-row tile tm = 2 pm + rank.
+template <int MODE>
 __device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t, uint32_t rank) {
   int c = 0;
   while (c + 1 < p.num_classes && t >= p.cls[c + 1].tile_begin) ++c;
@@ -75,8 +80,16 @@ __device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t, ui
   int w = static_cast<int>(local - static_cast<int64_t>(tc.view) * C.tiles_per_view);
   int pm;
   if (p.kind == GEMM_APPLY) {
-    pm = w % C.tiles_m;
-    tc.tn = w / C.tiles_m;
+    // Consecutive tiles walk the m x m operand P (which stays in L2) and share
+    // one block of X: for X = m x n the row blocks of the output, for a tall
+    // view's T = n x m (mode KK) its column blocks.
+    if (MODE == GEMM_MODE_KK) {
+      tc.tn = w % C.tiles_n;
+      pm = w / C.tiles_n;
+    } else {
+      pm = w % C.tiles_m;
+      tc.tn = w / C.tiles_m;
+    }
   } else {
     // Row block pm holds the column blocks tn >= pm (upper block triangle).
     pm = 0;
@@ -214,7 +227,10 @@ __device__ __forceinline__ void abort_pair(volatile int* abort_flag) {
   st_cluster_s32(abort_flag, 1, 1);
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool a_mn = MODE == GEMM_MODE_MM;
+  constexpr bool b_mn = MODE != GEMM_MODE_KK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -274,7 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       uint32_t inflight_par = 0; // parity of that load's phase
       bool ok = true;
       for (int64_t t = pair; ok && t < p.total_tiles; t += npairs) {
-        const TileCoord tc = map_tile(p, t, rank);
+        const TileCoord tc = map_tile<MODE>(p, t, rank);
         const GemmClass& C = p.cls[tc.cls];
         const int nk = (C.K + kBK - 1) / kBK;
         for (int kb = 0; kb < nk; ++kb) {
@@ -283,11 +299,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             break;
           }
           mbar_arrive_expect_tx(&full[stage], kStageABytes + kStageBBytes);
-          tma_load_3d(sA + stage * kStageABytes, &C.tmA, &full[stage], kb * kBK, tc.tm * kBM,
-                      tc.view);
+          uint8_t* a_dst = sA + stage * kStageABytes;
+          if constexpr (a_mn) {
+            // 128 columns of T as two MN-major 64-column chunks.
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_3d(a_dst + j * kApplyChunkBytes, &C.tmA, &full[stage],
+                          tc.tm * kBM + j * 64, kb * kBK, tc.view);
+          } else {
+            tma_load_3d(a_dst, &C.tmA, &full[stage], kb * kBK, tc.tm * kBM, tc.view);
+          }
           uint8_t* b_dst = sB + stage * kStageBBytes;
-          if (apply) {
-            // This CTA's two 64-column chunks of the 256-column X block.
+          if constexpr (b_mn) {
+            // This CTA's two 64-column chunks of the 256-column B block.
 #pragma unroll
             for (int j = 2 * static_cast<int>(rank); j < 2 * static_cast<int>(rank) + 2; ++j)
               tma_load_3d_mc(b_dst + j * kApplyChunkBytes, &C.tmB, &full[stage],
@@ -330,14 +354,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0, apply ? 1 : 0);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      // K-major: 16 bf16 of k = 32 bytes inside the 128-byte swizzle row.
+      // MN-major: 16 k-rows = two 1024-byte atoms, 64-column chunks 8 KB apart.
+      constexpr uint32_t a_kstep = a_mn ? 2048u : 32u, a_lbo = a_mn ? kApplyChunkBytes : 16u;
+      constexpr uint32_t b_kstep = b_mn ? 2048u : 32u, b_lbo = b_mn ? kApplyChunkBytes : 16u;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int64_t t = pair; ok && t < p.total_tiles; t += npairs) {
-        const TileCoord tc = map_tile(p, t, rank);
+        const TileCoord tc = map_tile<MODE>(p, t, rank);
         const GemmClass& C = p.cls[tc.cls];
         const int nk = (C.K + kBK - 1) / kBK;
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
@@ -356,12 +384,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           const uint32_t b0 = smem_addr(sB + stage * kStageBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            // K-major A: 16 bf16 of k = 32 bytes inside the 128-byte swizzle row.
-            const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-            // K-major B likewise; MN-major B: 16 k-rows = two 1024-byte atoms,
-            // 64-col chunks 8 KB apart.
-            const uint64_t bd = apply ? smem_desc_sw128(b0 + k * 2048, kApplyChunkBytes, 1024)
-                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
+            const uint64_t ad = smem_desc_sw128(a0 + k * a_kstep, a_lbo, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + k * b_kstep, b_lbo, 1024);
             tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued = true;
@@ -389,7 +413,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = pair; t < p.total_tiles; t += npairs) {
-      const TileCoord tc = map_tile(p, t, rank);
+      const TileCoord tc = map_tile<MODE>(p, t, rank);
       const GemmClass& C = p.cls[tc.cls];
       if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPI)) {
         abort_pair(abort_flag);
@@ -399,7 +423,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
       const int r0 = tc.tm * kBM + ew * 32;  // first row of this warp
       const int r = r0 + lane;
-      const int n_out = apply ? C.n : C.m;
+      const int rows_out = apply ? C.out_rows : C.m;
+      const int n_out = apply ? C.out_cols : C.m;
       float sc = 1.0f;
       if (p.first_iter) {
         const float s = 1.0f / (sqrtf(static_cast<float>(C.sumsq[tc.view])) + p.eps);
@@ -420,7 +445,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
-        const bool row_ok = r < C.m;
+        const bool row_ok = r < rows_out;
         const bool full_cols = c0 + 32 <= n_out;
 
         if (apply && p.final_update) {
@@ -443,34 +468,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 #pragma unroll
             for (int j = 0; j < 32; ++j) u[j] = 0.0f;
           }
+          // The record's view is stored exactly like this tile's output (tall
+          // views are kept in their stored layout), so row r / columns c0.. of
+          // the output are row r / columns c0.. of the parameter.
           const ViewRec R = C.vrec[tc.view];
-          if (!R.tall) {
-            if (row_ok) {
-              const int nvalid = n_out - c0 < 32 ? n_out - c0 : 32;
-              update_w32(R, R.elem0 + static_cast<int64_t>(r) * R.cols + c0, nvalid, u,
-                         p.cautious);
-            }
-          } else {
-            // Tall view: X row r is stored column r. Transpose the 32 x 32
-            // chunk so lane L updates stored row c0 + L, columns r0..r0+31.
-            float* tb = reinterpret_cast<float*>(tbuf);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) tb[j * kUPitch + lane] = u[j];
-            __syncwarp();
-            const int wrow = c0 + lane;
-            if (wrow < n_out) {
-              float ut[32];
-              const float4* s4 = reinterpret_cast<const float4*>(tb + lane * kUPitch);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 t4 = s4[q];
-                ut[4 * q] = t4.x; ut[4 * q + 1] = t4.y; ut[4 * q + 2] = t4.z; ut[4 * q + 3] = t4.w;
-              }
-              const int nvalid = C.m - r0 < 32 ? C.m - r0 : 32;
-              update_w32(R, R.elem0 + static_cast<int64_t>(wrow) * R.cols + r0, nvalid, ut,
-                         p.cautious);
-            }
-            __syncwarp();
+          if (row_ok) {
+            const int nvalid = n_out - c0 < 32 ? n_out - c0 : 32;
+            update_w32(R, R.elem0 + static_cast<int64_t>(r) * R.cols + c0, nvalid, u,
+                       p.cautious);
           }
           continue;
         }
@@ -593,7 +598,7 @@ int gemm_max_pairs(int dev, int num_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, ns_gemm_kernel, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&clusters, ns_gemm_kernel<GEMM_MODE_KK>, &cfg) != cudaSuccess ||
       clusters <= 0) {
     (void)cudaGetLastError();
     clusters = num_sms / 2;
@@ -604,15 +609,21 @@ int gemm_max_pairs(int dev, int num_sms) {
 
 cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
+  if (p.mode < 0 || p.mode >= kGemmModes) return cudaErrorInvalidValue;
+  using Kernel = void (*)(GemmParams);
+  static constexpr Kernel kKernels[kGemmModes] = {
+      ns_gemm_kernel<GEMM_MODE_KK>, ns_gemm_kernel<GEMM_MODE_KM>, ns_gemm_kernel<GEMM_MODE_MM>};
   const size_t smem = gemm_smem_bytes();
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    for (Kernel k : kKernels) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
     configured_device = dev;
   }
   const int64_t max_pairs = gemm_max_pairs(dev, num_sms);
@@ -629,7 +640,7 @@ cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, kKernels[p.mode], p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
