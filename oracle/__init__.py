@@ -8,16 +8,18 @@ the seeded input generator in ``synth``.
 Parity pins (each in tests/test_oracle_*.py) tie every function here to
 something other than itself: closed forms, the SVD of the input, invariances
 the iteration must respect, brute force on tiny inputs, and PyTorch's own
-AdamW in float64.
+AdamW and gradient clipping in float64.
 """
 from .muon import (NS_COEFFS, NS_EPS, NS_STEPS, CAUTIOUS_OFF, CAUTIOUS_UPDATE, CAUTIOUS_WD,
                    MuonHparams, momentum_nesterov, muon_apply, muon_plus_row_col,
                    muon_step_tensor, muon_step_view, newton_schulz, normuon, shape_scale)
 from .adamw import adamw_step
 from .bf16 import round_bf16
+from .grad_control import CLIP_EPS, GradControl, grad_control
 
 __all__ = [
     "NS_COEFFS", "NS_EPS", "NS_STEPS", "CAUTIOUS_OFF", "CAUTIOUS_UPDATE", "CAUTIOUS_WD",
     "MuonHparams", "momentum_nesterov", "muon_apply", "muon_plus_row_col", "muon_step_tensor",
     "muon_step_view", "newton_schulz", "normuon", "shape_scale", "adamw_step", "round_bf16",
+    "CLIP_EPS", "GradControl", "grad_control",
 ]
