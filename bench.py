@@ -58,6 +58,9 @@ def parse_args():
     ap.add_argument("--ns-n", type=int, default=4096)
     ap.add_argument("--ns-aspect", default="1:1", choices=["1:1", "1:4", "4:1"])
     ap.add_argument("--ns-batch", type=int, default=8)
+    ap.add_argument("--max-grad-norm", type=float, default=None,
+                    help="run the gradient control (global norm, clip to this value, overflow "
+                         "skip) ahead of both halves; 0 observes the norm only")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -210,7 +213,7 @@ def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
 # ---- workload on the device -------------------------------------------------------------
 
 class DeviceWorkload:
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, max_grad_norm=None):
         import numpy as np
         import torch
         import muon_adamw_hybrid_gb300 as mh
@@ -239,6 +242,18 @@ class DeviceWorkload:
         need = mh.muon_workspace_bytes(self.ts, self.hp) if self.ts else 0
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.step_count = 0
+        # Optional gradient control (global norm over every gradient, clip,
+        # overflow skip) ahead of both halves, as a trainer would run it.
+        self.max_grad_norm = max_grad_norm
+        self.control = None
+        if max_grad_norm is not None:
+            self.control = mh.GradientControl(device)
+            self.grefs = [mh.grad_ref(g) for g in self.mG + self.aG]
+            self.gws = torch.empty(mh.grad_prepare_workspace_bytes(self.grefs), dtype=torch.uint8,
+                                   device=device)
+            self.hp.grad_mult = self.control.grad_mult.data_ptr()
+            self.hp.skip = self.control.skip.data_ptr()
+            self.cstruct = self.control.struct()
         self.resident_bytes = sum(t.numel() * t.element_size() for t in
                                   self.mW + self.mG + self.mB + self.aW + self.aG + self.am + self.av)
         self.resident_bytes += self.ws.numel()
@@ -246,12 +261,19 @@ class DeviceWorkload:
     def step(self, stream) -> None:
         s = stream.cuda_stream
         self.step_count += 1
+        if self.control is not None:
+            self.mh._lib.grad_prepare(self.grefs, 1.0, float(self.max_grad_norm), self.cstruct,
+                                      self.gws.data_ptr(), self.gws.numel(), s)
         if self.ts:
             self.mh.muon_step_batched(self.ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
         if self.at:
             hp = self.wl.adam_hp
-            self.mh.adamw_step(self.at, hp["lr"], hp["betas"][0], hp["betas"][1], hp["eps"],
-                               self.step_count, s)
+            if self.control is not None:
+                self.mh.adamw_step_ctl(self.at, hp["lr"], hp["betas"][0], hp["betas"][1],
+                                       hp["eps"], self.cstruct, s)
+            else:
+                self.mh.adamw_step(self.at, hp["lr"], hp["betas"][0], hp["betas"][1], hp["eps"],
+                                   self.step_count, s)
 
     def check_status(self, stream) -> None:
         if self.ts:
@@ -367,11 +389,12 @@ class OracleSample:
     """Inputs of a bounded sample, generated once; ``run()`` times the fp64
     oracle on them and returns (muon seconds, adamw seconds)."""
 
-    def __init__(self, wl, views, adam):
+    def __init__(self, wl, views, adam, max_grad_norm=None):
         import numpy as np
         import oracle
         from synth import workloads as W
         self.wl, self.views, self.adam = wl, views, adam
+        self.max_grad_norm = max_grad_norm
         hp = wl.muon_hp
         self.hp = oracle.MuonHparams(
             lr=hp["lr"], momentum=hp["momentum"], nesterov=hp["nesterov"], eps=hp["eps"],
@@ -391,8 +414,13 @@ class OracleSample:
                         for j, cnt in adam]
 
     def run(self):
+        """Seconds for (Muon views, AdamW chunks, gradient control of both)."""
         import numpy as np
         import oracle
+        tc0 = time.perf_counter()
+        if self.max_grad_norm is not None:
+            oracle.grad_control([g for _, g, _, _ in self.inputs] + [g for _, g, _ in self.ainputs],
+                                1.0, self.max_grad_norm)
         t0 = time.perf_counter()
         for Wv, Gv, Bv, s in self.inputs:
             res = oracle.muon_step_view(Wv, Gv, Bv, self.hp, s.lr_mult, s.wd,
@@ -408,12 +436,18 @@ class OracleSample:
             if s.param_dtype == "bf16":
                 oracle.round_bf16(Wn)
         t2 = time.perf_counter()
-        return t1 - t0, t2 - t1
+        return t1 - t0, t2 - t1, t0 - tc0
+
+    def grad_elems(self) -> int:
+        return sum(g.size for _, g, _, _ in self.inputs) + sum(g.size for _, g, _ in self.ainputs)
 
 
-def oracle_extrapolated_ms(wl, views, adam, muon_s, adam_s):
-    """Full-step ms: Muon time scaled by NS FLOPs, AdamW time by elements."""
+def oracle_extrapolated_ms(wl, views, adam, muon_s, adam_s, ctl_s=0.0, ctl_elems=0):
+    """Full-step ms: Muon time scaled by NS FLOPs, AdamW time by elements,
+    gradient-control time by gradient elements."""
     ms = 0.0
+    if ctl_elems > 0:
+        ms += 1e3 * ctl_s * (wl.muon_elems + wl.adam_elems) / ctl_elems
     sample_flops = sum(f for _, _, f in views)
     if sample_flops > 0:
         ms += 1e3 * muon_s * ns_flops(wl) / sample_flops
@@ -443,20 +477,21 @@ def run_reference(args, wl):
         return 0
     # One bounded sample per step: about a second of CPU work.
     views, adam = oracle_sample_plan(wl, muon_flop_budget=2.0e11, adam_elems=1 << 22)
-    sample = OracleSample(wl, views, adam)
+    sample = OracleSample(wl, views, adam, args.max_grad_norm)
     for _ in range(args.warmup):
         sample.run()
     per = []
     for _ in range(args.steps):
-        ms_muon, ms_adam = sample.run()
-        per.append(oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam))
+        ms_muon, ms_adam, ms_ctl = sample.run()
+        per.append(oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam, ms_ctl,
+                                          sample.grad_elems()))
     ms = statistics.mean(per)
     cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms/step",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_dict(wl, world),
+        "data": "synthetic", "config": config_dict(wl, world, args.max_grad_norm),
         "cpu_baseline": {"value": round(ms, 3), "unit": "ms/step", "cores": cores,
                          "kind": "oracle", "sample": sample_desc(wl, views, adam)},
         "e2e": {"value": round(ms, 3), "unit": "ms/step", "h2d_bytes_per_step": 0,
@@ -466,8 +501,10 @@ def run_reference(args, wl):
     return 0
 
 
-def config_dict(wl, world):
-    return {"workload": wl.name,
+def config_dict(wl, world, max_grad_norm=None):
+    extra = {} if max_grad_norm is None else {
+        "grad_control": {"max_grad_norm": max_grad_norm, "inv_loss_scale": 1.0}}
+    return {**{"workload": wl.name,
             "muon_tensors": len(wl.muon), "muon_views": sum(s.views for s in wl.muon),
             "muon_elems": wl.muon_elems, "adamw_tensors": len(wl.adamw),
             "adamw_elems": wl.adam_elems, "ns_steps": wl.muon_hp["ns_steps"],
@@ -476,7 +513,7 @@ def config_dict(wl, world):
             "precision": "bf16 tensor-core NS operands, fp32 accumulate; fp32 elementwise math "
                          "and optimizer state; bf16 params/grads",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "l2": "inputs larger than L2 (no flush needed)"}
+            "l2": "inputs larger than L2 (no flush needed)"}, **extra}
 
 
 def run_ns_only(args):
@@ -567,7 +604,7 @@ def main():
     stream = torch.cuda.current_stream(device)
     peaks, peak_src = load_peaks()
 
-    dw = DeviceWorkload(wl, device)
+    dw = DeviceWorkload(wl, device, args.max_grad_norm)
     torch.cuda.synchronize()
     for _ in range(max(args.warmup, 0)):
         dw.step(stream)
@@ -689,18 +726,20 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         views, adam = oracle_sample_plan(wl, muon_flop_budget=1.2e13, adam_elems=1 << 24)
-        ms_muon, ms_adam = OracleSample(wl, views, adam).run()
-        cpu_ms = oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam)
+        osample = OracleSample(wl, views, adam, args.max_grad_norm)
+        ms_muon, ms_adam, ms_ctl = osample.run()
+        cpu_ms = oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam, ms_ctl,
+                                        osample.grad_elems())
         cpu = {"value": round(cpu_ms, 1), "unit": "ms/step", "cores": blas_threads(),
                "kind": "oracle", "sample": sample_desc(wl, views, adam),
-               "sample_seconds": round(ms_muon + ms_adam, 2)}
+               "sample_seconds": round(ms_muon + ms_adam + ms_ctl, 2)}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(ms_step, 3), "unit": "ms/step", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_dict(wl, world),
+            "data": "synthetic", "config": config_dict(wl, world, args.max_grad_norm),
             "ns_tflops": round(nsf / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
             "ns_ms_per_step": round(ns_ms, 3),
             "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,

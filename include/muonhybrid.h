@@ -103,6 +103,10 @@ typedef struct {
   int32_t muon_plus;  /* 1: Muon+ row_col normalisation (Speedtronic "Muon+") */
   float plus_eps;     /* Muon+ eps inside each square root, > 0 */
   int32_t cautious;   /* MH_CAUTIOUS_* */
+  /* Gradient control written by mh_grad_prepare (both DEVICE pointers, read
+   * by the kernels of this call, NULL = off): */
+  const float* grad_mult;  /* every gradient element is read as g * (*grad_mult) */
+  const int32_t* skip;     /* when *skip != 0 the call writes nothing at all */
 } mh_muon_hparams;
 
 /* Bytes of device workspace mh_muon_step_batched needs for these tensors and
@@ -185,6 +189,57 @@ typedef struct {
  * in fp32, bf16 parameters rounded to nearest even on store. */
 int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1, float beta2,
                   float eps, int64_t step, void* stream);
+
+/* ---- Gradient control ahead of both optimizer halves -------------------
+ * kimi-k3 "Optimization", "Keep the arithmetic and gradients under control":
+ * the global gradient norm is measured before the optimizer step; a positive
+ * max_grad_norm clips it when needed, 0 disables clipping while the norm is
+ * still observed; under FP16 a gradient scaler is used and an overflow skips
+ * the whole hybrid update (Muon and AdamW). dew.training.optim
+ * "build_optimizer": the clip reads every gradient of every group together.
+ *
+ * mh_grad_prepare reads every gradient once and leaves its decision in
+ * device memory, so the step calls that follow (same stream) apply it
+ * without a host round trip:
+ *   u      = g * inv_loss_scale                     (unscaled gradient)
+ *   norm   = sqrt(sum of u^2 over every element of every gradient)
+ *   skip   = some u is inf or NaN
+ *   mult   = skip ? 0 : inv_loss_scale * (max_norm > 0 ? min(1, max_norm / (norm + 1e-6)) : 1)
+ *   step  += skip ? 0 : 1                           (when ctl->step != NULL)
+ * The clip factor is PyTorch's clip_grad_norm_ definition. The sum of
+ * squares is accumulated in fp32 within each thread's share of a
+ * 65536-element chunk (at most 256 squares) and in fp64 across threads and
+ * chunks, in a fixed order (bitwise reproducible). A finite
+ * gradient whose square overflows fp32 (|u| > 1.8e19) gives norm = inf and
+ * mult = 0, not a skip. */
+typedef struct {
+  const void* grad;   /* numel elements, grad_dtype, DEVICE */
+  int32_t grad_dtype; /* mh_dtype */
+  int64_t numel;      /* >= 0 */
+} mh_grad_ref;
+
+typedef struct {
+  float* grad_mult;   /* DEVICE float: the factor above */
+  int32_t* skip;      /* DEVICE int32: 1 when the step must be skipped, else 0 */
+  double* norm;       /* DEVICE double: the global norm (NaN when skipping) */
+  int64_t* step;      /* DEVICE int64 step count advanced on applied steps, or NULL */
+} mh_grad_control;
+
+/* Workspace bytes mh_grad_prepare needs (8 per 65536 gradient elements). */
+size_t mh_grad_prepare_workspace_bytes(const mh_grad_ref* grads, int32_t n);
+
+/* Computes the control block above for `n` gradients. inv_loss_scale > 0
+ * and finite, max_norm >= 0. ctl->grad_mult, ctl->skip and ctl->norm must be
+ * non-NULL. n = 0 gives norm 0, mult = inv_loss_scale, no skip. */
+int mh_grad_prepare(const mh_grad_ref* grads, int32_t n, float inv_loss_scale, float max_norm,
+                    const mh_grad_control* ctl, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* mh_adamw_step under a control block: gradients are read as g * (*grad_mult),
+ * nothing is written when *skip != 0, and the bias-correction count t is read
+ * on the device from *ctl->step (required, >= 1 once mh_grad_prepare has run). */
+int mh_adamw_step_ctl(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1,
+                      float beta2, float eps, const mh_grad_control* ctl, void* stream);
 
 /* Optional per-kernel timing. When enabled, every kernel the library launches
  * is bracketed by two CUDA events recorded on its own stream, and the

@@ -21,7 +21,8 @@ MH_CAUTIOUS_OFF, MH_CAUTIOUS_WD, MH_CAUTIOUS_UPDATE = 0, 1, 2
 EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_bytes",
             "mh_newton_schulz_batched", "mh_adamw_step", "mh_workspace_status", "mh_last_error",
             "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read",
-            "mh_newton_schulz_batched_noalloc")
+            "mh_newton_schulz_batched_noalloc", "mh_grad_prepare_workspace_bytes",
+            "mh_grad_prepare", "mh_adamw_step_ctl")
 NS_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -36,7 +37,8 @@ class MuonHparams(ctypes.Structure):
     _fields_ = [("lr", c_float), ("momentum", c_float), ("nesterov", c_int32), ("eps", c_float),
                 ("ns_steps", c_int32), ("a", c_float), ("b", c_float), ("c", c_float),
                 ("normuon", c_int32), ("beta2", c_float), ("muon_plus", c_int32),
-                ("plus_eps", c_float), ("cautious", c_int32)]
+                ("plus_eps", c_float), ("cautious", c_int32),
+                ("grad_mult", c_void_p), ("skip", c_void_p)]
 
 
 class NsProblem(ctypes.Structure):
@@ -48,6 +50,15 @@ class AdamwTensor(ctypes.Structure):
     _fields_ = [("param", c_void_p), ("grad", c_void_p), ("exp_avg", c_void_p),
                 ("exp_avg_sq", c_void_p), ("param_dtype", c_int32), ("grad_dtype", c_int32),
                 ("numel", c_int64), ("lr_mult", c_float), ("wd", c_float)]
+
+
+class GradRef(ctypes.Structure):
+    _fields_ = [("grad", c_void_p), ("grad_dtype", c_int32), ("numel", c_int64)]
+
+
+class GradControl(ctypes.Structure):
+    _fields_ = [("grad_mult", c_void_p), ("skip", c_void_p), ("norm", c_void_p),
+                ("step", c_void_p)]
 
 
 class KernelStats(ctypes.Structure):
@@ -85,6 +96,14 @@ def _load() -> ctypes.CDLL:
     lib.mh_adamw_step.argtypes = [POINTER(AdamwTensor), c_int32, c_float, c_float, c_float,
                                   c_float, c_int64, c_void_p]
     lib.mh_adamw_step.restype = c_int
+    lib.mh_adamw_step_ctl.argtypes = [POINTER(AdamwTensor), c_int32, c_float, c_float, c_float,
+                                      c_float, POINTER(GradControl), c_void_p]
+    lib.mh_adamw_step_ctl.restype = c_int
+    lib.mh_grad_prepare_workspace_bytes.argtypes = [POINTER(GradRef), c_int32]
+    lib.mh_grad_prepare_workspace_bytes.restype = c_size_t
+    lib.mh_grad_prepare.argtypes = [POINTER(GradRef), c_int32, c_float, c_float,
+                                    POINTER(GradControl), c_void_p, c_size_t, c_void_p]
+    lib.mh_grad_prepare.restype = c_int
     lib.mh_workspace_status.argtypes = [c_void_p, c_void_p]
     lib.mh_workspace_status.restype = c_int
     lib.mh_last_error.argtypes = []
@@ -161,6 +180,27 @@ def adamw_step(tensors, lr: float, beta1: float, beta2: float, eps: float, step:
                stream: int) -> None:
     arr, n = _array(AdamwTensor, tensors)
     _check(LIB.mh_adamw_step(arr, n, lr, beta1, beta2, eps, step, stream))
+
+
+def adamw_step_ctl(tensors, lr: float, beta1: float, beta2: float, eps: float,
+                   control: GradControl, stream: int) -> None:
+    arr, n = _array(AdamwTensor, tensors)
+    _check(LIB.mh_adamw_step_ctl(arr, n, lr, beta1, beta2, eps, ctypes.byref(control), stream))
+
+
+def grad_prepare_workspace_bytes(grads) -> int:
+    arr, n = _array(GradRef, grads)
+    nbytes = LIB.mh_grad_prepare_workspace_bytes(arr, n)
+    if nbytes == 0:
+        raise MuonHybridError(MH_EINVAL, last_error())
+    return int(nbytes)
+
+
+def grad_prepare(grads, inv_loss_scale: float, max_norm: float, control: GradControl,
+                 workspace: int, workspace_bytes: int, stream: int) -> None:
+    arr, n = _array(GradRef, grads)
+    _check(LIB.mh_grad_prepare(arr, n, inv_loss_scale, max_norm, ctypes.byref(control),
+                               workspace, workspace_bytes, stream))
 
 
 def workspace_status(workspace: int, stream: int) -> None:

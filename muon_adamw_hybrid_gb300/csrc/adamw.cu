@@ -83,6 +83,9 @@ __device__ __forceinline__ void adam_elem(float& w, float g, float& m, float& v,
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamParams p) {
+  __shared__ float s_bc[2];
+  if (step_skipped(p.skip)) return;
+  const float gmul = p.grad_mult != nullptr ? *p.grad_mult : 1.0f;
   AdamConsts k;
   k.b1 = p.beta1;
   k.omb1 = 1.0f - p.beta1;
@@ -91,6 +94,19 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   k.eps = p.eps;
   k.inv_bc1 = p.inv_bc1;
   k.inv_sqrt_bc2 = p.inv_sqrt_bc2;
+  if (p.step != nullptr) {
+    // Bias corrections from the device step count (advanced by the gradient
+    // control only on applied steps), once per block, in double like the
+    // host path.
+    if (threadIdx.x == 0) {
+      const double t = static_cast<double>(*p.step < 1 ? 1 : *p.step);
+      s_bc[0] = static_cast<float>(1.0 / (1.0 - pow(static_cast<double>(p.beta1), t)));
+      s_bc[1] = static_cast<float>(1.0 / sqrt(1.0 - pow(static_cast<double>(p.beta2), t)));
+    }
+    __syncthreads();
+    k.inv_bc1 = s_bc[0];
+    k.inv_sqrt_bc2 = s_bc[1];
+  }
 
   for (int64_t chunk = blockIdx.x; chunk < p.total_chunks; chunk += gridDim.x) {
     int lo = 0, hi = p.njobs - 1;
@@ -107,7 +123,9 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
       for (int64_t i = start + 8 * static_cast<int64_t>(threadIdx.x); i < end; i += 8 * 256) {
         if (i + 8 <= end) {
           F8 w = load8(J.param, J.pdt, i);
-          const F8 g = load8(J.grad, J.gdt, i);
+          F8 g = load8(J.grad, J.gdt, i);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) g.v[e] *= gmul;
           F8 m = load8(J.m, MH_F32, i);
           F8 v = load8(J.v, MH_F32, i);
 #pragma unroll
@@ -118,7 +136,7 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
         } else {
           for (int64_t e = i; e < end; ++e) {
             float w = load1(J.param, J.pdt, e), m = J.m[e], v = J.v[e];
-            adam_elem(w, load1(J.grad, J.gdt, e), m, v, lr, decay, k);
+            adam_elem(w, load1(J.grad, J.gdt, e) * gmul, m, v, lr, decay, k);
             store1(J.param, J.pdt, e, w);
             J.m[e] = m;
             J.v[e] = v;
@@ -128,7 +146,7 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     } else {
       for (int64_t e = start + threadIdx.x; e < end; e += 256) {
         float w = load1(J.param, J.pdt, e), m = J.m[e], v = J.v[e];
-        adam_elem(w, load1(J.grad, J.gdt, e), m, v, lr, decay, k);
+        adam_elem(w, load1(J.grad, J.gdt, e) * gmul, m, v, lr, decay, k);
         store1(J.param, J.pdt, e, w);
         J.m[e] = m;
         J.v[e] = v;

@@ -340,7 +340,8 @@ class ProfScope {
 // last apply stage writes the parameter update (from the per-view records)
 // instead of the last X.
 int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, float eps, int sms,
-           cudaStream_t stream, int* final_buf, bool final_update = false, int cautious = 0) {
+           cudaStream_t stream, int* final_buf, bool final_update = false, int cautious = 0,
+           const int32_t* skip = nullptr) {
   int cur = 0;
   const int nclass = static_cast<int>(P.classes.size());
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
@@ -368,6 +369,7 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           gp.c = c;
           gp.eps = eps;
           gp.status = status;
+          gp.skip = skip;
           const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
           gp.final_update = fused ? 1 : 0;
           gp.cautious = cautious;
@@ -567,10 +569,12 @@ int run_ew(EwKind kind, const Plan& P, const EwParams& proto, Fill fill, int sms
   return run_ew_sel(kind, P, proto, fill, sms, stream, [](const TensorInfo&) { return true; });
 }
 
-int run_view_norm(const Plan& P, float* tile_ss, double* sumsq, cudaStream_t stream) {
+int run_view_norm(const Plan& P, float* tile_ss, double* sumsq, cudaStream_t stream,
+                  const int32_t* skip = nullptr) {
   for (size_t t0 = 0; t0 < P.tensors.size(); t0 += kMaxNormJobs) {
     NormParams np;
     std::memset(&np, 0, sizeof(np));
+    np.skip = skip;
     int64_t views = 0;
     for (size_t t = t0; t < P.tensors.size() && np.njobs < kMaxNormJobs; ++t) {
       const TensorInfo& T = P.tensors[t];
@@ -702,6 +706,8 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   proto.use_colfac = hp->muon_plus ? 1 : 0;
   proto.ns_eps = hp->eps;
   proto.u_scale_from_sumsq = hp->ns_steps == 0 ? 1 : 0;
+  proto.grad_mult = hp->grad_mult;
+  proto.skip = hp->skip;
 
   int final_buf = 0;
   auto fill_common = [&](const TensorInfo& T, EwJob& J, int xbuf) {
@@ -741,9 +747,9 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   rc = run_ew(EW_PROLOGUE, P, proto, [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, 0); },
               sms, stream);
   if (rc != MH_OK) return rc;
-  if ((rc = run_view_norm(P, tile_ss, sumsq, stream)) != MH_OK) return rc;
+  if ((rc = run_view_norm(P, tile_ss, sumsq, stream, hp->skip)) != MH_OK) return rc;
   rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf,
-              fuse_update, hp->cautious);
+              fuse_update, hp->cautious, hp->skip);
   if (rc != MH_OK) return rc;
   if (fuse_update) return MH_OK;
   auto fill_final = [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, final_buf); };
@@ -757,6 +763,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
       rp.muon_plus = hp->muon_plus ? 1 : 0;
       rp.beta2 = hp->beta2;
       rp.plus_eps = hp->plus_eps;
+      rp.skip = hp->skip;
       int64_t views = 0;
       for (size_t t = t0; t < P.tensors.size() && rp.njobs < kMaxRowFinJobs; ++t) {
         const TensorInfo& T = P.tensors[t];
@@ -783,6 +790,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
         ColFinParams cp;
         std::memset(&cp, 0, sizeof(cp));
         cp.plus_eps = hp->plus_eps;
+        cp.skip = hp->skip;
         int64_t total = 0;
         for (size_t t = t0; t < P.tensors.size() && cp.njobs < kMaxColFinJobs; ++t) {
           const TensorInfo& T = P.tensors[t];
@@ -888,11 +896,17 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
                 [&](const TensorInfo& T, EwJob& J) { fill(T, J, final_buf); }, sms, stream);
 }
 
-int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1, float beta2,
-                  float eps, int64_t step, void* stream_) {
+// AdamW over `n` tensors; with a control block the gradient factor, the skip
+// flag and the step count are read on the device.
+static int adamw_impl(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1,
+                      float beta2, float eps, int64_t step, const mh_grad_control* ctl,
+                      void* stream_) {
   if (n < 0) return fail(MH_EINVAL, "n must be >= 0 (got %d)", n);
   if (n > 0 && !tensors) return fail(MH_EINVAL, "tensors is NULL");
-  if (step < 1) return fail(MH_EINVAL, "step must be >= 1 (got %lld)", (long long)step);
+  if (ctl == nullptr && step < 1)
+    return fail(MH_EINVAL, "step must be >= 1 (got %lld)", (long long)step);
+  if (ctl != nullptr && (!ctl->grad_mult || !ctl->skip || !ctl->step))
+    return fail(MH_EINVAL, "the control block needs grad_mult, skip and step");
   if (!std::isfinite(lr)) return fail(MH_EINVAL, "lr must be finite");
   if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
     return fail(MH_EINVAL, "betas must be in [0, 1) (got %g, %g)", beta1, beta2);
@@ -922,10 +936,16 @@ int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float bet
   ap.beta1 = beta1;
   ap.beta2 = beta2;
   ap.eps = eps;
-  const double bc1 = 1.0 - std::pow(double(beta1), double(step));
-  const double bc2 = 1.0 - std::pow(double(beta2), double(step));
-  ap.inv_bc1 = static_cast<float>(1.0 / bc1);
-  ap.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  if (ctl != nullptr) {
+    ap.grad_mult = ctl->grad_mult;
+    ap.skip = ctl->skip;
+    ap.step = ctl->step;
+  } else {
+    const double bc1 = 1.0 - std::pow(double(beta1), double(step));
+    const double bc2 = 1.0 - std::pow(double(beta2), double(step));
+    ap.inv_bc1 = static_cast<float>(1.0 / bc1);
+    ap.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  }
   int64_t chunks = 0;
   auto flush = [&]() -> int {
     ap.total_chunks = chunks;
@@ -960,6 +980,110 @@ int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float bet
     if (ap.njobs == kMaxAdamJobs && (rc = flush()) != MH_OK) return rc;
   }
   if (ap.njobs > 0 && (rc = flush()) != MH_OK) return rc;
+  return MH_OK;
+}
+
+int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1, float beta2,
+                  float eps, int64_t step, void* stream) {
+  return adamw_impl(tensors, n, lr, beta1, beta2, eps, step, nullptr, stream);
+}
+
+int mh_adamw_step_ctl(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1,
+                      float beta2, float eps, const mh_grad_control* ctl, void* stream) {
+  if (!ctl) return fail(MH_EINVAL, "ctl is NULL");
+  return adamw_impl(tensors, n, lr, beta1, beta2, eps, 0, ctl, stream);
+}
+
+// ---- gradient control --------------------------------------------------------
+
+static int check_grads(const mh_grad_ref* grads, int32_t n, int64_t* chunks) {
+  if (n < 0) return fail(MH_EINVAL, "n must be >= 0 (got %d)", n);
+  if (n > 0 && !grads) return fail(MH_EINVAL, "grads is NULL");
+  int64_t c = 0;
+  for (int i = 0; i < n; ++i) {
+    const mh_grad_ref& G = grads[i];
+    if (G.numel < 0) return fail(MH_ESHAPE, "grads[%d]: numel must be >= 0", i);
+    if (!valid_dtype(G.grad_dtype))
+      return fail(MH_EDTYPE, "grads[%d]: only fp32 and bf16 dense gradients are supported", i);
+    if (G.numel > 0 && !G.grad) return fail(MH_EINVAL, "grads[%d]: grad is NULL", i);
+    c += (G.numel + kGradChunk - 1) / kGradChunk;
+  }
+  *chunks = c;
+  return MH_OK;
+}
+
+size_t mh_grad_prepare_workspace_bytes(const mh_grad_ref* grads, int32_t n) {
+  int64_t chunks = 0;
+  if (check_grads(grads, n, &chunks) != MH_OK) return 0;
+  return static_cast<size_t>(std::max<int64_t>(chunks, 1)) * sizeof(double);
+}
+
+int mh_grad_prepare(const mh_grad_ref* grads, int32_t n, float inv_loss_scale, float max_norm,
+                    const mh_grad_control* ctl, void* workspace, size_t workspace_bytes,
+                    void* stream_) {
+  int64_t chunks = 0;
+  int rc = check_grads(grads, n, &chunks);
+  if (rc != MH_OK) return rc;
+  if (!(inv_loss_scale > 0.0f) || !std::isfinite(inv_loss_scale))
+    return fail(MH_EINVAL, "inv_loss_scale must be finite and > 0 (got %g)", inv_loss_scale);
+  if (!(max_norm >= 0.0f) || !std::isfinite(max_norm))
+    return fail(MH_EINVAL, "max_norm must be finite and >= 0 (got %g)", max_norm);
+  if (!ctl || !ctl->grad_mult || !ctl->skip || !ctl->norm)
+    return fail(MH_EINVAL, "ctl, ctl->grad_mult, ctl->skip and ctl->norm must be non-NULL");
+  const size_t need = static_cast<size_t>(std::max<int64_t>(chunks, 1)) * sizeof(double);
+  if (!workspace || workspace_bytes < need)
+    return fail(MH_EWORKSPACE, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) % 8 != 0)
+    return fail(MH_EWORKSPACE, "workspace must be 8-byte aligned");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != MH_OK) return rc;
+  double* partial = static_cast<double*>(workspace);
+
+  GradParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  gp.inv_scale = inv_loss_scale;
+  gp.partial = partial;
+  int64_t next = 0;  // global chunk index of the next tensor
+  auto flush = [&]() -> int {
+    gp.nchunks = next - gp.chunk_first;
+    double bytes = 0.0;
+    for (int k = 0; k < gp.njobs; ++k) bytes += double(gp.jobs[k].numel) * dsize(gp.jobs[k].gdt);
+    ProfScope ps(stream, "grad_norm", bytes);
+    cudaError_t e = launch_grad_sumsq(gp, sms, stream);
+    gp.njobs = 0;
+    gp.chunk_first = next;
+    if (e != cudaSuccess) return cuda_fail(e, "gradient norm launch");
+    return MH_OK;
+  };
+  for (int i = 0; i < n; ++i) {
+    const mh_grad_ref& G = grads[i];
+    if (G.numel == 0) continue;
+    GradJob& J = gp.jobs[gp.njobs++];
+    J.grad = G.grad;
+    J.numel = G.numel;
+    J.gdt = G.grad_dtype;
+    J.vec = aligned16(G.grad) ? 1 : 0;
+    J.chunk_begin = next;
+    next += (G.numel + kGradChunk - 1) / kGradChunk;
+    if (gp.njobs == kMaxGradJobs && (rc = flush()) != MH_OK) return rc;
+  }
+  if (gp.njobs > 0 && (rc = flush()) != MH_OK) return rc;
+
+  GradFinParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.partial = partial;
+  fp.nchunks = next;
+  fp.inv_scale = inv_loss_scale;
+  fp.max_norm = max_norm;
+  fp.clip_eps = 1e-6;
+  fp.mult = ctl->grad_mult;
+  fp.skip = ctl->skip;
+  fp.norm = ctl->norm;
+  fp.step = ctl->step;
+  ProfScope ps(stream, "grad_finalize", 0.0);
+  cudaError_t e = launch_grad_finalize(fp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gradient norm finalisation launch");
   return MH_OK;
 }
 

@@ -203,6 +203,8 @@ __device__ __forceinline__ void store8(void* base, int dt, int64_t off, int nval
 // ||Q||_F^2 partial per warp and chunk.
 __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __grid_constant__ EwParams p) {
   __shared__ __align__(16) EwJob sJ;
+  if (step_skipped(p.skip)) return;
+  const float gmul = p.grad_mult != nullptr ? *p.grad_mult : 1.0f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int cur_job = -1;
   for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
@@ -251,6 +253,8 @@ __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __gr
       if (nv == 0) continue;
       float g[8], q[8];
       load8(J.src, J.src_dtype, view_elem0 + off, nv, J.src_vec, g);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) g[k] *= gmul;
       if (p.use_momentum) {
         float b[8];
         load8(J.mom, MH_F32, view_elem0 + off, nv, J.mom_vec, b);
@@ -280,6 +284,8 @@ __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __gr
 // 2^31 or more tiles).
 __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_constant__ EwParams p) {
   __shared__ __align__(16) EwJob sJ;
+  if (step_skipped(p.skip)) return;
+  const float gmul = p.grad_mult != nullptr ? *p.grad_mult : 1.0f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int cur_job = -1;
 
@@ -337,6 +343,8 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
       if (ok[i]) {
         const int64_t off = view_elem0 + row * J.cols + col;
         load8(J.src, J.src_dtype, off, nvalid, J.src_vec, g[i]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) g[i][k] *= gmul;
         if (p.use_momentum) load8(J.mom, MH_F32, off, nvalid, J.mom_vec, b[i]);
       }
     }
@@ -378,6 +386,7 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
   // indexing a large parameter table per access would keep missing the small
   // constant cache.
   __shared__ __align__(16) EwJob sJ;
+  if (step_skipped(p.skip)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int cur_job = -1;
 
@@ -492,6 +501,7 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
 __global__ void __launch_bounds__(256) row_finalize_kernel(const __grid_constant__ RowFinParams p) {
   __shared__ double red[2][8];
   __shared__ float s_kappa;
+  if (step_skipped(p.skip)) return;
   for (int64_t vv = blockIdx.x; vv < p.total_views; vv += gridDim.x) {
     int lo = 0, hi = p.njobs - 1;
     while (lo < hi) {
@@ -555,6 +565,7 @@ __global__ void __launch_bounds__(256) row_finalize_kernel(const __grid_constant
 }
 
 __global__ void __launch_bounds__(256) col_finalize_kernel(const __grid_constant__ ColFinParams p) {
+  if (step_skipped(p.skip)) return;
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < p.total;
        e += int64_t(gridDim.x) * blockDim.x) {
     int lo = 0, hi = p.njobs - 1;
@@ -576,6 +587,7 @@ __global__ void __launch_bounds__(256) col_finalize_kernel(const __grid_constant
 // each thread summing a fixed stride of them, then a fixed-order tree.
 __global__ void __launch_bounds__(256) view_norm_kernel(const __grid_constant__ NormParams p) {
   __shared__ double red[256];
+  if (step_skipped(p.skip)) return;
   for (int64_t vv = blockIdx.x; vv < p.total_views; vv += gridDim.x) {
     int lo = 0, hi = p.njobs - 1;
     while (lo < hi) {

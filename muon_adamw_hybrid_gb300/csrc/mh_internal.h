@@ -78,7 +78,14 @@ struct EwParams {
   int32_t use_rowfac, use_colfac;
   float ns_eps;
   int32_t u_scale_from_sumsq;  // ns_steps == 0: U = X0 / (||Q|| + eps)
+  const float* grad_mult;      // device: gradients are read as g * (*grad_mult), or null
+  const int32_t* skip;         // device: *skip != 0 -> the kernel returns at once, or null
 };
+
+// True when a gradient-control block asks the step to write nothing.
+__device__ __forceinline__ bool step_skipped(const int32_t* skip) {
+  return skip != nullptr && *skip != 0;
+}
 
 enum EwKind {
   EW_PROLOGUE = 0,       // transposing 32 x 256 tiles (tall views, ragged wide views)
@@ -106,6 +113,7 @@ struct RowFinParams {
   int64_t total_views;
   int32_t normuon, muon_plus;
   float beta2, plus_eps;
+  const int32_t* skip;   // gradient control: return at once when set, or null
 };
 
 // Column finalisation (Muon+ column factor 1/sqrt(sum + eps)), one thread per
@@ -122,6 +130,7 @@ struct ColFinParams {
   int32_t njobs;
   int64_t total;
   float plus_eps;
+  const int32_t* skip;
 };
 
 // Per-view ||Q||_F^2 from the prologue's per-tile partials, one warp per view.
@@ -136,6 +145,7 @@ struct NormParams {
   NormJob jobs[kMaxNormJobs];
   int32_t njobs;
   int64_t total_views;
+  const int32_t* skip;
 };
 
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s);
@@ -203,6 +213,7 @@ struct GemmParams {
   int64_t total_tiles;
   float a, b, c, eps;
   int* status;             // device status word (bounded-wait timeouts)
+  const int32_t* skip;     // gradient control: every thread returns at once when set
 };
 
 size_t gemm_smem_bytes();
@@ -233,10 +244,50 @@ struct AdamParams {
   int32_t njobs;
   int64_t total_chunks;
   float beta1, beta2, eps;
-  float inv_bc1, inv_sqrt_bc2;  // 1/(1-b1^t), 1/sqrt(1-b2^t)
+  float inv_bc1, inv_sqrt_bc2;  // 1/(1-b1^t), 1/sqrt(1-b2^t), when step is null
+  const float* grad_mult;       // device: gradients read as g * (*grad_mult), or null
+  const int32_t* skip;          // device: write nothing when set, or null
+  const int64_t* step;          // device: bias-correction count t, or null (use the above)
 };
 
 cudaError_t launch_adamw(const AdamParams& p, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Gradient control: global norm of the unscaled gradients, clip factor and
+// overflow skip (one pass over every gradient, then a one-block finalise).
+// ---------------------------------------------------------------------------
+constexpr int kMaxGradJobs = 512;
+constexpr int64_t kGradChunk = 65536;  // elements per partial sum
+
+struct GradJob {
+  const void* grad;
+  int64_t numel;
+  int64_t chunk_begin;   // global index of this tensor's first chunk
+  int32_t gdt;
+  int32_t vec;           // 16-byte aligned
+};
+
+struct GradParams {
+  GradJob jobs[kMaxGradJobs];
+  int32_t njobs;
+  int64_t chunk_first;   // first global chunk of this launch
+  int64_t nchunks;       // chunks in this launch
+  float inv_scale;
+  double* partial;       // [all chunks] sum of u^2, NaN if the chunk holds inf/NaN
+};
+
+struct GradFinParams {
+  const double* partial;
+  int64_t nchunks;
+  double inv_scale, max_norm, clip_eps;
+  float* mult;
+  int32_t* skip;
+  double* norm;
+  int64_t* step;
+};
+
+cudaError_t launch_grad_sumsq(const GradParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_grad_finalize(const GradFinParams& p, cudaStream_t s);
 
 // Sets the calling thread's message returned by mh_last_error().
 void set_last_error(const char* msg);

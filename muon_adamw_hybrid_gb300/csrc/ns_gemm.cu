@@ -231,6 +231,9 @@ template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool a_mn = MODE == GEMM_MODE_MM;
   constexpr bool b_mn = MODE != GEMM_MODE_KK;
+  // A skipped step (gradient control): every thread of both CTAs of the pair
+  // reads the same flag and leaves before any barrier, TMEM or cluster op.
+  if (step_skipped(p.skip)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));

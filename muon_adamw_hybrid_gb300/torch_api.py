@@ -10,7 +10,8 @@ from dataclasses import dataclass, field
 import torch
 
 from . import _lib
-from ._lib import MH_BF16, MH_F32, AdamwTensor, MuonHparams, MuonTensor, NsProblem
+from ._lib import (MH_BF16, MH_F32, AdamwTensor, GradControl, GradRef, MuonHparams, MuonTensor,
+                   NsProblem)
 
 # Speedtronic docs "v2 optimizers", "Newton-Schulz": coefficients, steps, eps.
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
@@ -135,6 +136,46 @@ def newton_schulz(xs, outs=None, views=None, steps: int = NS_STEPS, coeffs=NS_CO
     return outs
 
 
+def grad_ref(g: torch.Tensor) -> GradRef:
+    return GradRef(grad=_dev_ptr(g, "grad"), grad_dtype=dtype_code(g), numel=g.numel())
+
+
+class GradientControl:
+    """Device-resident result of grad_prepare, read by the step kernels.
+
+    kimi-k3 "Optimization", "Keep the arithmetic and gradients under control":
+    one global gradient norm over both groups, a clip when max_norm > 0, and
+    the whole hybrid update skipped when an unscaled gradient is inf or NaN.
+    ``grad_mult`` (float32), ``skip`` (int32), ``norm`` (float64) and ``step``
+    (int64, the count of applied steps, used for AdamW's bias correction) are
+    one-element device tensors.
+    """
+
+    def __init__(self, device, step: int = 0):
+        self.grad_mult = torch.ones(1, dtype=torch.float32, device=device)
+        self.skip = torch.zeros(1, dtype=torch.int32, device=device)
+        self.norm = torch.zeros(1, dtype=torch.float64, device=device)
+        self.step = torch.full((1,), int(step), dtype=torch.int64, device=device)
+
+    def struct(self) -> GradControl:
+        return GradControl(grad_mult=self.grad_mult.data_ptr(), skip=self.skip.data_ptr(),
+                           norm=self.norm.data_ptr(), step=self.step.data_ptr())
+
+
+def grad_prepare(grads, control: GradientControl, inv_loss_scale: float = 1.0,
+                 max_norm: float = 0.0, workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Global norm, clip factor and overflow skip of ``grads`` into ``control``
+    (all on the device, stream-ordered). Returns the workspace it used."""
+    refs = [grad_ref(g) for g in grads]
+    need = _lib.grad_prepare_workspace_bytes(refs)
+    if workspace is None or workspace.numel() < need:
+        workspace = alloc_workspace(need, control.norm.device)
+    _lib.grad_prepare(refs, inv_loss_scale, max_norm, control.struct(), workspace.data_ptr(),
+                      workspace.numel(), _stream_ptr(stream))
+    return workspace
+
+
 @dataclass
 class MuonGroupEntry:
     param: torch.Tensor
@@ -163,7 +204,7 @@ class HybridMuonAdamW:
     def __init__(self, muon_params, adamw_params, lr=0.02, momentum=0.95, nesterov=True,
                  ns_steps=NS_STEPS, coeffs=NS_COEFFS, eps=NS_EPS, normuon=False,
                  normuon_beta2=0.95, muon_plus=False, plus_eps=NS_EPS, cautious=0,
-                 adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8):
+                 adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8, max_grad_norm=None):
         self.muon = [e if isinstance(e, MuonGroupEntry) else MuonGroupEntry(**e) for e in muon_params]
         self.adam = [e if isinstance(e, AdamGroupEntry) else AdamGroupEntry(**e) for e in adamw_params]
         self.hp = make_hparams(lr, momentum, nesterov, eps, ns_steps, coeffs, normuon,
@@ -183,6 +224,16 @@ class HybridMuonAdamW:
                         for e in self.adam]
         self.exp_avg_sq = [torch.zeros_like(m) for m in self.exp_avg]
         self._ws = None
+        # Gradient control (global norm / clip / overflow skip), on when
+        # max_grad_norm is given (0 = observe the norm without clipping).
+        self.max_grad_norm = max_grad_norm
+        self.control = None
+        self._gws = None
+        if max_grad_norm is not None:
+            dev = (self.muon or self.adam)[0].param.device
+            self.control = GradientControl(dev)
+            self.hp.grad_mult = self.control.grad_mult.data_ptr()
+            self.hp.skip = self.control.skip.data_ptr()
 
     @property
     def lr(self) -> float:
@@ -203,11 +254,22 @@ class HybridMuonAdamW:
     def workspace_bytes(self) -> int:
         return _lib.muon_workspace_bytes(self._muon_structs([e.param for e in self.muon]), self.hp)
 
-    def step(self, muon_grads=None, adam_grads=None, stream=None) -> None:
-        """One hybrid step. Gradients default to each parameter's ``.grad``."""
+    def step(self, muon_grads=None, adam_grads=None, stream=None,
+             inv_loss_scale: float = 1.0) -> None:
+        """One hybrid step. Gradients default to each parameter's ``.grad``.
+
+        With gradient control on, the gradients are first unscaled by
+        ``inv_loss_scale``, their global norm is taken and clipped to
+        ``max_grad_norm``, and the whole step is skipped on the device when one
+        of them is inf or NaN (``self.control.skip``); no host sync happens."""
         muon_grads = muon_grads if muon_grads is not None else [e.param.grad for e in self.muon]
         adam_grads = adam_grads if adam_grads is not None else [e.param.grad for e in self.adam]
         s = _stream_ptr(stream)
+        if self.control is not None:
+            self._gws = grad_prepare(list(muon_grads) + list(adam_grads), self.control,
+                                     inv_loss_scale, float(self.max_grad_norm), self._gws, stream)
+        elif inv_loss_scale != 1.0:
+            raise ValueError("inv_loss_scale needs gradient control (pass max_grad_norm)")
         self.step_count += 1
         if self.muon:
             ts = self._muon_structs(muon_grads)
@@ -217,11 +279,21 @@ class HybridMuonAdamW:
             _lib.muon_step_batched(ts, self.hp, self._ws.data_ptr(), self._ws.numel(), s)
         if self.adam:
             b1, b2 = self.adam_betas
-            _lib.adamw_step(self._adam_structs(adam_grads), self.adam_lr, b1, b2, self.adam_eps,
-                            self.step_count, s)
+            if self.control is not None:
+                _lib.adamw_step_ctl(self._adam_structs(adam_grads), self.adam_lr, b1, b2,
+                                    self.adam_eps, self.control.struct(), s)
+            else:
+                _lib.adamw_step(self._adam_structs(adam_grads), self.adam_lr, b1, b2,
+                                self.adam_eps, self.step_count, s)
+
+    def applied_steps(self) -> int:
+        """Steps actually applied (skipped ones excluded when gradient control is on)."""
+        if self.control is not None:
+            return int(self.control.step.item())
+        return self.step_count
 
     def state_dict(self) -> dict:
-        return {"step": self.step_count,
+        return {"step": self.applied_steps(),
                 "momentum": [m.clone() for m in self.momentum],
                 "normuon_sm": [None if s is None else s.clone() for s in self.normuon_sm],
                 "exp_avg": [m.clone() for m in self.exp_avg],
@@ -229,6 +301,8 @@ class HybridMuonAdamW:
 
     def load_state_dict(self, sd: dict) -> None:
         self.step_count = int(sd["step"])
+        if self.control is not None:
+            self.control.step.fill_(self.step_count)
         for dst, src in zip(self.momentum, sd["momentum"]):
             dst.copy_(src)
         for dst, src in zip(self.normuon_sm, sd["normuon_sm"]):

@@ -47,10 +47,13 @@ def test_struct_layout_matches_header(tmp_path):
     src = tmp_path / "sizes.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "muonhybrid.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(mh_muon_tensor),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\","
+        " sizeof(mh_muon_tensor),"
         " sizeof(mh_muon_hparams), sizeof(mh_ns_problem), sizeof(mh_adamw_tensor),"
         " offsetof(mh_muon_tensor, views), offsetof(mh_muon_hparams, cautious),"
-        " offsetof(mh_adamw_tensor, numel)); return 0;}\n")
+        " offsetof(mh_adamw_tensor, numel), offsetof(mh_muon_hparams, grad_mult),"
+        " offsetof(mh_muon_hparams, skip), sizeof(mh_grad_ref), sizeof(mh_grad_control),"
+        " offsetof(mh_grad_control, step)); return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                    check=True)
@@ -59,7 +62,9 @@ def test_struct_layout_matches_header(tmp_path):
     want = [ctypes.sizeof(mh.MuonTensor), ctypes.sizeof(mh.MuonHparams),
             ctypes.sizeof(mh.NsProblem), ctypes.sizeof(mh.AdamwTensor),
             mh.MuonTensor.views.offset, mh.MuonHparams.cautious.offset,
-            mh.AdamwTensor.numel.offset]
+            mh.AdamwTensor.numel.offset, mh.MuonHparams.grad_mult.offset,
+            mh.MuonHparams.skip.offset, ctypes.sizeof(mh.GradRef),
+            ctypes.sizeof(mh.GradControl), mh.GradControl.step.offset]
     assert got == want
 
 
@@ -179,3 +184,40 @@ def test_torch_marshalling_rejects_sparse_and_complex():
         mh.dtype_code(torch.zeros(2, 2, dtype=torch.float16))
     with pytest.raises(ValueError):
         mh.muon_tensor(torch.zeros(4, 4), torch.zeros(4, 4), torch.zeros(4, 4))  # not CUDA
+
+
+def test_grad_prepare_rejects_bad_args_before_device_work():
+    L = _lib.LIB
+    g = mh.GradRef(grad=256, grad_dtype=0, numel=70000)
+    arr = (mh.GradRef * 1)(g)
+    ctl = mh.GradControl(grad_mult=512, skip=768, norm=1024, step=0)
+    assert L.mh_grad_prepare_workspace_bytes(arr, 1) == 16        # two 65536-element chunks
+    assert L.mh_grad_prepare(arr, -1, 1.0, 1.0, ctypes.byref(ctl), 4096, 64, None) == _lib.MH_EINVAL
+    assert L.mh_grad_prepare(arr, 1, 0.0, 1.0, ctypes.byref(ctl), 4096, 64, None) == _lib.MH_EINVAL
+    assert L.mh_grad_prepare(arr, 1, float("inf"), 1.0, ctypes.byref(ctl), 4096, 64,
+                             None) == _lib.MH_EINVAL
+    assert L.mh_grad_prepare(arr, 1, 1.0, -1.0, ctypes.byref(ctl), 4096, 64, None) == _lib.MH_EINVAL
+    assert L.mh_grad_prepare(arr, 1, 1.0, 1.0, None, 4096, 64, None) == _lib.MH_EINVAL
+    no_norm = mh.GradControl(grad_mult=512, skip=768, norm=0, step=0)
+    assert L.mh_grad_prepare(arr, 1, 1.0, 1.0, ctypes.byref(no_norm), 4096, 64,
+                             None) == _lib.MH_EINVAL
+    assert L.mh_grad_prepare(arr, 1, 1.0, 1.0, ctypes.byref(ctl), 4096, 8,
+                             None) == _lib.MH_EWORKSPACE
+    assert L.mh_grad_prepare(arr, 1, 1.0, 1.0, ctypes.byref(ctl), 4100, 64,
+                             None) == _lib.MH_EWORKSPACE                     # misaligned
+    bad = (mh.GradRef * 1)(mh.GradRef(grad=256, grad_dtype=7, numel=10))
+    assert L.mh_grad_prepare(bad, 1, 1.0, 1.0, ctypes.byref(ctl), 4096, 64, None) == _lib.MH_EDTYPE
+    null = (mh.GradRef * 1)(mh.GradRef(grad=0, grad_dtype=0, numel=10))
+    assert L.mh_grad_prepare(null, 1, 1.0, 1.0, ctypes.byref(ctl), 4096, 64, None) == _lib.MH_EINVAL
+    neg = (mh.GradRef * 1)(mh.GradRef(grad=256, grad_dtype=0, numel=-1))
+    assert L.mh_grad_prepare_workspace_bytes(neg, 1) == 0
+
+
+def test_adamw_ctl_needs_a_full_control_block():
+    L = _lib.LIB
+    good = mh.AdamwTensor(param=256, grad=512, exp_avg=768, exp_avg_sq=1024, numel=10)
+    arr = (mh.AdamwTensor * 1)(good)
+    assert L.mh_adamw_step_ctl(arr, 1, 1e-3, 0.9, 0.95, 1e-8, None, None) == _lib.MH_EINVAL
+    no_step = mh.GradControl(grad_mult=512, skip=768, norm=1024, step=0)
+    assert L.mh_adamw_step_ctl(arr, 1, 1e-3, 0.9, 0.95, 1e-8, ctypes.byref(no_step),
+                               None) == _lib.MH_EINVAL
