@@ -15,8 +15,10 @@ Readings (the page names neither the hash nor how the seed is composed):
   * The hash is SplitMix64 (Steele, Lea and Flood, "Fast splittable
     pseudorandom number generators", 2014): splitmix64(x) is the generator's
     output from state x, i.e. its finaliser applied to x + 0x9E3779B97F4A7C15.
-  * key(seed, stream) = splitmix64(seed XOR splitmix64(stream)); the noise of
-    flat element i is the top 16 bits of splitmix64(key + i) (mod 2**64).
+  * key(seed, stream) = splitmix64(seed XOR splitmix64(stream)); one hash
+    serves four consecutive elements: the noise of flat element i is bits
+    16*(i mod 4) .. 16*(i mod 4)+15 of splitmix64(key + floor(i / 4))
+    (mod 2**64).
   * stream = 4 * (index of the tensor in its call) + moment, moment 0 for the
     Muon momentum or AdamW's first moment, 1 for AdamW's second moment, 2 for
     the parameter itself.
@@ -65,8 +67,9 @@ def sr_noise16(key: int, index) -> np.ndarray:
     """16 uniform bits for each flat index (uint32 values in [0, 65536))."""
     idx = np.asarray(index, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        h = splitmix64(np.uint64(key) + idx)
-    return (h >> np.uint64(48)).astype(np.uint32)
+        h = splitmix64(np.uint64(key) + (idx >> np.uint64(2)))
+    shift = np.uint64(16) * (idx & np.uint64(3))
+    return ((h >> shift) & np.uint64(0xFFFF)).astype(np.uint32)
 
 
 def round_bf16_with_noise(x, noise16) -> np.ndarray:

@@ -84,6 +84,13 @@ def test_noise_is_uniform_and_streams_differ():
         a, oracle.sr_noise16(oracle.sr_key(5, oracle.sr_stream(0, 0)), idx).astype(np.int64))
 
 
+def test_one_hash_serves_four_elements():
+    key = oracle.sr_key(3, oracle.sr_stream(1, 2))
+    h = oracle.splitmix64((key + 5) & ((1 << 64) - 1))
+    got = oracle.sr_noise16(key, np.arange(20, 24, dtype=np.uint64))
+    assert list(map(int, got)) == [(h >> (16 * k)) & 0xFFFF for k in range(4)]
+
+
 def test_small_increments_survive_in_expectation():
     """dew "bf16_moments": at b2 = 0.999 round-to-nearest loses every
     increment below half a bf16 spacing, stochastic rounding keeps them in
