@@ -228,16 +228,19 @@ class DeviceWorkload:
                                   cautious=hp.get("cautious", 0))
         self.mW = [W.device_tensor(wl, W.KIND_W, i, device=device) for i in range(len(wl.muon))]
         self.mG = [W.device_tensor(wl, W.KIND_G, i, 0, device=device) for i in range(len(wl.muon))]
-        self.mB = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.muon]
+        sdt = torch.bfloat16 if wl.state_dtype == "bf16" else torch.float32
+        self.mB = [torch.zeros(s.shape, dtype=sdt, device=device) for s in wl.muon]
         self.sm = [torch.zeros(s.views * s.rows, dtype=torch.float32, device=device)
                    if self.hp.normuon else None for s in wl.muon]
         self.aW = [W.device_tensor(wl, W.KIND_AW, j, device=device) for j in range(len(wl.adamw))]
         self.aG = [W.device_tensor(wl, W.KIND_AG, j, 0, device=device) for j in range(len(wl.adamw))]
-        self.am = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.adamw]
-        self.av = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.adamw]
-        self.ts = [mh.muon_tensor(w, g, b, s.views, sm, s.lr_mult, s.wd)
+        self.am = [torch.zeros(s.shape, dtype=sdt, device=device) for s in wl.adamw]
+        self.av = [torch.zeros(s.shape, dtype=sdt, device=device) for s in wl.adamw]
+        self.ts = [mh.muon_tensor(w, g, b, s.views, sm, s.lr_mult, s.wd,
+                                  param_sr=wl.param_sr and w.dtype == torch.bfloat16)
                    for w, g, b, sm, s in zip(self.mW, self.mG, self.mB, self.sm, wl.muon)]
-        self.at = [mh.adamw_tensor(w, g, m, v, s.lr_mult, s.wd)
+        self.at = [mh.adamw_tensor(w, g, m, v, s.lr_mult, s.wd,
+                                   param_sr=wl.param_sr and w.dtype == torch.bfloat16)
                    for w, g, m, v, s in zip(self.aW, self.aG, self.am, self.av, wl.adamw)]
         need = mh.muon_workspace_bytes(self.ts, self.hp) if self.ts else 0
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
@@ -261,6 +264,7 @@ class DeviceWorkload:
     def step(self, stream) -> None:
         s = stream.cuda_stream
         self.step_count += 1
+        self.hp.sr_seed = self.step_count
         if self.control is not None:
             self.mh._lib.grad_prepare(self.grefs, 1.0, float(self.max_grad_norm), self.cstruct,
                                       self.gws.data_ptr(), self.gws.numel(), s)
@@ -511,7 +515,9 @@ def config_dict(wl, world, max_grad_norm=None):
             "variants": {k: wl.muon_hp.get(k) for k in ("normuon", "muon_plus", "cautious")
                          if wl.muon_hp.get(k)},
             "precision": "bf16 tensor-core NS operands, fp32 accumulate; fp32 elementwise math "
-                         "and optimizer state; bf16 params/grads",
+                         + ("and optimizer state; bf16 params/grads" if wl.state_dtype == "f32"
+                            else "; bf16 optimizer state and bf16 params, stochastically rounded; "
+                                 "bf16 grads"),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": "inputs larger than L2 (no flush needed)"}, **extra}
 

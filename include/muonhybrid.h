@@ -75,7 +75,7 @@ enum { MH_CAUTIOUS_OFF = 0, MH_CAUTIOUS_WD = 1, MH_CAUTIOUS_UPDATE = 2 };
 typedef struct {
   void* param;            /* (views*rows, cols), param_dtype, updated in place */
   const void* grad;       /* (views*rows, cols), grad_dtype, read only */
-  float* momentum;        /* (views*rows, cols) fp32, updated in place */
+  void* momentum;         /* (views*rows, cols) momentum_dtype, updated in place */
   float* normuon_sm;      /* (views*rows) fp32 NorMuon second moment, updated in
                              place; required when hparams.normuon != 0, else
                              ignored (may be NULL). Zero-initialise it. */
@@ -86,6 +86,10 @@ typedef struct {
   int64_t cols;           /* cols of one view (>= 1) */
   float lr_mult;          /* this tensor's lr = hparams.lr * lr_mult */
   float wd;               /* this tensor's decoupled weight decay */
+  int32_t momentum_dtype; /* MH_F32 (0, default) or MH_BF16: bf16 state, updated in fp32
+                             and written back stochastically rounded (below) */
+  int32_t param_sr;       /* 1: a bf16 param is written stochastically rounded
+                             instead of to nearest even (bf16 params only) */
 } mh_muon_tensor;
 
 /* Muon hyperparameters shared by one call. Defaults from the pages:
@@ -107,6 +111,7 @@ typedef struct {
    * by the kernels of this call, NULL = off): */
   const float* grad_mult;  /* every gradient element is read as g * (*grad_mult) */
   const int32_t* skip;     /* when *skip != 0 the call writes nothing at all */
+  uint64_t sr_seed;        /* stochastic-rounding seed of this call, e.g. the step count */
 } mh_muon_hparams;
 
 /* Bytes of device workspace mh_muon_step_batched needs for these tensors and
@@ -173,14 +178,29 @@ int mh_newton_schulz_batched_noalloc(const mh_ns_problem* problems, int32_t n, i
 typedef struct {
   void* param;            /* numel, param_dtype, updated in place */
   const void* grad;       /* numel, grad_dtype */
-  float* exp_avg;         /* numel fp32 first moment, updated in place */
-  float* exp_avg_sq;      /* numel fp32 second moment, updated in place */
+  void* exp_avg;          /* numel first moment (state_dtype), updated in place */
+  void* exp_avg_sq;       /* numel second moment (state_dtype), updated in place */
   int32_t param_dtype;
   int32_t grad_dtype;
   int64_t numel;          /* >= 0 */
   float lr_mult;
   float wd;
+  int32_t state_dtype;    /* MH_F32 (0, default) or MH_BF16 moments, stochastically rounded */
+  int32_t param_sr;       /* 1: a bf16 param is written stochastically rounded */
 } mh_adamw_tensor;
+
+/* bf16 state (dew.training.optim "bf16_moments", "stochastic_round_bf16"):
+ * the update reads the state widened to fp32, computes in fp32 exactly as for
+ * fp32 state, and writes the new state rounded to bf16 up or down with the
+ * probability of its distance to each: 16 noise bits are added below the kept
+ * mantissa and the low half dropped. The noise of flat element i of a tensor
+ * is the low (i even) or high (i odd) half of fmix32(key + floor(i/2)), with
+ * key = fmix32(fmix32(fmix32(4*t + m) ^ seed_lo) ^ seed_hi): fmix32 the 32-bit
+ * finaliser of MurmurHash3, all arithmetic mod 2^32, t the tensor's index in
+ * the call, m = 0 for the momentum / first moment, 1 for the second moment, 2
+ * for the parameter, seed_lo/hi the halves of the 64-bit seed. The seed is
+ * hparams.sr_seed for Muon and the 1-based step count for AdamW. NaN stays
+ * NaN. */
 
 /* Fused multi-tensor AdamW step (step >= 1, the 1-based count used for bias
  * correction):

@@ -7,7 +7,8 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t, c_void_p
+from ctypes import (POINTER, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t, c_uint64,
+                    c_void_p)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmuonhybrid.so")
@@ -30,7 +31,8 @@ class MuonTensor(ctypes.Structure):
     _fields_ = [("param", c_void_p), ("grad", c_void_p), ("momentum", c_void_p),
                 ("normuon_sm", c_void_p), ("param_dtype", c_int32), ("grad_dtype", c_int32),
                 ("views", c_int64), ("rows", c_int64), ("cols", c_int64),
-                ("lr_mult", c_float), ("wd", c_float)]
+                ("lr_mult", c_float), ("wd", c_float), ("momentum_dtype", c_int32),
+                ("param_sr", c_int32)]
 
 
 class MuonHparams(ctypes.Structure):
@@ -38,7 +40,7 @@ class MuonHparams(ctypes.Structure):
                 ("ns_steps", c_int32), ("a", c_float), ("b", c_float), ("c", c_float),
                 ("normuon", c_int32), ("beta2", c_float), ("muon_plus", c_int32),
                 ("plus_eps", c_float), ("cautious", c_int32),
-                ("grad_mult", c_void_p), ("skip", c_void_p)]
+                ("grad_mult", c_void_p), ("skip", c_void_p), ("sr_seed", c_uint64)]
 
 
 class NsProblem(ctypes.Structure):
@@ -49,7 +51,8 @@ class NsProblem(ctypes.Structure):
 class AdamwTensor(ctypes.Structure):
     _fields_ = [("param", c_void_p), ("grad", c_void_p), ("exp_avg", c_void_p),
                 ("exp_avg_sq", c_void_p), ("param_dtype", c_int32), ("grad_dtype", c_int32),
-                ("numel", c_int64), ("lr_mult", c_float), ("wd", c_float)]
+                ("numel", c_int64), ("lr_mult", c_float), ("wd", c_float),
+                ("state_dtype", c_int32), ("param_sr", c_int32)]
 
 
 class GradRef(ctypes.Structure):

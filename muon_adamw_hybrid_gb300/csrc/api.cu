@@ -38,6 +38,7 @@
 #include <vector>
 
 #include "mh_internal.h"
+#include "mh_sr.cuh"
 #include "muonhybrid.h"
 
 namespace mh {
@@ -485,7 +486,7 @@ double ew_bytes(EwKind kind, const EwParams& p, const EwJob& J) {
   switch (kind) {
     case EW_PROLOGUE:
     case EW_PROLOGUE_FLAT:
-      return e * (dsize(J.src_dtype) + (p.use_momentum ? 8.0 : 0.0) + 2.0);
+      return e * (dsize(J.src_dtype) + (p.use_momentum ? 2.0 * dsize(J.mom_dtype) : 0.0) + 2.0);
     case EW_ROWSQ:
       return e * 2.0;
     case EW_COLSQ:
@@ -618,11 +619,16 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
     if (rc != MH_OK) return rc;
     if (T.views * ceil_div(T.rows, kEwTileR) * ceil_div(T.cols, kEwTileC) >= (int64_t(1) << 31))
       return fail(MH_EUNSUPPORTED, "tensors[%d]: too many elements for one tensor", i);
-    if (!valid_dtype(T.param_dtype) || !valid_dtype(T.grad_dtype))
+    if (!valid_dtype(T.param_dtype) || !valid_dtype(T.grad_dtype) ||
+        !valid_dtype(T.momentum_dtype))
       return fail(MH_EDTYPE,
                   "tensors[%d]: only fp32 and bf16 dense tensors are supported (sparse and complex "
                   "gradients are rejected)",
                   i);
+    if (T.param_sr != 0 && T.param_sr != 1)
+      return fail(MH_EINVAL, "tensors[%d]: param_sr must be 0 or 1", i);
+    if (T.param_sr && T.param_dtype != MH_BF16)
+      return fail(MH_EINVAL, "tensors[%d]: param_sr needs a bf16 parameter", i);
     if (T.views * T.rows * T.cols == 0) continue;
     if (!T.param || !T.grad || !T.momentum)
       return fail(MH_EINVAL, "tensors[%d]: param, grad and momentum must be non-NULL", i);
@@ -715,6 +721,10 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     const ClassInfo& C = P.classes[T.cls];
     J.src = U.grad;
     J.mom = U.momentum;
+    J.mom_dtype = U.momentum_dtype;
+    J.param_sr = U.param_sr;
+    J.mom_key = sr_key(hp->sr_seed, sr_stream(T.idx, SR_FIRST));
+    J.param_key = sr_key(hp->sr_seed, sr_stream(T.idx, SR_PARAM));
     J.dst = U.param;
     J.sm = U.normuon_sm;
     J.src_dtype = U.grad_dtype;
@@ -914,11 +924,16 @@ static int adamw_impl(const mh_adamw_tensor* tensors, int32_t n, float lr, float
   for (int i = 0; i < n; ++i) {
     const mh_adamw_tensor& T = tensors[i];
     if (T.numel < 0) return fail(MH_ESHAPE, "tensors[%d]: numel must be >= 0", i);
-    if (!valid_dtype(T.param_dtype) || !valid_dtype(T.grad_dtype))
+    if (!valid_dtype(T.param_dtype) || !valid_dtype(T.grad_dtype) ||
+        !valid_dtype(T.state_dtype))
       return fail(MH_EDTYPE,
                   "tensors[%d]: only fp32 and bf16 dense tensors are supported (sparse and complex "
                   "gradients are rejected)",
                   i);
+    if (T.param_sr != 0 && T.param_sr != 1)
+      return fail(MH_EINVAL, "tensors[%d]: param_sr must be 0 or 1", i);
+    if (T.param_sr && T.param_dtype != MH_BF16)
+      return fail(MH_EINVAL, "tensors[%d]: param_sr needs a bf16 parameter", i);
     if (T.numel > 0 && (!T.param || !T.grad || !T.exp_avg || !T.exp_avg_sq))
       return fail(MH_EINVAL, "tensors[%d]: param, grad, exp_avg and exp_avg_sq must be non-NULL", i);
     if (!std::isfinite(T.lr_mult) || !std::isfinite(T.wd))
@@ -945,14 +960,15 @@ static int adamw_impl(const mh_adamw_tensor* tensors, int32_t n, float lr, float
     const double bc2 = 1.0 - std::pow(double(beta2), double(step));
     ap.inv_bc1 = static_cast<float>(1.0 / bc1);
     ap.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+    ap.sr_seed = static_cast<uint64_t>(step);
   }
   int64_t chunks = 0;
   auto flush = [&]() -> int {
     ap.total_chunks = chunks;
     double bytes = 0.0;
     for (int k = 0; k < ap.njobs; ++k)
-      bytes += double(ap.jobs[k].numel) *
-               (2.0 * dsize(ap.jobs[k].pdt) + dsize(ap.jobs[k].gdt) + 16.0);
+      bytes += double(ap.jobs[k].numel) * (2.0 * dsize(ap.jobs[k].pdt) + dsize(ap.jobs[k].gdt) +
+                                           4.0 * dsize(ap.jobs[k].sdt));
     ProfScope ps(stream, "adamw", bytes);
     cudaError_t e = launch_adamw(ap, sms, stream);
     ap.njobs = 0;
@@ -975,6 +991,9 @@ static int adamw_impl(const mh_adamw_tensor* tensors, int32_t n, float lr, float
             aligned16(T.exp_avg_sq);
     J.lr = lr * T.lr_mult;
     J.wd = T.wd;
+    J.sdt = T.state_dtype;
+    J.psr = T.param_sr;
+    J.tindex = i;
     J.chunk_begin = chunks;
     chunks += (T.numel + kAdamChunk - 1) / kAdamChunk;
     if (ap.njobs == kMaxAdamJobs && (rc = flush()) != MH_OK) return rc;

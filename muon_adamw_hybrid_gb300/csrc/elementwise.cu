@@ -20,6 +20,7 @@
 // Plus the per-view row finalisation (NorMuon state update, norm restore,
 // Muon+ row factor; flaxchat step 3, Speedtronic "Muon+").
 #include "mh_internal.h"
+#include "mh_sr.cuh"
 #include "muonhybrid.h"
 
 namespace mh {
@@ -196,12 +197,100 @@ __device__ __forceinline__ void store8(void* base, int dt, int64_t off, int nval
   }
 }
 
+// Writes 8 (or nvalid) momentum values at flat element `off` of the tensor:
+// fp32, or bf16 stochastically rounded (dew "bf16_moments").
+__device__ __forceinline__ void store_mom8(const EwJob& J, int64_t off, int nvalid,
+                                           const float (&b)[8]) {
+  if (J.mom_dtype == MH_BF16)
+    store_bf16_sr<8>(static_cast<bf16*>(J.mom) + off, nvalid, J.mom_vec, b, J.mom_key,
+                     static_cast<uint64_t>(off));
+  else
+    store8(J.mom, MH_F32, off, nvalid, J.mom_vec, b);
+}
+
+// Raw 16-byte loads of 8 consecutive elements (bf16: one uint4; fp32: two),
+// kept packed until they are needed so that many can be in flight per thread.
+template <int DT>
+struct Raw8 {
+  uint4 v[DT == MH_F32 ? 2 : 1];
+};
+
+template <int DT>
+__device__ __forceinline__ void raw_load8(Raw8<DT>& r, const void* base, int64_t off) {
+  const uint4* s = DT == MH_F32
+                       ? reinterpret_cast<const uint4*>(static_cast<const float*>(base) + off)
+                       : reinterpret_cast<const uint4*>(static_cast<const bf16*>(base) + off);
+#pragma unroll
+  for (int q = 0; q < (DT == MH_F32 ? 2 : 1); ++q) r.v[q] = __ldcs(s + q);
+}
+
+template <int DT>
+__device__ __forceinline__ void raw_unpack8(const Raw8<DT>& r, float (&o)[8]) {
+  if constexpr (DT == MH_F32) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      o[4 * q + 0] = __uint_as_float(r.v[q].x);
+      o[4 * q + 1] = __uint_as_float(r.v[q].y);
+      o[4 * q + 2] = __uint_as_float(r.v[q].z);
+      o[4 * q + 3] = __uint_as_float(r.v[q].w);
+    }
+  } else {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r.v[0]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      o[2 * k] = f.x;
+      o[2 * k + 1] = f.y;
+    }
+  }
+}
+
+// One full interior chunk of the flat prologue (momentum on, 16-byte aligned
+// gradient and momentum): every load of the chunk is issued before any is
+// consumed, four groups of 8 elements per thread. Returns the thread's share
+// of ||Q||^2. e0: first element of this thread's first group in the tensor;
+// xd: the matching position in X.
+template <int GDT, int MDT>
+__device__ __forceinline__ float prologue_chunk_fast(const EwJob& J, const EwParams& p, float gmul,
+                                                     int64_t e0, bf16* xd) {
+  constexpr int kIt = kProChunk / (8 * kEwThreads);
+  constexpr int kStep = 8 * kEwThreads;
+  Raw8<GDT> gr[kIt];
+  Raw8<MDT> br[kIt];
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    raw_load8<GDT>(gr[it], J.src, e0 + it * kStep);
+    raw_load8<MDT>(br[it], J.mom, e0 + it * kStep);
+  }
+  float ss = 0.0f;
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    float g[8], b[8], q[8];
+    raw_unpack8<GDT>(gr[it], g);
+    raw_unpack8<MDT>(br[it], b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      g[k] *= gmul;
+      b[k] = p.mu * b[k] + (1.0f - p.mu) * g[k];
+      q[k] = p.nesterov ? g[k] + p.mu * (b[k] - g[k]) : b[k];
+      ss += q[k] * q[k];
+    }
+    if constexpr (MDT == MH_BF16)
+      store_bf16_sr<8>(static_cast<bf16*>(J.mom) + e0 + it * kStep, 8, true, b, J.mom_key,
+                       static_cast<uint64_t>(e0 + it * kStep));
+    else
+      store8(J.mom, MH_F32, e0 + it * kStep, 8, true, b);
+    store8(xd + it * kStep, MH_BF16, 0, 8, true, q);
+  }
+  return ss;
+}
+
 // Prologue of views whose X layout equals their stored layout (cols a
 // multiple of 8): a plain contiguous stream, like AdamW. One work item is a
 // kProChunk-element chunk of one view; each thread handles 8 consecutive
 // elements per step, the block 2048 per step, four steps per chunk. One
 // ||Q||_F^2 partial per warp and chunk.
-__global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __grid_constant__ EwParams p) {
+__global__ void __launch_bounds__(kEwThreads, 2) prologue_flat_kernel(const __grid_constant__ EwParams p) {
   __shared__ __align__(16) EwJob sJ;
   if (step_skipped(p.skip)) return;
   const float gmul = p.grad_mult != nullptr ? *p.grad_mult : 1.0f;
@@ -241,10 +330,25 @@ __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __gr
       rec.gdt = J.src_dtype;
       rec.tall = 0;
       rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
+      rec.psr = J.param_sr;
+      rec.psr_key = J.param_key;
       J.vrec[v] = rec;
     }
     bf16* xv = J.x0 + v * J.x_view_stride;
     float ss = 0.0f;
+    if (p.use_momentum && J.src_vec && J.mom_vec && base + kProChunk <= vsz) {
+      const int64_t e0 = view_elem0 + base + 8 * static_cast<int64_t>(threadIdx.x);
+      bf16* xd = xv + base + 8 * static_cast<int64_t>(threadIdx.x);
+      if (J.src_dtype == MH_BF16)
+        ss = J.mom_dtype == MH_BF16 ? prologue_chunk_fast<MH_BF16, MH_BF16>(J, p, gmul, e0, xd)
+                                    : prologue_chunk_fast<MH_BF16, MH_F32>(J, p, gmul, e0, xd);
+      else
+        ss = J.mom_dtype == MH_BF16 ? prologue_chunk_fast<MH_F32, MH_BF16>(J, p, gmul, e0, xd)
+                                    : prologue_chunk_fast<MH_F32, MH_F32>(J, p, gmul, e0, xd);
+      ss = warp_sum(ss);
+      if (lane == 0) J.tile_ss[static_cast<int64_t>(local) * (kEwThreads / 32) + warp] = ss;
+      continue;
+    }
 #pragma unroll 1
     for (int i = 0; i < kProChunk / (8 * kEwThreads); ++i) {
       const int64_t off = base + i * (8 * kEwThreads) + warp * 256 + lane * 8;
@@ -257,13 +361,13 @@ __global__ void __launch_bounds__(kEwThreads, 4) prologue_flat_kernel(const __gr
       for (int k = 0; k < 8; ++k) g[k] *= gmul;
       if (p.use_momentum) {
         float b[8];
-        load8(J.mom, MH_F32, view_elem0 + off, nv, J.mom_vec, b);
+        load8(J.mom, J.mom_dtype, view_elem0 + off, nv, J.mom_vec, b);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           b[k] = p.mu * b[k] + (1.0f - p.mu) * g[k];
           q[k] = p.nesterov ? g[k] + p.mu * (b[k] - g[k]) : b[k];
         }
-        store8(J.mom, MH_F32, view_elem0 + off, nv, J.mom_vec, b);
+        store_mom8(J, view_elem0 + off, nv, b);
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) q[k] = g[k];
@@ -330,6 +434,8 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
       rec.gdt = J.src_dtype;
       rec.tall = 0;
       rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
+      rec.psr = J.param_sr;
+      rec.psr_key = J.param_key;
       J.vrec[v] = rec;
     }
 
@@ -345,7 +451,7 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
         load8(J.src, J.src_dtype, off, nvalid, J.src_vec, g[i]);
 #pragma unroll
         for (int k = 0; k < 8; ++k) g[i][k] *= gmul;
-        if (p.use_momentum) load8(J.mom, MH_F32, off, nvalid, J.mom_vec, b[i]);
+        if (p.use_momentum) load8(J.mom, J.mom_dtype, off, nvalid, J.mom_vec, b[i]);
       }
     }
     float ss = 0.0f;
@@ -362,7 +468,7 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
           b[i][k] = p.mu * b[i][k] + (1.0f - p.mu) * g[i][k];
           q[k] = p.nesterov ? g[i][k] + p.mu * (b[i][k] - g[i][k]) : b[i][k];
         }
-        store8(J.mom, MH_F32, off, nvalid, J.mom_vec, b[i]);
+        store_mom8(J, off, nvalid, b[i]);
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) q[k] = g[i][k];
@@ -490,7 +596,11 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
                 if (delta * gr[k] > 0.0f) w[k] = w[k] - delta;
               }
             }
-            store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
+            if (J.param_sr && J.dst_dtype == MH_BF16)
+              store_bf16_sr<4>(static_cast<bf16*>(J.dst) + off, nvalid, J.dst_vec, w, J.param_key,
+                               static_cast<uint64_t>(off));
+            else
+              store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
           }
         }
       }

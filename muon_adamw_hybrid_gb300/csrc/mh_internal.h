@@ -37,11 +37,13 @@ struct ViewRec {
   int32_t pdt, gdt;
   int32_t tall;
   int32_t vec;          // param and grad 16-byte aligned and cols % 8 == 0
+  int32_t psr;          // bf16 parameter written stochastically rounded
+  uint32_t psr_key;     // its rounding key
 };
 
 struct EwJob {
   const void* src;       // prologue: gradient (Muon) or input x (NS only)
-  float* mom;            // Muon momentum (fp32), null for NS only
+  void* mom;             // Muon momentum (mom_dtype), null for NS only
   void* dst;             // apply: parameter; copy-out: NS output
   float* sm;             // NorMuon second moment (views*rows)
   float* tile_ss;        // per prologue tile and warp: partial ||Q||^2 (this tensor's first)
@@ -64,6 +66,9 @@ struct EwJob {
   int32_t src_dtype, dst_dtype;
   int32_t src_vec, dst_vec, mom_vec;  // 16-byte aligned and cols % 4 == 0
   float lr, wd, shape_scale;
+  int32_t mom_dtype;     // momentum: MH_F32, or MH_BF16 stored stochastically rounded
+  int32_t param_sr;      // bf16 parameter written stochastically rounded
+  uint32_t mom_key, param_key;  // rounding keys (momentum, parameter streams)
 };
 
 struct EwParams {
@@ -230,13 +235,16 @@ constexpr int64_t kAdamChunk = 16384;  // elements per work item
 struct AdamJob {
   void* param;
   const void* grad;
-  float* m;
-  float* v;
+  void* m;               // first moment, sdt
+  void* v;               // second moment, sdt
   int64_t numel;
   int64_t chunk_begin;
   int32_t pdt, gdt;
   int32_t vec;  // all four pointers 16-byte aligned
   float lr, wd;  // lr already multiplied by lr_mult
+  int32_t sdt;   // moments: MH_F32, or MH_BF16 stored stochastically rounded
+  int32_t psr;   // bf16 parameter written stochastically rounded
+  int64_t tindex;  // index of the tensor in the call (its rounding streams)
 };
 
 struct AdamParams {
@@ -248,6 +256,7 @@ struct AdamParams {
   const float* grad_mult;       // device: gradients read as g * (*grad_mult), or null
   const int32_t* skip;          // device: write nothing when set, or null
   const int64_t* step;          // device: bias-correction count t, or null (use the above)
+  uint64_t sr_seed;             // stochastic-rounding seed when step is null (the host step)
 };
 
 cudaError_t launch_adamw(const AdamParams& p, int num_sms, cudaStream_t s);

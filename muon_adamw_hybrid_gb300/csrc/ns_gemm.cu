@@ -45,6 +45,7 @@
 
 #include "mh_internal.h"
 #include "mh_ptx.cuh"
+#include "mh_sr.cuh"
 #include "muonhybrid.h"
 
 namespace mh {
@@ -217,7 +218,11 @@ __device__ __forceinline__ void update_w32(const ViewRec& R, int64_t off, int nv
       if (delta * gr[j] > 0.0f) w[j] = w[j] - delta;
     }
   }
-  store_f32x32(R.param, R.pdt, off, nvalid, vec, w);
+  if (R.psr && R.pdt == MH_BF16)
+    store_bf16_sr<32>(static_cast<bf16*>(R.param) + off, nvalid, vec, w, R.psr_key,
+                      static_cast<uint64_t>(off));
+  else
+    store_f32x32(R.param, R.pdt, off, nvalid, vec, w);
 }
 
 // Raises the abort flag of both CTAs of the pair.

@@ -46,6 +46,13 @@ def _stream_ptr(stream) -> int:
     return int(stream.cuda_stream)
 
 
+def _keep(struct, *tensors):
+    """The C structs hold raw device pointers: the struct object keeps the
+    tensors it points into alive for as long as it lives."""
+    struct._tensors = tuple(t for t in tensors if t is not None)
+    return struct
+
+
 def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_STEPS,
                  coeffs=NS_COEFFS, normuon=False, beta2=0.95, muon_plus=False, plus_eps=NS_EPS,
                  cautious=0) -> MuonHparams:
@@ -71,47 +78,54 @@ def _view_dims(param: torch.Tensor, views: int, rows: int | None = None):
 
 def muon_tensor(param: torch.Tensor, grad: torch.Tensor, momentum: torch.Tensor, views: int = 1,
                 normuon_sm: torch.Tensor | None = None, lr_mult: float = 1.0,
-                wd: float = 0.0, rows: int | None = None) -> MuonTensor:
+                wd: float = 0.0, rows: int | None = None, param_sr: bool = False) -> MuonTensor:
     """One Muon-routed tensor: ``views`` independent matrices of rows x cols.
 
-    ``param`` is (views*rows, cols) or (views, rows, cols), contiguous.
+    ``param`` is (views*rows, cols) or (views, rows, cols), contiguous. The
+    momentum buffer is float32, or bfloat16 (kept stochastically rounded);
+    ``param_sr`` writes a bf16 parameter stochastically rounded.
     """
     v, r, c = _view_dims(param, views, rows)
     if grad.numel() != param.numel() or momentum.numel() != param.numel():
         raise ValueError("grad and momentum must have the parameter's number of elements")
-    if momentum.dtype != torch.float32:
-        raise TypeError("the momentum buffer must be float32")
     sm = 0
     if normuon_sm is not None:
         if normuon_sm.dtype != torch.float32 or normuon_sm.numel() != v * r:
             raise ValueError("normuon_sm must be float32 with views*rows elements")
         sm = _dev_ptr(normuon_sm, "normuon_sm")
-    return MuonTensor(param=_dev_ptr(param, "param"), grad=_dev_ptr(grad, "grad"),
-                      momentum=_dev_ptr(momentum, "momentum"), normuon_sm=sm,
-                      param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), views=v,
-                      rows=r, cols=c, lr_mult=lr_mult, wd=wd)
+    st = MuonTensor(param=_dev_ptr(param, "param"), grad=_dev_ptr(grad, "grad"),
+                    momentum=_dev_ptr(momentum, "momentum"), normuon_sm=sm,
+                    param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), views=v,
+                    rows=r, cols=c, lr_mult=lr_mult, wd=wd, momentum_dtype=dtype_code(momentum),
+                    param_sr=int(bool(param_sr)))
+    return _keep(st, param, grad, momentum, normuon_sm)
 
 
 def adamw_tensor(param, grad, exp_avg, exp_avg_sq, lr_mult: float = 1.0,
-                 wd: float = 0.0) -> AdamwTensor:
+                 wd: float = 0.0, param_sr: bool = False) -> AdamwTensor:
+    """One AdamW tensor; moments float32, or bfloat16 (kept stochastically
+    rounded), both of one dtype."""
     n = param.numel()
     if grad.numel() != n or exp_avg.numel() != n or exp_avg_sq.numel() != n:
         raise ValueError("grad and moments must have the parameter's number of elements")
-    if exp_avg.dtype != torch.float32 or exp_avg_sq.dtype != torch.float32:
-        raise TypeError("AdamW moments must be float32")
-    return AdamwTensor(param=_dev_ptr(param, "param"), grad=_dev_ptr(grad, "grad"),
-                       exp_avg=_dev_ptr(exp_avg, "exp_avg"),
-                       exp_avg_sq=_dev_ptr(exp_avg_sq, "exp_avg_sq"),
-                       param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), numel=n,
-                       lr_mult=lr_mult, wd=wd)
+    if exp_avg.dtype != exp_avg_sq.dtype:
+        raise TypeError("both AdamW moments must have one dtype")
+    st = AdamwTensor(param=_dev_ptr(param, "param"), grad=_dev_ptr(grad, "grad"),
+                     exp_avg=_dev_ptr(exp_avg, "exp_avg"),
+                     exp_avg_sq=_dev_ptr(exp_avg_sq, "exp_avg_sq"),
+                     param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), numel=n,
+                     lr_mult=lr_mult, wd=wd, state_dtype=dtype_code(exp_avg),
+                     param_sr=int(bool(param_sr)))
+    return _keep(st, param, grad, exp_avg, exp_avg_sq)
 
 
 def ns_problem(x: torch.Tensor, out: torch.Tensor, views: int = 1) -> NsProblem:
     v, r, c = _view_dims(x, views)
     if out.numel() != x.numel():
         raise ValueError("out must have x's number of elements")
-    return NsProblem(x=_dev_ptr(x, "x"), out=_dev_ptr(out, "out"), in_dtype=dtype_code(x),
-                     out_dtype=dtype_code(out), views=v, rows=r, cols=c)
+    st = NsProblem(x=_dev_ptr(x, "x"), out=_dev_ptr(out, "out"), in_dtype=dtype_code(x),
+                   out_dtype=dtype_code(out), views=v, rows=r, cols=c)
+    return _keep(st, x, out)
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
@@ -137,7 +151,7 @@ def newton_schulz(xs, outs=None, views=None, steps: int = NS_STEPS, coeffs=NS_CO
 
 
 def grad_ref(g: torch.Tensor) -> GradRef:
-    return GradRef(grad=_dev_ptr(g, "grad"), grad_dtype=dtype_code(g), numel=g.numel())
+    return _keep(GradRef(grad=_dev_ptr(g, "grad"), grad_dtype=dtype_code(g), numel=g.numel()), g)
 
 
 class GradientControl:
@@ -204,14 +218,20 @@ class HybridMuonAdamW:
     def __init__(self, muon_params, adamw_params, lr=0.02, momentum=0.95, nesterov=True,
                  ns_steps=NS_STEPS, coeffs=NS_COEFFS, eps=NS_EPS, normuon=False,
                  normuon_beta2=0.95, muon_plus=False, plus_eps=NS_EPS, cautious=0,
-                 adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8, max_grad_norm=None):
+                 adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8, max_grad_norm=None,
+                 state_dtype=torch.float32, param_sr=False):
         self.muon = [e if isinstance(e, MuonGroupEntry) else MuonGroupEntry(**e) for e in muon_params]
         self.adam = [e if isinstance(e, AdamGroupEntry) else AdamGroupEntry(**e) for e in adamw_params]
         self.hp = make_hparams(lr, momentum, nesterov, eps, ns_steps, coeffs, normuon,
                                normuon_beta2, muon_plus, plus_eps, cautious)
         self.adam_lr, self.adam_betas, self.adam_eps = adam_lr, adam_betas, adam_eps
         self.step_count = 0
-        self.momentum = [torch.zeros(e.param.shape, dtype=torch.float32, device=e.param.device)
+        # dew.training.optim "bf16_moments": bf16 state is kept stochastically
+        # rounded; param_sr does the same for bf16 parameters.
+        if state_dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("state_dtype must be torch.float32 or torch.bfloat16")
+        self.param_sr = bool(param_sr)
+        self.momentum = [torch.zeros(e.param.shape, dtype=state_dtype, device=e.param.device)
                          for e in self.muon]
         self.normuon_sm = []
         for e in self.muon:
@@ -220,7 +240,7 @@ class HybridMuonAdamW:
                 self.normuon_sm.append(torch.zeros(v * r, dtype=torch.float32, device=e.param.device))
             else:
                 self.normuon_sm.append(None)
-        self.exp_avg = [torch.zeros(e.param.shape, dtype=torch.float32, device=e.param.device)
+        self.exp_avg = [torch.zeros(e.param.shape, dtype=state_dtype, device=e.param.device)
                         for e in self.adam]
         self.exp_avg_sq = [torch.zeros_like(m) for m in self.exp_avg]
         self._ws = None
@@ -244,11 +264,13 @@ class HybridMuonAdamW:
         self.hp.lr = value
 
     def _muon_structs(self, grads):
-        return [muon_tensor(e.param, g, m, e.views, sm, e.lr_mult, e.wd)
+        return [muon_tensor(e.param, g, m, e.views, sm, e.lr_mult, e.wd,
+                            param_sr=self.param_sr and e.param.dtype == torch.bfloat16)
                 for e, g, m, sm in zip(self.muon, grads, self.momentum, self.normuon_sm)]
 
     def _adam_structs(self, grads):
-        return [adamw_tensor(e.param, g, m, v, e.lr_mult, e.wd)
+        return [adamw_tensor(e.param, g, m, v, e.lr_mult, e.wd,
+                             param_sr=self.param_sr and e.param.dtype == torch.bfloat16)
                 for e, g, m, v in zip(self.adam, grads, self.exp_avg, self.exp_avg_sq)]
 
     def workspace_bytes(self) -> int:
@@ -271,6 +293,7 @@ class HybridMuonAdamW:
         elif inv_loss_scale != 1.0:
             raise ValueError("inv_loss_scale needs gradient control (pass max_grad_norm)")
         self.step_count += 1
+        self.hp.sr_seed = self.step_count   # a fresh rounding stream every call
         if self.muon:
             ts = self._muon_structs(muon_grads)
             need = _lib.muon_workspace_bytes(ts, self.hp)

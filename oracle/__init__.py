@@ -17,13 +17,13 @@ from .adamw import adamw_step
 from .bf16 import round_bf16
 from .grad_control import CLIP_EPS, GradControl, grad_control
 from .stochastic_round import (MOMENT_FIRST, MOMENT_PARAM, MOMENT_SECOND, round_bf16_with_noise,
-                               splitmix64, sr_key, sr_noise16, sr_stream, stochastic_round_bf16)
+                               fmix32, sr_key, sr_noise16, sr_stream, stochastic_round_bf16)
 
 __all__ = [
     "NS_COEFFS", "NS_EPS", "NS_STEPS", "CAUTIOUS_OFF", "CAUTIOUS_UPDATE", "CAUTIOUS_WD",
     "MuonHparams", "momentum_nesterov", "muon_apply", "muon_plus_row_col", "muon_step_tensor",
     "muon_step_view", "newton_schulz", "normuon", "shape_scale", "adamw_step", "round_bf16",
     "CLIP_EPS", "GradControl", "grad_control", "MOMENT_FIRST", "MOMENT_PARAM", "MOMENT_SECOND",
-    "round_bf16_with_noise", "splitmix64", "sr_key", "sr_noise16", "sr_stream",
+    "round_bf16_with_noise", "fmix32", "sr_key", "sr_noise16", "sr_stream",
     "stochastic_round_bf16",
 ]

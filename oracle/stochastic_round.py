@@ -12,13 +12,14 @@ to fp32 and writes them back stochastically rounded, seeded by the step
 count, the leaf and the moment.
 
 Readings (the page names neither the hash nor how the seed is composed):
-  * The hash is SplitMix64 (Steele, Lea and Flood, "Fast splittable
-    pseudorandom number generators", 2014): splitmix64(x) is the generator's
-    output from state x, i.e. its finaliser applied to x + 0x9E3779B97F4A7C15.
-  * key(seed, stream) = splitmix64(seed XOR splitmix64(stream)); one hash
-    serves four consecutive elements: the noise of flat element i is bits
-    16*(i mod 4) .. 16*(i mod 4)+15 of splitmix64(key + floor(i / 4))
-    (mod 2**64).
+  * The hash is the 32-bit finaliser of MurmurHash3 (Austin Appleby, public
+    domain), fmix32: x ^= x >> 16; x *= 0x85EBCA6B; x ^= x >> 13;
+    x *= 0xC2B2AE35; x ^= x >> 16 (mod 2**32). It is cheap in 32-bit integer
+    arithmetic, which the page's "a few integer ops per element" asks for.
+  * key(seed, stream) = fmix32(fmix32(fmix32(stream) ^ seed_lo) ^ seed_hi),
+    seed_lo / seed_hi the low and high 32 bits of the 64-bit seed. One hash
+    serves two consecutive elements: the noise of flat element i is the low
+    (i even) or high (i odd) 16 bits of fmix32(key + floor(i / 2) mod 2**32).
   * stream = 4 * (index of the tensor in its call) + moment, moment 0 for the
     Muon momentum or AdamW's first moment, 1 for AdamW's second moment, 2 for
     the parameter itself.
@@ -32,31 +33,33 @@ from __future__ import annotations
 
 import numpy as np
 
-_M64 = (1 << 64) - 1
-_INC = 0x9E3779B97F4A7C15
-_C1 = 0xBF58476D1CE4E5B9
-_C2 = 0x94D049BB133111EB
+_M32 = 0xFFFFFFFF
 
 MOMENT_FIRST = 0    # Muon momentum, AdamW exp_avg
 MOMENT_SECOND = 1   # AdamW exp_avg_sq
 MOMENT_PARAM = 2    # the parameter
 
 
-def splitmix64(x):
-    """SplitMix64 output from state x, for a Python int or a uint64 array."""
+def fmix32(x):
+    """MurmurHash3's 32-bit finaliser, for a Python int or a uint32/uint64 array."""
     if isinstance(x, (int, np.integer)):
-        z = (int(x) + _INC) & _M64
-        z = ((z ^ (z >> 30)) * _C1) & _M64
-        z = ((z ^ (z >> 27)) * _C2) & _M64
-        return z ^ (z >> 31)
-    z = np.asarray(x, dtype=np.uint64) + np.uint64(_INC)
-    z = (z ^ (z >> np.uint64(30))) * np.uint64(_C1)
-    z = (z ^ (z >> np.uint64(27))) * np.uint64(_C2)
-    return z ^ (z >> np.uint64(31))
+        x = int(x) & _M32
+        x ^= x >> 16
+        x = (x * 0x85EBCA6B) & _M32
+        x ^= x >> 13
+        x = (x * 0xC2B2AE35) & _M32
+        return x ^ (x >> 16)
+    x = np.asarray(x, dtype=np.uint64) & np.uint64(_M32)
+    x ^= x >> np.uint64(16)
+    x = (x * np.uint64(0x85EBCA6B)) & np.uint64(_M32)
+    x ^= x >> np.uint64(13)
+    x = (x * np.uint64(0xC2B2AE35)) & np.uint64(_M32)
+    return x ^ (x >> np.uint64(16))
 
 
 def sr_key(seed: int, stream: int) -> int:
-    return splitmix64((int(seed) & _M64) ^ splitmix64(int(stream) & _M64))
+    seed = int(seed) & ((1 << 64) - 1)
+    return fmix32(fmix32(fmix32(int(stream) & _M32) ^ (seed & _M32)) ^ (seed >> 32))
 
 
 def sr_stream(tensor_index: int, moment: int) -> int:
@@ -66,9 +69,8 @@ def sr_stream(tensor_index: int, moment: int) -> int:
 def sr_noise16(key: int, index) -> np.ndarray:
     """16 uniform bits for each flat index (uint32 values in [0, 65536))."""
     idx = np.asarray(index, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        h = splitmix64(np.uint64(key) + (idx >> np.uint64(2)))
-    shift = np.uint64(16) * (idx & np.uint64(3))
+    h = fmix32((np.uint64(key) + (idx >> np.uint64(1))) & np.uint64(_M32))
+    shift = np.uint64(16) * (idx & np.uint64(1))
     return ((h >> shift) & np.uint64(0xFFFF)).astype(np.uint32)
 
 

@@ -81,6 +81,8 @@ class Workload:
     adam_hp: dict = field(default_factory=dict)
     steps: int = 1
     seed: int = SEED
+    state_dtype: str = "f32"   # optimizer state: "f32", or "bf16" kept stochastically rounded
+    param_sr: bool = False     # bf16 parameters written stochastically rounded
 
     def grad_std(self, kind: int, index: int) -> np.float32:
         spec = (self.muon if kind == KIND_G else self.adamw)[index]
@@ -147,6 +149,27 @@ def llama7b() -> Workload:
     return Workload("llama7b_d4096_l32", muon, adamw, dict(MUON_HP), dict(ADAM_HP), steps=1)
 
 
+def llama7b_bf16_state() -> Workload:
+    """The 7B-shape set with bf16 optimizer state (Muon momentum, Adam
+    moments) and bf16 parameters, all written stochastically rounded
+    (dew.training.optim "bf16_moments", "stochastic_round_bf16")."""
+    wl = llama7b()
+    wl.name = "llama7b_d4096_l32_bf16state"
+    wl.state_dtype = "bf16"
+    wl.param_sr = True
+    return wl
+
+
+def gpt124m_bf16_state() -> Workload:
+    """The 124M set with bf16 optimizer state and stochastically rounded
+    bf16 parameters (a small case of the bf16-state path)."""
+    wl = gpt124m()
+    wl.name = "gpt124m_d768_l12_bf16state"
+    wl.state_dtype = "bf16"
+    wl.param_sr = True
+    return wl
+
+
 def moe_mla() -> Workload:
     """One MoE layer with 64 experts (gate_up (2, 1408, 2048) as two wide
     views, down 2048 x 1408 tall) and the MLA kv up-projection, 32 heads x
@@ -185,6 +208,8 @@ WORKLOADS = {
     "single": single_matrix,
     "gpt124m": gpt124m,
     "llama7b": llama7b,
+    "llama7b_bf16state": llama7b_bf16_state,
+    "gpt124m_bf16state": gpt124m_bf16_state,
     "moe_mla": moe_mla,
     "adamw_2p30": adamw_2p30,
 }

@@ -10,12 +10,14 @@ def _bits(x32):
     return np.asarray(x32, dtype=np.float32).view(np.uint32)
 
 
-def test_splitmix64_published_outputs():
-    # The first two outputs of SplitMix64 seeded with 0.
-    assert oracle.splitmix64(0) == 0xE220A8397B1DCDAF
-    assert oracle.splitmix64(0x9E3779B97F4A7C15) == 0x6E789E6AA1B965F4
-    vec = oracle.splitmix64(np.array([0, 0x9E3779B97F4A7C15], dtype=np.uint64))
-    assert list(map(int, vec)) == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4]
+def test_fmix32_published_values():
+    """MurmurHash3_x86_32 of the empty input is fmix32(seed): the published
+    test vectors for seeds 0, 1 and 0xFFFFFFFF."""
+    assert oracle.fmix32(0) == 0
+    assert oracle.fmix32(1) == 0x514E28B7
+    assert oracle.fmix32(0xFFFFFFFF) == 0x81F16F39
+    vec = oracle.fmix32(np.array([0, 1, 0xFFFFFFFF], dtype=np.uint64))
+    assert list(map(int, vec)) == [0, 0x514E28B7, 0x81F16F39]
 
 
 @pytest.mark.parametrize("pattern", [0x3F800001, 0x3F807FFF, 0x3F808000, 0x3F80FFFF, 0xBF812345,
@@ -84,11 +86,17 @@ def test_noise_is_uniform_and_streams_differ():
         a, oracle.sr_noise16(oracle.sr_key(5, oracle.sr_stream(0, 0)), idx).astype(np.int64))
 
 
-def test_one_hash_serves_four_elements():
+def test_one_hash_serves_two_elements():
     key = oracle.sr_key(3, oracle.sr_stream(1, 2))
-    h = oracle.splitmix64((key + 5) & ((1 << 64) - 1))
-    got = oracle.sr_noise16(key, np.arange(20, 24, dtype=np.uint64))
-    assert list(map(int, got)) == [(h >> (16 * k)) & 0xFFFF for k in range(4)]
+    h = oracle.fmix32((key + 10) & 0xFFFFFFFF)
+    got = oracle.sr_noise16(key, np.arange(20, 22, dtype=np.uint64))
+    assert list(map(int, got)) == [h & 0xFFFF, h >> 16]
+
+
+def test_key_uses_both_halves_of_the_seed():
+    s = oracle.sr_stream(0, 0)
+    assert oracle.sr_key(5, s) != oracle.sr_key(5 + (1 << 32), s)
+    assert oracle.sr_key(5, s) != oracle.sr_key(5, oracle.sr_stream(0, 1))
 
 
 def test_small_increments_survive_in_expectation():
