@@ -70,9 +70,10 @@ def parse_args():
 # profiles/ is used only while these files still hash to the digest it was
 # taken on; once a kernel changes, its traffic is reported as null.
 KERNEL_SOURCES = {
-    "ns_gemm": ["ns_gemm.cu", "mh_ptx.cuh", "mh_internal.h"],
-    "muon_prologue": ["elementwise.cu", "mh_internal.h"],
-    "adamw": ["adamw.cu", "mh_internal.h"],
+    "ns_gemm": ["ns_gemm.cu", "mh_ptx.cuh", "mh_internal.h", "mh_sr.cuh"],
+    "muon_prologue": ["elementwise.cu", "mh_internal.h", "mh_sr.cuh"],
+    "adamw": ["adamw.cu", "mh_internal.h", "mh_sr.cuh"],
+    "grad_norm": ["grad_control.cu", "mh_internal.h"],
 }
 
 
