@@ -17,7 +17,9 @@ Sources (page title, section):
 
 Readings taken where the pages are silent or ambiguous (each also listed in
 the design notes):
-  * Frobenius normalisation is X = T / (||T||_F + eps) with eps = 1e-7 [SPD].
+  * Frobenius normalisation is X = T / (||T||_F + eps) with eps = 1e-7 [SPD];
+    flaxchat's Polar Express form X = g / (||g|| * 1.01) is norm_scale 1.01
+    with eps 0, and its per-iteration coefficients a schedule of (a, b, c).
   * "tall" means rows > cols strictly; a square matrix is not transposed.
   * The shape scale uses the stored view's rows/cols: max(1, rows/cols)**0.5.
   * NorMuon [FLX step 3]: statistics per row of the stored view (mean over
@@ -57,6 +59,7 @@ class MuonHparams:
     eps: float = NS_EPS
     ns_steps: int = NS_STEPS
     coeffs: tuple = NS_COEFFS
+    norm_scale: float = 1.0       # X = Q / (||Q|| * norm_scale + eps)
     normuon: bool = False
     beta2: float = 0.95
     muon_plus: bool = False
@@ -79,20 +82,37 @@ def momentum_nesterov(B: np.ndarray, G: np.ndarray, mu: float, nesterov: bool = 
     return B_new, Q
 
 
+def coeff_schedule(coeffs, steps: int):
+    """One (a, b, c) per step: a single triple repeated, or a sequence of
+    `steps` triples taken in order."""
+    c = np.asarray(coeffs, dtype=np.float64)
+    if c.shape == (3,):
+        return [tuple(c)] * steps
+    if c.shape != (steps, 3):
+        raise ValueError(f"need one (a, b, c) or {steps} of them, got shape {c.shape}")
+    return [tuple(r) for r in c]
+
+
 def newton_schulz(Q: np.ndarray, steps: int = NS_STEPS, coeffs=NS_COEFFS,
-                  eps: float = NS_EPS) -> np.ndarray:
+                  eps: float = NS_EPS, norm_scale: float = 1.0) -> np.ndarray:
     """[SPD "Newton-Schulz"]: quintic iteration on one matrix.
 
     A tall matrix (rows > cols) is transposed, normalised, iterated and
     transposed back. Each step forms A = X X^T and X <- a X + (b A + c A^2) X.
-    A zero matrix stays zero (eps keeps the division finite).
+
+    The normalisation is X = T / (||T||_F * norm_scale + eps): Speedtronic's
+    form with norm_scale 1 and eps 1e-7; flaxchat's Polar Express (step 2,
+    X <- g / (||g|| * 1.01), then one (a, b, c) per iteration from a list)
+    with norm_scale 1.01, eps 0 and a coefficient schedule. A zero matrix
+    stays zero (with eps 0 the division is skipped).
     """
-    a, b, c = coeffs
+    sched = coeff_schedule(coeffs, steps)
     Q = np.asarray(Q, dtype=np.float64)
     tall = Q.shape[0] > Q.shape[1]
     T = Q.T if tall else Q
-    X = T / (np.sqrt(np.sum(T * T)) + eps)
-    for _ in range(steps):
+    den = np.sqrt(np.sum(T * T)) * norm_scale + eps
+    X = T / den if den > 0 else np.zeros_like(T)
+    for a, b, c in sched:
         A = X @ X.T
         P = b * A + c * (A @ A)
         X = a * X + P @ X
@@ -170,7 +190,7 @@ def muon_step_view(W, G, B, hp: MuonHparams, lr_mult: float = 1.0, wd: float = 0
     G = np.asarray(G, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
     B_new, Q = momentum_nesterov(B, G, hp.momentum, hp.nesterov)
-    U = newton_schulz(Q, hp.ns_steps, hp.coeffs, hp.eps)
+    U = newton_schulz(Q, hp.ns_steps, hp.coeffs, hp.eps, hp.norm_scale)
     sm_new = None
     if hp.normuon:
         U, sm_new = normuon(U, np.zeros(W.shape[0]) if sm is None else np.asarray(sm, np.float64),

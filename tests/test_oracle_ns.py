@@ -161,3 +161,59 @@ def test_brute_force_tiny(shape):
     Q = synth.normal(7, shape[0] * 10 + shape[1], shape).astype(np.float64)
     want = np.array(_brute_ns(Q.tolist(), STEPS, EPS))
     np.testing.assert_allclose(oracle.newton_schulz(Q), want, rtol=1e-12, atol=1e-14)
+
+
+# ---- coefficient schedules and the Polar Express normalisation ---------------------
+# flaxchat "Optimizer", "Muon Algorithm" step 2: X <- g / (||g|| * 1.01), then one
+# (a, b, c) per iteration from a list. The page prints no coefficient values, so
+# the schedules below are arbitrary; the pins hold for any schedule.
+
+SCHED = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.6, -2.4, 0.8), (2.0, -1.5, 0.5),
+         (1.875, -1.25, 0.375)]
+
+
+def spectral_schedule(Q, sched, eps, norm_scale):
+    """U (p_k o ... o p_1)(Sigma) V^T from the SVD of Q / (||Q|| * norm_scale + eps),
+    p_i(s) = a_i s + b_i s^3 + c_i s^5 applied in the schedule's order."""
+    Q = np.asarray(Q, dtype=np.float64)
+    U, s, Vt = np.linalg.svd(Q / (np.linalg.norm(Q) * norm_scale + eps), full_matrices=False)
+    for a, b, c in sched:
+        s = a * s + b * s ** 3 + c * s ** 5
+    return (U * s[None, :]) @ Vt
+
+
+@pytest.mark.parametrize("shape", [(24, 40), (40, 24), (32, 32), (5, 17)])
+@pytest.mark.parametrize("norm_scale,eps", [(1.0, EPS), (1.01, 0.0)])
+def test_schedule_spectral_pin(shape, norm_scale, eps):
+    Q = synth.normal(9, shape[0] * 100 + shape[1], shape).astype(np.float64)
+    got = oracle.newton_schulz(Q, steps=len(SCHED), coeffs=SCHED, eps=eps, norm_scale=norm_scale)
+    want = spectral_schedule(Q, SCHED, eps, norm_scale)
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-11
+
+
+def test_schedule_order_matters_and_constant_schedule_is_the_triple():
+    Q = synth.normal(9, 1, (20, 36)).astype(np.float64)
+    fwd = oracle.newton_schulz(Q, steps=5, coeffs=SCHED)
+    rev = oracle.newton_schulz(Q, steps=5, coeffs=SCHED[::-1])
+    assert np.linalg.norm(fwd - rev) / np.linalg.norm(fwd) > 1e-3
+    const = oracle.newton_schulz(Q, steps=5, coeffs=[(A, B, C)] * 5)
+    np.testing.assert_array_equal(const, oracle.newton_schulz(Q))
+
+
+def test_polar_express_normalisation_keeps_zero_and_scales():
+    Z = np.zeros((6, 9))
+    out = oracle.newton_schulz(Z, steps=5, coeffs=SCHED, eps=0.0, norm_scale=1.01)
+    assert np.all(out == 0)
+    Q = synth.normal(9, 2, (12, 30)).astype(np.float64)
+    # with eps 0 the normalised input is scale-free: NS(alpha Q) == NS(Q)
+    a = oracle.newton_schulz(Q, steps=5, coeffs=SCHED, eps=0.0, norm_scale=1.01)
+    b = oracle.newton_schulz(1e3 * Q, steps=5, coeffs=SCHED, eps=0.0, norm_scale=1.01)
+    assert np.linalg.norm(a - b) / np.linalg.norm(a) < 1e-12
+    # and its largest input singular value is 1/1.01 of the Frobenius-normalised one
+    s = np.linalg.svd(Q / (np.linalg.norm(Q) * 1.01), compute_uv=False)
+    assert s[0] < 1.0 / 1.01 + 1e-15
+
+
+def test_schedule_length_must_match_steps():
+    with pytest.raises(ValueError):
+        oracle.newton_schulz(np.eye(4), steps=3, coeffs=SCHED)
