@@ -99,7 +99,7 @@ typedef struct {
   float lr;
   float momentum;     /* mu in [0, 1) */
   int32_t nesterov;   /* 1: Q = lerp(G, B, mu); 0: Q = B */
-  float eps;          /* Frobenius-normalisation guard, > 0 */
+  float eps;          /* Frobenius-normalisation guard, >= 0 */
   int32_t ns_steps;   /* 0..16 quintic iterations */
   float a, b, c;      /* quintic coefficients */
   int32_t normuon;    /* 1: NorMuon per-row second moment (flaxchat step 3) */
@@ -112,6 +112,12 @@ typedef struct {
   const float* grad_mult;  /* every gradient element is read as g * (*grad_mult) */
   const int32_t* skip;     /* when *skip != 0 the call writes nothing at all */
   uint64_t sr_seed;        /* stochastic-rounding seed of this call, e.g. the step count */
+  /* Polar Express form (flaxchat "Muon Algorithm" step 2): one (a, b, c) per
+   * iteration and X = Q / (||Q||_F * norm_scale + eps), e.g. norm_scale 1.01
+   * with eps 0. */
+  const float* coeff_schedule;  /* HOST array of ns_steps x 3 floats (a, b, c of each
+                                   iteration in order), or NULL: (a, b, c) above every time */
+  float norm_scale;             /* > 0; 0 means 1 (the Speedtronic form) */
 } mh_muon_hparams;
 
 /* Bytes of device workspace mh_muon_step_batched needs for these tensors and
@@ -147,6 +153,15 @@ size_t mh_ns_workspace_bytes(const mh_ns_problem* problems, int32_t n);
 int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t steps, float a,
                              float b, float c, float eps, void* workspace,
                              size_t workspace_bytes, void* stream);
+
+/* mh_newton_schulz_batched with one (a, b, c) per iteration and the
+ * normalisation X = X0 / (||X0||_F * norm_scale + eps) (flaxchat "Muon
+ * Algorithm" step 2, Polar Express: norm_scale 1.01, eps 0): `coeffs` is a HOST
+ * array of steps x 3 floats, read during the call. norm_scale > 0, eps >= 0;
+ * a zero matrix stays zero. Same workspace as mh_newton_schulz_batched. */
+int mh_newton_schulz_batched_ex(const mh_ns_problem* problems, int32_t n, int32_t steps,
+                                const float* coeffs, float eps, float norm_scale,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the fixed scratch array behind mh_newton_schulz_batched_noalloc. */
 #define MH_NS_STATIC_SCRATCH_BYTES ((size_t)64 << 20)

@@ -23,7 +23,7 @@ EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_
             "mh_newton_schulz_batched", "mh_adamw_step", "mh_workspace_status", "mh_last_error",
             "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read",
             "mh_newton_schulz_batched_noalloc", "mh_grad_prepare_workspace_bytes",
-            "mh_grad_prepare", "mh_adamw_step_ctl")
+            "mh_grad_prepare", "mh_adamw_step_ctl", "mh_newton_schulz_batched_ex")
 NS_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -40,7 +40,8 @@ class MuonHparams(ctypes.Structure):
                 ("ns_steps", c_int32), ("a", c_float), ("b", c_float), ("c", c_float),
                 ("normuon", c_int32), ("beta2", c_float), ("muon_plus", c_int32),
                 ("plus_eps", c_float), ("cautious", c_int32),
-                ("grad_mult", c_void_p), ("skip", c_void_p), ("sr_seed", c_uint64)]
+                ("grad_mult", c_void_p), ("skip", c_void_p), ("sr_seed", c_uint64),
+                ("coeff_schedule", c_void_p), ("norm_scale", c_float)]
 
 
 class NsProblem(ctypes.Structure):
@@ -93,6 +94,10 @@ def _load() -> ctypes.CDLL:
                                              c_float, c_float, c_float, c_void_p, c_size_t,
                                              c_void_p]
     lib.mh_newton_schulz_batched.restype = c_int
+    lib.mh_newton_schulz_batched_ex.argtypes = [POINTER(NsProblem), c_int32, c_int32,
+                                                POINTER(c_float), c_float, c_float, c_void_p,
+                                                c_size_t, c_void_p]
+    lib.mh_newton_schulz_batched_ex.restype = c_int
     lib.mh_newton_schulz_batched_noalloc.argtypes = [POINTER(NsProblem), c_int32, c_int32,
                                                      c_float, c_float, c_float, c_float, c_void_p]
     lib.mh_newton_schulz_batched_noalloc.restype = c_int
@@ -169,6 +174,17 @@ def newton_schulz_batched(problems, steps: int, a: float, b: float, c: float, ep
     arr, n = _array(NsProblem, problems)
     _check(LIB.mh_newton_schulz_batched(arr, n, steps, a, b, c, eps, workspace, workspace_bytes,
                                         stream))
+
+
+def newton_schulz_batched_ex(problems, coeffs, eps: float, norm_scale: float, workspace: int,
+                             workspace_bytes: int, stream: int) -> None:
+    """Newton-Schulz with one (a, b, c) per iteration (a sequence of triples)
+    and the normalisation X0 / (||X0|| * norm_scale + eps)."""
+    arr, n = _array(NsProblem, problems)
+    flat = [float(v) for t in coeffs for v in t]
+    carr = (c_float * max(len(flat), 1))(*flat)
+    _check(LIB.mh_newton_schulz_batched_ex(arr, n, len(coeffs), carr, eps, norm_scale, workspace,
+                                           workspace_bytes, stream))
 
 
 def newton_schulz_batched_noalloc(problems, steps: int, a: float, b: float, c: float, eps: float,

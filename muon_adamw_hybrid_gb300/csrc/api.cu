@@ -340,9 +340,13 @@ class ProfScope {
 // Launches the 3 * steps grouped GEMM stages. When `final_update` is set, the
 // last apply stage writes the parameter update (from the per-view records)
 // instead of the last X.
+// Newton-Schulz stages of every view: `steps` iterations, iteration `it`
+// using (sched[3 it], sched[3 it + 1], sched[3 it + 2]) when a schedule is
+// given, else (a, b, c).
 int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, float eps, int sms,
            cudaStream_t stream, int* final_buf, bool final_update = false, int cautious = 0,
-           const int32_t* skip = nullptr) {
+           const int32_t* skip = nullptr, const float* sched = nullptr,
+           float norm_scale = 1.0f) {
   int cur = 0;
   const int nclass = static_cast<int>(P.classes.size());
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
@@ -365,10 +369,11 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           gp.kind = kind;
           gp.mode = mode;
           gp.first_iter = it == 0 ? 1 : 0;
-          gp.a = a;
-          gp.b = b;
-          gp.c = c;
+          gp.a = sched ? sched[3 * it] : a;
+          gp.b = sched ? sched[3 * it + 1] : b;
+          gp.c = sched ? sched[3 * it + 2] : c;
           gp.eps = eps;
+          gp.norm_scale = norm_scale;
           gp.status = status;
           gp.skip = skip;
           const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
@@ -602,11 +607,17 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
   if (!std::isfinite(hp->lr)) return fail(MH_EINVAL, "lr must be finite");
   if (!(hp->momentum >= 0.0f && hp->momentum < 1.0f))
     return fail(MH_EINVAL, "momentum must be in [0, 1) (got %g)", hp->momentum);
-  if (!(hp->eps > 0.0f) || !std::isfinite(hp->eps)) return fail(MH_EINVAL, "eps must be > 0");
+  if (!(hp->eps >= 0.0f) || !std::isfinite(hp->eps)) return fail(MH_EINVAL, "eps must be >= 0");
+  if (!(hp->norm_scale >= 0.0f) || !std::isfinite(hp->norm_scale))
+    return fail(MH_EINVAL, "norm_scale must be finite and >= 0 (0 means 1)");
   if (hp->ns_steps < 0 || hp->ns_steps > 16)
     return fail(MH_EINVAL, "ns_steps must be in [0, 16] (got %d)", hp->ns_steps);
   if (!std::isfinite(hp->a) || !std::isfinite(hp->b) || !std::isfinite(hp->c))
     return fail(MH_EINVAL, "Newton-Schulz coefficients must be finite");
+  if (hp->coeff_schedule)
+    for (int k = 0; k < 3 * hp->ns_steps; ++k)
+      if (!std::isfinite(hp->coeff_schedule[k]))
+        return fail(MH_EINVAL, "coeff_schedule[%d] is not finite", k);
   if (hp->normuon && !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
     return fail(MH_EINVAL, "beta2 must be in [0, 1) (got %g)", hp->beta2);
   if (hp->muon_plus && !(hp->plus_eps > 0.0f))
@@ -711,6 +722,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   proto.use_rowfac = need_rows ? 1 : 0;
   proto.use_colfac = hp->muon_plus ? 1 : 0;
   proto.ns_eps = hp->eps;
+  proto.ns_norm_scale = hp->norm_scale > 0.0f ? hp->norm_scale : 1.0f;
   proto.u_scale_from_sumsq = hp->ns_steps == 0 ? 1 : 0;
   proto.grad_mult = hp->grad_mult;
   proto.skip = hp->skip;
@@ -759,7 +771,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   if (rc != MH_OK) return rc;
   if ((rc = run_view_norm(P, tile_ss, sumsq, stream, hp->skip)) != MH_OK) return rc;
   rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf,
-              fuse_update, hp->cautious, hp->skip);
+              fuse_update, hp->cautious, hp->skip, hp->coeff_schedule, proto.ns_norm_scale);
   if (rc != MH_OK) return rc;
   if (fuse_update) return MH_OK;
   auto fill_final = [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, final_buf); };
@@ -837,15 +849,22 @@ size_t mh_ns_workspace_bytes(const mh_ns_problem* problems, int32_t n) {
   return make_plan(shapes, false, false).bytes;
 }
 
-int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t steps, float a,
-                             float b, float c, float eps, void* workspace,
-                             size_t workspace_bytes, void* stream_) {
+// Newton-Schulz only; `sched` (host, steps x 3) overrides (a, b, c) when
+// non-null.
+static int ns_impl(const mh_ns_problem* problems, int32_t n, int32_t steps, float a, float b,
+                   float c, const float* sched, float eps, float norm_scale, void* workspace,
+                   size_t workspace_bytes, void* stream_) {
   if (n < 0) return fail(MH_EINVAL, "n must be >= 0 (got %d)", n);
   if (n > 0 && !problems) return fail(MH_EINVAL, "problems is NULL");
   if (steps < 0 || steps > 16) return fail(MH_EINVAL, "steps must be in [0, 16] (got %d)", steps);
-  if (!(eps > 0.0f) || !std::isfinite(eps)) return fail(MH_EINVAL, "eps must be > 0");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(MH_EINVAL, "eps must be >= 0");
+  if (!(norm_scale > 0.0f) || !std::isfinite(norm_scale))
+    return fail(MH_EINVAL, "norm_scale must be finite and > 0");
   if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c))
     return fail(MH_EINVAL, "Newton-Schulz coefficients must be finite");
+  if (sched)
+    for (int k = 0; k < 3 * steps; ++k)
+      if (!std::isfinite(sched[k])) return fail(MH_EINVAL, "coeffs[%d] is not finite", k);
   std::vector<Shape> shapes(n);
   for (int i = 0; i < n; ++i) {
     const mh_ns_problem& p = problems[i];
@@ -876,6 +895,7 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
   std::memset(&proto, 0, sizeof(proto));
   proto.use_momentum = 0;
   proto.ns_eps = eps;
+  proto.ns_norm_scale = norm_scale;
   proto.u_scale_from_sumsq = steps == 0 ? 1 : 0;
   int final_buf = 0;
   auto fill = [&](const TensorInfo& T, EwJob& J, int xbuf) {
@@ -900,10 +920,27 @@ int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t s
               stream);
   if (rc != MH_OK) return rc;
   if ((rc = run_view_norm(P, tile_ss, sumsq, stream)) != MH_OK) return rc;
-  rc = run_ns(P, ws, steps, a, b, c, eps, sms, stream, &final_buf);
+  rc = run_ns(P, ws, steps, a, b, c, eps, sms, stream, &final_buf, false, 0, nullptr, sched,
+              norm_scale);
   if (rc != MH_OK) return rc;
   return run_ew(EW_COPYOUT, P, proto,
                 [&](const TensorInfo& T, EwJob& J) { fill(T, J, final_buf); }, sms, stream);
+}
+
+int mh_newton_schulz_batched(const mh_ns_problem* problems, int32_t n, int32_t steps, float a,
+                             float b, float c, float eps, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!(eps > 0.0f)) return fail(MH_EINVAL, "eps must be > 0");
+  return ns_impl(problems, n, steps, a, b, c, nullptr, eps, 1.0f, workspace, workspace_bytes,
+                 stream);
+}
+
+int mh_newton_schulz_batched_ex(const mh_ns_problem* problems, int32_t n, int32_t steps,
+                                const float* coeffs, float eps, float norm_scale,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (steps > 0 && !coeffs) return fail(MH_EINVAL, "coeffs is NULL");
+  return ns_impl(problems, n, steps, 0.0f, 0.0f, 0.0f, coeffs, eps, norm_scale, workspace,
+                 workspace_bytes, stream);
 }
 
 // AdamW over `n` tensors; with a control block the gradient factor, the skip

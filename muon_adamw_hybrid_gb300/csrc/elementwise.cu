@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
         // EW_APPLY / EW_COPYOUT: final update direction U_ij.
         float uscale = 1.0f;
         if (p.u_scale_from_sumsq)
-          uscale = 1.0f / (sqrtf(static_cast<float>(J.sumsq[t.v])) + p.ns_eps);
+          uscale = ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps);
         float h[4] = {1.f, 1.f, 1.f, 1.f};
         if (p.use_colfac) {
 #pragma unroll

@@ -82,10 +82,17 @@ struct EwParams {
   int32_t cautious;
   int32_t use_rowfac, use_colfac;
   float ns_eps;
-  int32_t u_scale_from_sumsq;  // ns_steps == 0: U = X0 / (||Q|| + eps)
+  float ns_norm_scale;         // X0 = Q / (||Q|| * ns_norm_scale + ns_eps)
+  int32_t u_scale_from_sumsq;  // ns_steps == 0: U = X0
   const float* grad_mult;      // device: gradients are read as g * (*grad_mult), or null
   const int32_t* skip;         // device: *skip != 0 -> the kernel returns at once, or null
 };
+
+// 1 / (||Q|| * norm_scale + eps), or 0 for a zero matrix with eps 0.
+__host__ __device__ __forceinline__ float ns_inv_norm(double sumsq, float norm_scale, float eps) {
+  const float den = sqrtf(static_cast<float>(sumsq)) * norm_scale + eps;
+  return den > 0.0f ? 1.0f / den : 0.0f;
+}
 
 // True when a gradient-control block asks the step to write nothing.
 __device__ __forceinline__ bool step_skipped(const int32_t* skip) {
@@ -217,6 +224,7 @@ struct GemmParams {
   int32_t cautious;        // MH_CAUTIOUS_* for the final update
   int64_t total_tiles;
   float a, b, c, eps;
+  float norm_scale;        // first iteration: X0 = Q / (||Q|| * norm_scale + eps)
   int* status;             // device status word (bounded-wait timeouts)
   const int32_t* skip;     // gradient control: every thread returns at once when set
 };

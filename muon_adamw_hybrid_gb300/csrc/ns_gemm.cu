@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const int n_out = apply ? C.out_cols : C.m;
       float sc = 1.0f;
       if (p.first_iter) {
-        const float s = 1.0f / (sqrtf(static_cast<float>(C.sumsq[tc.view])) + p.eps);
+        const float s = ns_inv_norm(C.sumsq[tc.view], p.norm_scale, p.eps);
         sc = apply ? s : s * s;
       }
       bf16* out = C.out + static_cast<int64_t>(tc.view) * C.out_view_stride;

@@ -5,6 +5,7 @@ optimizer runs in libmuonhybrid's kernels.
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass, field
 
 import torch
@@ -55,11 +56,27 @@ def _keep(struct, *tensors):
 
 def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_STEPS,
                  coeffs=NS_COEFFS, normuon=False, beta2=0.95, muon_plus=False, plus_eps=NS_EPS,
-                 cautious=0) -> MuonHparams:
-    a, b, c = coeffs
-    return MuonHparams(lr=lr, momentum=momentum, nesterov=int(bool(nesterov)), eps=eps,
-                       ns_steps=ns_steps, a=a, b=b, c=c, normuon=int(bool(normuon)), beta2=beta2,
-                       muon_plus=int(bool(muon_plus)), plus_eps=plus_eps, cautious=int(cautious))
+                 cautious=0, norm_scale=1.0) -> MuonHparams:
+    """Muon hyperparameters. ``coeffs`` is one (a, b, c) for every iteration, or
+    a sequence of ``ns_steps`` triples (flaxchat's Polar Express schedule);
+    ``norm_scale`` gives X0 = Q / (||Q|| * norm_scale + eps)."""
+    sched = None
+    if len(coeffs) and not isinstance(coeffs[0], (int, float)):
+        if len(coeffs) != ns_steps:
+            raise ValueError(f"the schedule has {len(coeffs)} triples for {ns_steps} steps")
+        flat = [float(v) for t in coeffs for v in t]
+        sched = (ctypes.c_float * len(flat))(*flat)
+        a, b, c = coeffs[0]
+    else:
+        a, b, c = coeffs
+    hp = MuonHparams(lr=lr, momentum=momentum, nesterov=int(bool(nesterov)), eps=eps,
+                     ns_steps=ns_steps, a=a, b=b, c=c, normuon=int(bool(normuon)), beta2=beta2,
+                     muon_plus=int(bool(muon_plus)), plus_eps=plus_eps, cautious=int(cautious),
+                     norm_scale=norm_scale)
+    if sched is not None:
+        hp.coeff_schedule = ctypes.addressof(sched)
+        hp._sched = sched          # the library reads it during each call
+    return hp
 
 
 def _view_dims(param: torch.Tensor, views: int, rows: int | None = None):
@@ -134,8 +151,10 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def newton_schulz(xs, outs=None, views=None, steps: int = NS_STEPS, coeffs=NS_COEFFS,
-                  eps: float = NS_EPS, workspace: torch.Tensor | None = None, stream=None):
-    """U = NS(X) for a list of matrices (or stacks of views); returns the outputs."""
+                  eps: float = NS_EPS, workspace: torch.Tensor | None = None, stream=None,
+                  norm_scale: float = 1.0):
+    """U = NS(X) for a list of matrices (or stacks of views); returns the outputs.
+    ``coeffs``: one (a, b, c), or ``steps`` of them (one per iteration)."""
     xs = list(xs)
     if outs is None:
         outs = [torch.empty_like(x) for x in xs]
@@ -144,9 +163,19 @@ def newton_schulz(xs, outs=None, views=None, steps: int = NS_STEPS, coeffs=NS_CO
     need = _lib.ns_workspace_bytes(probs)
     if workspace is None or workspace.numel() < need:
         workspace = alloc_workspace(need, xs[0].device)
-    a, b, c = coeffs
-    _lib.newton_schulz_batched(probs, steps, a, b, c, eps, workspace.data_ptr(), workspace.numel(),
-                               _stream_ptr(stream))
+    if len(coeffs) and not isinstance(coeffs[0], (int, float)):
+        if len(coeffs) != steps:
+            raise ValueError(f"the schedule has {len(coeffs)} triples for {steps} steps")
+        _lib.newton_schulz_batched_ex(probs, list(coeffs), eps, norm_scale, workspace.data_ptr(),
+                                      workspace.numel(), _stream_ptr(stream))
+    elif norm_scale != 1.0:
+        _lib.newton_schulz_batched_ex(probs, [tuple(coeffs)] * steps, eps, norm_scale,
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream_ptr(stream))
+    else:
+        a, b, c = coeffs
+        _lib.newton_schulz_batched(probs, steps, a, b, c, eps, workspace.data_ptr(),
+                                   workspace.numel(), _stream_ptr(stream))
     return outs
 
 

@@ -25,6 +25,7 @@ def oracle_hparams(wl: W.Workload) -> oracle.MuonHparams:
     hp = wl.muon_hp
     return oracle.MuonHparams(lr=hp["lr"], momentum=hp["momentum"], nesterov=hp["nesterov"],
                               eps=hp["eps"], ns_steps=hp["ns_steps"], coeffs=tuple(hp["coeffs"]),
+                              norm_scale=hp.get("norm_scale", 1.0),
                               normuon=hp.get("normuon", False), beta2=hp.get("beta2", 0.95),
                               muon_plus=hp.get("muon_plus", False),
                               plus_eps=hp.get("plus_eps", hp["eps"]),
@@ -91,6 +92,7 @@ class GpuRun:
         hp = wl.muon_hp
         self.hp = mh.make_hparams(lr=hp["lr"], momentum=hp["momentum"], nesterov=hp["nesterov"],
                                   eps=hp["eps"], ns_steps=hp["ns_steps"], coeffs=hp["coeffs"],
+                                  norm_scale=hp.get("norm_scale", 1.0),
                                   normuon=hp.get("normuon", False), beta2=hp.get("beta2", 0.95),
                                   muon_plus=hp.get("muon_plus", False),
                                   plus_eps=hp.get("plus_eps", hp["eps"]),

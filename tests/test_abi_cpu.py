@@ -53,7 +53,10 @@ def test_struct_layout_matches_header(tmp_path):
         " offsetof(mh_muon_tensor, views), offsetof(mh_muon_hparams, cautious),"
         " offsetof(mh_adamw_tensor, numel), offsetof(mh_muon_hparams, grad_mult),"
         " offsetof(mh_muon_hparams, skip), sizeof(mh_grad_ref), sizeof(mh_grad_control),"
-        " offsetof(mh_grad_control, step)); return 0;}\n")
+        " offsetof(mh_grad_control, step)); printf(\"%zu %zu %zu %zu\\n\","
+        " offsetof(mh_muon_hparams, sr_seed), offsetof(mh_muon_hparams, coeff_schedule),"
+        " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, momentum_dtype));"
+        " return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                    check=True)
@@ -64,7 +67,9 @@ def test_struct_layout_matches_header(tmp_path):
             mh.MuonTensor.views.offset, mh.MuonHparams.cautious.offset,
             mh.AdamwTensor.numel.offset, mh.MuonHparams.grad_mult.offset,
             mh.MuonHparams.skip.offset, ctypes.sizeof(mh.GradRef),
-            ctypes.sizeof(mh.GradControl), mh.GradControl.step.offset]
+            ctypes.sizeof(mh.GradControl), mh.GradControl.step.offset,
+            mh.MuonHparams.sr_seed.offset, mh.MuonHparams.coeff_schedule.offset,
+            mh.MuonHparams.norm_scale.offset, mh.MuonTensor.momentum_dtype.offset]
     assert got == want
 
 
@@ -96,7 +101,9 @@ def test_muon_rejects_bad_tensor(kw, code):
     assert mh.last_error() != ""
 
 
-@pytest.mark.parametrize("kw", [dict(momentum=1.0), dict(momentum=-0.1), dict(eps=0.0),
+@pytest.mark.parametrize("kw", [dict(momentum=1.0), dict(momentum=-0.1), dict(eps=-1e-7),
+                                dict(norm_scale=-1.0), dict(norm_scale=float("nan")),
+                                dict(ns_steps=2, coeffs=[(1.0, 0.0, 0.0), (float("nan"), 0, 0)]),
                                 dict(ns_steps=17), dict(ns_steps=-1), dict(cautious=3),
                                 dict(coeffs=(float("inf"), 0, 0)),
                                 dict(normuon=True, beta2=1.0)])
@@ -221,3 +228,23 @@ def test_adamw_ctl_needs_a_full_control_block():
     no_step = mh.GradControl(grad_mult=512, skip=768, norm=1024, step=0)
     assert L.mh_adamw_step_ctl(arr, 1, 1e-3, 0.9, 0.95, 1e-8, ctypes.byref(no_step),
                                None) == _lib.MH_EINVAL
+
+
+def test_ns_ex_rejects_bad_args():
+    p = mh.NsProblem(x=256, out=512, in_dtype=0, out_dtype=0, views=1, rows=8, cols=8)
+    arr = (mh.NsProblem * 1)(p)
+    L = _lib.LIB
+    co = (ctypes.c_float * 6)(3.0, -4.0, 2.0, 2.0, -1.5, 0.5)
+    assert L.mh_newton_schulz_batched_ex(arr, 1, 2, None, 0.0, 1.01, None, 0, None) == _lib.MH_EINVAL
+    assert L.mh_newton_schulz_batched_ex(arr, 1, 2, co, 0.0, 0.0, None, 0, None) == _lib.MH_EINVAL
+    assert L.mh_newton_schulz_batched_ex(arr, 1, 2, co, -1.0, 1.0, None, 0, None) == _lib.MH_EINVAL
+    bad = (ctypes.c_float * 6)(3.0, -4.0, float("inf"), 2.0, -1.5, 0.5)
+    assert L.mh_newton_schulz_batched_ex(arr, 1, 2, bad, 0.0, 1.01, None, 0, None) == _lib.MH_EINVAL
+    # valid arguments get as far as the workspace check
+    assert L.mh_newton_schulz_batched_ex(arr, 1, 2, co, 0.0, 1.01, None, 0,
+                                         None) == _lib.MH_EWORKSPACE
+
+
+def test_schedule_length_is_checked_in_python():
+    with pytest.raises(ValueError):
+        mh.make_hparams(ns_steps=3, coeffs=[(1.0, 0.0, 0.0)] * 2)

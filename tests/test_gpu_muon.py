@@ -169,3 +169,19 @@ def test_repeat_call_same_workspace_is_reproducible():
     r2.step()
     torch.cuda.synchronize()
     assert rel_fro(to_np(r1.mW[0]), to_np(r2.mW[0])) < 1e-6
+
+
+def test_polar_express_schedule_step():
+    """flaxchat "Muon Algorithm" step 2 in the full step: X = Q / (||Q|| * 1.01),
+    one (a, b, c) per iteration (arbitrary values: the page prints none)."""
+    sched = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.6, -2.4, 0.8), (2.0, -1.5, 0.5),
+             (1.875, -1.25, 0.375)]
+    specs = [W.MuonSpec("a", 2, 256, 512, "f32", "f32", w_std=1.0, g_std=1.0),
+             W.MuonSpec("b", 1, 384, 128, "bf16", "bf16"),
+             W.MuonSpec("c", 1, 96, 200, "f32", "f32", w_std=0.5, g_std=0.3)]
+    wl = _wl(specs, coeffs=sched, eps=0.0, norm_scale=1.01)
+    run = GpuRun(wl)
+    w0 = [to_np(w).copy() for w in run.mW]
+    run.step()
+    run.status_ok()
+    _check(wl, run, w_prev=w0)

@@ -16,13 +16,15 @@ pytestmark = pytest.mark.gpu
 COEFFS = (3.4445, -4.7750, 2.0315)
 
 
-def gpu_ns(mats, steps=5, coeffs=COEFFS, eps=1e-7, views=None, in_dtype="f32", out_dtype="f32"):
+def gpu_ns(mats, steps=5, coeffs=COEFFS, eps=1e-7, views=None, in_dtype="f32", out_dtype="f32",
+           norm_scale=1.0):
     import torch
     import muon_adamw_hybrid_gb300 as mh
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
     xs = [torch.tensor(m.reshape(-1, m.shape[-1]), dtype=tdt[in_dtype], device="cuda") for m in mats]
     outs = [torch.full_like(x, float("nan"), dtype=tdt[out_dtype]) for x in xs]
-    mh.newton_schulz(xs, outs, views=views, steps=steps, coeffs=coeffs, eps=eps)
+    mh.newton_schulz(xs, outs, views=views, steps=steps, coeffs=coeffs, eps=eps,
+                     norm_scale=norm_scale)
     torch.cuda.synchronize()
     return [to_np(o) for o in outs]
 
@@ -129,3 +131,34 @@ def test_ns_large(shape):
     Q = _mat(22, shape[0], shape)
     got = gpu_ns([Q])[0]
     assert rel_fro(got, oracle.newton_schulz(Q)) < 2e-2
+
+
+# ---- coefficient schedules and the Polar Express normalisation (flaxchat "Muon
+# Algorithm" step 2). The page prints no coefficients; any schedule must match.
+SCHED = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.6, -2.4, 0.8), (2.0, -1.5, 0.5),
+         (1.875, -1.25, 0.375)]
+
+
+@pytest.mark.parametrize("shape", [(256, 768), (768, 256), (300, 200), (64, 1000)])
+@pytest.mark.parametrize("norm_scale,eps", [(1.01, 0.0), (1.0, 1e-7)])
+def test_schedule_matches_oracle(shape, norm_scale, eps):
+    Q = _mat(40, shape[0] + shape[1], shape)
+    got = gpu_ns([Q], steps=5, coeffs=SCHED, eps=eps, norm_scale=norm_scale)[0]
+    want = oracle.newton_schulz(Q, steps=5, coeffs=SCHED, eps=eps, norm_scale=norm_scale)
+    assert rel_fro(got, want) < 2e-2, rel_fro(got, want)
+    # a constant schedule is the plain iteration
+    const = gpu_ns([Q], steps=5, coeffs=[COEFFS] * 5)[0]
+    assert rel_fro(const, gpu_ns([Q])[0]) < 1e-6
+
+
+def test_schedule_zero_matrix_without_eps_stays_zero():
+    got = gpu_ns([np.zeros((128, 384)), np.zeros((300, 100))], steps=5, coeffs=SCHED, eps=0.0,
+                 norm_scale=1.01)
+    for g in got:
+        assert np.all(g == 0)
+
+
+def test_zero_steps_with_norm_scale():
+    Q = _mat(41, 1, (100, 260), std=5.0)
+    got = gpu_ns([Q], steps=0, coeffs=[], eps=0.0, norm_scale=1.01)[0]
+    assert rel_fro(got, Q / (np.linalg.norm(Q) * 1.01)) < 5e-3
