@@ -182,13 +182,24 @@ class ViewResult:
 
 
 def muon_step_view(W, G, B, hp: MuonHparams, lr_mult: float = 1.0, wd: float = 0.0,
-                   sm=None) -> ViewResult:
+                   sm=None, skip_zero_grad: bool = False) -> ViewResult:
     """One Muon update of one r x c view, in the pages' order:
     momentum + Nesterov -> Newton-Schulz -> [NorMuon] -> [Muon+] -> apply.
+
+    skip_zero_grad [KIMI "One more kind of state: which experts learn?";
+    "A tensor's storage shape can be misleading": unselected experts with no
+    gradient are not quietly decayed]: a view whose gradient is zero
+    everywhere is left as it is -- parameter, momentum and NorMuon state --
+    and its update direction is zero.
     """
     W = np.asarray(W, dtype=np.float64)
     G = np.asarray(G, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
+    if skip_zero_grad and not np.any(G):
+        keep_sm = None
+        if hp.normuon:
+            keep_sm = np.zeros(W.shape[0]) if sm is None else np.asarray(sm, np.float64).copy()
+        return ViewResult(W=W.copy(), B=B.copy(), U=np.zeros_like(W), sm=keep_sm)
     B_new, Q = momentum_nesterov(B, G, hp.momentum, hp.nesterov)
     U = newton_schulz(Q, hp.ns_steps, hp.coeffs, hp.eps, hp.norm_scale)
     sm_new = None
@@ -203,7 +214,7 @@ def muon_step_view(W, G, B, hp: MuonHparams, lr_mult: float = 1.0, wd: float = 0
 
 
 def muon_step_tensor(W, G, B, hp: MuonHparams, views: int = 1, lr_mult: float = 1.0,
-                     wd: float = 0.0, sm=None):
+                     wd: float = 0.0, sm=None, skip_zero_grad: bool = False):
     """[KIMI "storage shape"]: a packed tensor declared as (views, r, c) is
     ``views`` independent r x c matrices sharing one momentum buffer.
 
@@ -226,7 +237,7 @@ def muon_step_tensor(W, G, B, hp: MuonHparams, views: int = 1, lr_mult: float = 
     smn = np.empty((views, r)) if hp.normuon else None
     for k in range(views):
         res = muon_step_view(Wv[k], Gv[k], Bv[k], hp, lr_mult, wd,
-                             None if smv is None else smv[k])
+                             None if smv is None else smv[k], skip_zero_grad)
         Wn[k], Bn[k], Un[k] = res.W, res.B, res.U
         if hp.normuon:
             smn[k] = res.sm

@@ -177,3 +177,62 @@ def test_full_view_step_composes_pieces():
     U, _ = oracle.normuon(U, np.zeros(9), hp.beta2)
     U = oracle.muon_plus_row_col(U, hp.plus_eps)
     np.testing.assert_array_equal(res.W, oracle.muon_apply(W, U, G, hp.lr * 0.5, 0.1, 1))
+
+
+# ---- inactive experts (kimi-k3 "Optimization", "One more kind of state: which
+# experts learn?": an expert that received no gradient acquires no momentum and
+# no weight decay) ------------------------------------------------------------
+
+def _expert(seed):
+    W = synth.normal(seed, 1, (24, 40)).astype(np.float64)
+    B = synth.normal(seed, 2, (24, 40), std=1e-2).astype(np.float64)
+    return W, B
+
+
+def test_zero_gradient_view_is_left_alone_with_the_flag():
+    W, B = _expert(50)
+    for hp in (oracle.MuonHparams(), oracle.MuonHparams(normuon=True)):
+        sm = np.full(24, 0.3)
+        r = oracle.muon_step_view(W, np.zeros_like(W), B, hp, 1.0, 0.1, sm, skip_zero_grad=True)
+        np.testing.assert_array_equal(r.W, W)
+        np.testing.assert_array_equal(r.B, B)
+        assert np.all(r.U == 0)
+        if hp.normuon:
+            np.testing.assert_array_equal(r.sm, sm)
+
+
+def test_without_the_flag_a_zero_gradient_view_still_moves():
+    """The closed form the flag prevents: B <- mu B, and the step runs on
+    Q = mu B with decay (1 - lr wd)."""
+    W, B = _expert(51)
+    hp = oracle.MuonHparams()
+    r = oracle.muon_step_view(W, np.zeros_like(W), B, hp, 1.0, 0.1)
+    np.testing.assert_allclose(r.B, hp.momentum * B, rtol=1e-15)
+    U = oracle.newton_schulz(hp.momentum * hp.momentum * B)
+    want = (1 - hp.lr * 0.1) * W - hp.lr * U     # 24 x 40: shape scale 1
+    np.testing.assert_allclose(r.W, want, rtol=1e-12, atol=1e-15)
+
+
+def test_flag_does_not_touch_views_with_any_gradient():
+    W, B = _expert(52)
+    G = np.zeros_like(W)
+    G[3, 7] = 1e-3                                 # one routed token is enough
+    hp = oracle.MuonHparams()
+    a = oracle.muon_step_view(W, G, B, hp, 1.0, 0.1, skip_zero_grad=True)
+    b = oracle.muon_step_view(W, G, B, hp, 1.0, 0.1)
+    np.testing.assert_array_equal(a.W, b.W)
+    np.testing.assert_array_equal(a.B, b.B)
+
+
+def test_flag_is_per_view_in_a_packed_tensor():
+    """A packed (2, r, c) tensor with one silent view: only that view stays."""
+    W = synth.normal(53, 1, (2 * 24, 40)).astype(np.float64)
+    B = synth.normal(53, 2, (2 * 24, 40), std=1e-2).astype(np.float64)
+    G = synth.normal(53, 3, (2 * 24, 40), std=1e-3).astype(np.float64)
+    G[:24] = 0.0
+    hp = oracle.MuonHparams()
+    Wn, Bn, _, _ = oracle.muon_step_tensor(W, G, B, hp, views=2, wd=0.1, skip_zero_grad=True)
+    np.testing.assert_array_equal(Wn[:24], W[:24])
+    np.testing.assert_array_equal(Bn[:24], B[:24])
+    ref = oracle.muon_step_view(W[24:], G[24:], B[24:], hp, 1.0, 0.1)
+    np.testing.assert_array_equal(Wn[24:], ref.W)
