@@ -90,6 +90,11 @@ typedef struct {
                              and written back stochastically rounded (below) */
   int32_t param_sr;       /* 1: a bf16 param is written stochastically rounded
                              instead of to nearest even (bf16 params only) */
+  int32_t skip_zero_grad; /* 1: inactive-expert rule (kimi-k3 "Optimization", "One more
+                             kind of state: which experts learn?"): a view whose
+                             gradient is zero everywhere keeps its parameter,
+                             momentum and NorMuon state unchanged. Costs one read
+                             of the gradients of silent views (a chunk for others). */
 } mh_muon_tensor;
 
 /* Muon hyperparameters shared by one call. Defaults from the pages:

@@ -32,7 +32,7 @@ class MuonTensor(ctypes.Structure):
                 ("normuon_sm", c_void_p), ("param_dtype", c_int32), ("grad_dtype", c_int32),
                 ("views", c_int64), ("rows", c_int64), ("cols", c_int64),
                 ("lr_mult", c_float), ("wd", c_float), ("momentum_dtype", c_int32),
-                ("param_sr", c_int32)]
+                ("param_sr", c_int32), ("skip_zero_grad", c_int32)]
 
 
 class MuonHparams(ctypes.Structure):

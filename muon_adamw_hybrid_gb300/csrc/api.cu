@@ -97,6 +97,7 @@ struct Plan {
   std::vector<TensorInfo> tensors;
   int64_t total_views = 0, total_tiles = 0;
   int64_t n_rowpart = 0, n_rowfac = 0, n_colpart = 0, n_colfac = 0;
+  size_t off_active = 0;  // int32 per view (inactive-expert rule)
   size_t off_sumsq = 0, off_tile_ss = 0, off_vrec = 0, off_rowpart = 0, off_rowfac = 0,
          off_colpart = 0, off_colfac = 0;
   size_t bytes = 0;
@@ -175,6 +176,8 @@ Plan make_plan(const std::vector<Shape>& shapes, bool need_rows, bool need_cols)
   off = align_up(off + sizeof(float) * (kEwThreads / 32) * static_cast<size_t>(P.total_tiles), 256);
   P.off_vrec = off;
   off = align_up(off + sizeof(ViewRec) * static_cast<size_t>(P.total_views), 256);
+  P.off_active = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(P.total_views), 256);
   if (need_rows) {
     P.off_rowpart = off;
     off = align_up(off + sizeof(float) * static_cast<size_t>(P.n_rowpart), 256);
@@ -600,6 +603,49 @@ int run_view_norm(const Plan& P, float* tile_ss, double* sumsq, cudaStream_t str
   return MH_OK;
 }
 
+// Inactive-expert rule: clears the per-view flags and marks the views of
+// flagged tensors that have a nonzero gradient entry.
+int run_view_active(const Plan& P, const mh_muon_tensor* tensors, int32_t* active, int sms,
+                    cudaStream_t stream) {
+  bool any = false;
+  for (const TensorInfo& T : P.tensors) any = any || tensors[T.idx].skip_zero_grad;
+  if (!any) return MH_OK;
+  cudaError_t e = cudaMemsetAsync(active, 0, sizeof(int32_t) * P.total_views, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(active flags)");
+  ActiveParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  int64_t chunks = 0;
+  auto flush = [&]() -> int {
+    ap.total_chunks = chunks;
+    double bytes = 0.0;
+    for (int k = 0; k < ap.njobs; ++k)
+      bytes += double(ap.jobs[k].view_elems) * ap.jobs[k].views * dsize(ap.jobs[k].gdt);
+    ProfScope ps(stream, "muon_active", bytes);
+    cudaError_t err = launch_view_active(ap, sms, stream);
+    ap.njobs = 0;
+    chunks = 0;
+    if (err != cudaSuccess) return cuda_fail(err, "inactive-expert scan launch");
+    return MH_OK;
+  };
+  int rc;
+  for (const TensorInfo& T : P.tensors) {
+    const mh_muon_tensor& U = tensors[T.idx];
+    if (!U.skip_zero_grad) continue;
+    ActiveJob& J = ap.jobs[ap.njobs++];
+    J.grad = U.grad;
+    J.active = active + T.view_slot;
+    J.view_elems = T.rows * T.cols;
+    J.views = T.views;
+    J.gdt = U.grad_dtype;
+    J.vec = aligned16(U.grad) && (J.view_elems % 8) == 0;
+    J.chunk_begin = chunks;
+    chunks += T.views * ((J.view_elems + kActiveChunk - 1) / kActiveChunk);
+    if (ap.njobs == kMaxActiveJobs && (rc = flush()) != MH_OK) return rc;
+  }
+  if (ap.njobs > 0 && (rc = flush()) != MH_OK) return rc;
+  return MH_OK;
+}
+
 int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* hp) {
   if (n < 0) return fail(MH_EINVAL, "n must be >= 0 (got %d)", n);
   if (n > 0 && !t) return fail(MH_EINVAL, "tensors is NULL");
@@ -640,6 +686,8 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
       return fail(MH_EINVAL, "tensors[%d]: param_sr must be 0 or 1", i);
     if (T.param_sr && T.param_dtype != MH_BF16)
       return fail(MH_EINVAL, "tensors[%d]: param_sr needs a bf16 parameter", i);
+    if (T.skip_zero_grad != 0 && T.skip_zero_grad != 1)
+      return fail(MH_EINVAL, "tensors[%d]: skip_zero_grad must be 0 or 1", i);
     if (T.views * T.rows * T.cols == 0) continue;
     if (!T.param || !T.grad || !T.momentum)
       return fail(MH_EINVAL, "tensors[%d]: param, grad and momentum must be non-NULL", i);
@@ -708,6 +756,8 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   float* colpart = reinterpret_cast<float*>(ws + P.off_colpart);
   float* colfac = reinterpret_cast<float*>(ws + P.off_colfac);
   ViewRec* vrec = reinterpret_cast<ViewRec*>(ws + P.off_vrec);
+  int32_t* active = reinterpret_cast<int32_t*>(ws + P.off_active);
+  if ((rc = run_view_active(P, tensors, active, sms, stream)) != MH_OK) return rc;
   const bool need_rows = hp->normuon || hp->muon_plus;
   // Without NorMuon / Muon+ the update needs nothing beyond U itself, so the
   // last Newton-Schulz apply stage writes the parameters directly.
@@ -737,6 +787,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     J.param_sr = U.param_sr;
     J.mom_key = sr_key(hp->sr_seed, sr_stream(T.idx, SR_FIRST));
     J.param_key = sr_key(hp->sr_seed, sr_stream(T.idx, SR_PARAM));
+    J.active = U.skip_zero_grad ? active + T.view_slot : nullptr;
     J.dst = U.param;
     J.sm = U.normuon_sm;
     J.src_dtype = U.grad_dtype;
@@ -798,6 +849,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
         J.views = T.views;
         J.tiles_c = T.tiles_c;
         J.view_begin = views;
+        J.active = tensors[T.idx].skip_zero_grad ? active + T.view_slot : nullptr;
         views += T.views;
       }
       rp.total_views = views;

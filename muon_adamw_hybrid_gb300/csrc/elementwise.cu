@@ -30,6 +30,7 @@ static_assert(sizeof(EwParams) <= 32000, "EwParams exceeds the kernel parameter 
 static_assert(sizeof(RowFinParams) <= 32000, "RowFinParams exceeds the kernel parameter space");
 static_assert(sizeof(ColFinParams) <= 32000, "ColFinParams exceeds the kernel parameter space");
 static_assert(sizeof(NormParams) <= 32000, "NormParams exceeds the kernel parameter space");
+static_assert(sizeof(ActiveParams) <= 32000, "ActiveParams exceeds the kernel parameter space");
 
 namespace {
 
@@ -316,6 +317,7 @@ __global__ void __launch_bounds__(kEwThreads, 2) prologue_flat_kernel(const __gr
     const int64_t view_elem0 = v * J.rows * J.cols;
     const int64_t vsz = J.rows * J.cols;
     const int64_t base = w * kProChunk;
+    const bool inactive = J.active != nullptr && J.active[v] == 0;  // block-uniform
     if (J.vrec != nullptr && threadIdx.x == 0 && w == 0) {
       ViewRec rec;
       rec.param = J.dst;
@@ -332,10 +334,24 @@ __global__ void __launch_bounds__(kEwThreads, 2) prologue_flat_kernel(const __gr
       rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
       rec.psr = J.param_sr;
       rec.psr_key = J.param_key;
+      rec.inactive = inactive ? 1 : 0;
       J.vrec[v] = rec;
     }
     bf16* xv = J.x0 + v * J.x_view_stride;
     float ss = 0.0f;
+    if (inactive) {
+      // Zero gradient under the inactive-expert rule: momentum untouched,
+      // X = 0 (so U = 0), no norm contribution.
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int i = 0; i < kProChunk / (8 * kEwThreads); ++i) {
+        const int64_t off = base + i * (8 * kEwThreads) + warp * 256 + lane * 8;
+        const int64_t rem = vsz - off;
+        const int nv = rem >= 8 ? 8 : (rem > 0 ? static_cast<int>(rem) : 0);
+        if (nv > 0) store8(xv, MH_BF16, off, nv, true, z);
+      }
+      if (lane == 0) J.tile_ss[static_cast<int64_t>(local) * (kEwThreads / 32) + warp] = 0.0f;
+      continue;
+    }
     if (p.use_momentum && J.src_vec && J.mom_vec && base + kProChunk <= vsz) {
       const int64_t e0 = view_elem0 + base + 8 * static_cast<int64_t>(threadIdx.x);
       bf16* xd = xv + base + 8 * static_cast<int64_t>(threadIdx.x);
@@ -420,6 +436,7 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
     const int64_t ncol = J.cols - col;
     const int nvalid = ncol >= 8 ? 8 : (ncol > 0 ? static_cast<int>(ncol) : 0);
 
+    const bool inactive = J.active != nullptr && J.active[v] == 0;  // block-uniform
     if (J.vrec != nullptr && threadIdx.x == 0 && r0 == 0 && c0 == 0) {
       ViewRec rec;
       rec.param = J.dst;
@@ -436,6 +453,7 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
       rec.vec = (J.dst_vec && J.src_vec && (J.cols % 8) == 0) ? 1 : 0;
       rec.psr = J.param_sr;
       rec.psr_key = J.param_key;
+      rec.inactive = inactive ? 1 : 0;
       J.vrec[v] = rec;
     }
 
@@ -446,6 +464,15 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
     for (int i = 0; i < 4; ++i) {
       const int64_t row = r0 + warp * 4 + i;
       ok[i] = row < J.rows && nvalid > 0;
+      if (inactive) {
+        // Zero gradient under the inactive-expert rule: X = 0, state untouched.
+        if (ok[i]) {
+          const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          store8(xv + row * J.ldx, MH_BF16, col, nvalid, true, z);
+        }
+        ok[i] = false;
+        continue;
+      }
       if (ok[i]) {
         const int64_t off = view_elem0 + row * J.cols + col;
         load8(J.src, J.src_dtype, off, nvalid, J.src_vec, g[i]);
@@ -572,7 +599,7 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
           const int64_t off = view_elem0 + row * J.cols + col;
           if constexpr (KIND == EW_COPYOUT) {
             store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, uu);
-          } else {
+          } else if (J.active == nullptr || J.active[t.v] != 0) {
             float w[4];
             load4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
             const float lr = J.lr, wd = J.wd, s = J.shape_scale;
@@ -608,6 +635,35 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
   }
 }
 
+// Inactive-expert rule: marks each view of a flagged tensor that has a
+// nonzero gradient entry. Chunks of views already marked are skipped, so an
+// active view usually costs one chunk; a silent view is read once in full.
+__global__ void __launch_bounds__(256) view_active_kernel(const __grid_constant__ ActiveParams p) {
+  for (int64_t c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
+    int lo = 0, hi = p.njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.jobs[mid].chunk_begin <= c) lo = mid; else hi = mid - 1;
+    }
+    const ActiveJob& J = p.jobs[lo];
+    const int64_t chunks_per_view = (J.view_elems + kActiveChunk - 1) / kActiveChunk;
+    const int64_t local = c - J.chunk_begin;
+    const int64_t v = local / chunks_per_view;
+    if (*reinterpret_cast<volatile const int32_t*>(J.active + v) != 0) continue;  // block-uniform
+    const int64_t start = v * J.view_elems + (local - v * chunks_per_view) * kActiveChunk;
+    const int64_t end = min(start + kActiveChunk, (v + 1) * J.view_elems);
+    bool nz = false;
+    for (int64_t i = start + 8 * static_cast<int64_t>(threadIdx.x); i < end; i += 8 * 256) {
+      float g[8];
+      const int64_t rem = end - i;
+      load8(J.grad, J.gdt, i, rem >= 8 ? 8 : static_cast<int>(rem), J.vec != 0, g);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) nz |= g[k] != 0.0f;  // NaN counts as nonzero
+    }
+    if (__syncthreads_or(nz ? 1 : 0) && threadIdx.x == 0) J.active[v] = 1;
+  }
+}
+
 __global__ void __launch_bounds__(256) row_finalize_kernel(const __grid_constant__ RowFinParams p) {
   __shared__ double red[2][8];
   __shared__ float s_kappa;
@@ -620,6 +676,7 @@ __global__ void __launch_bounds__(256) row_finalize_kernel(const __grid_constant
     }
     const RowFinJob& J = p.jobs[lo];
     const int64_t v = vv - J.view_begin;
+    if (J.active != nullptr && J.active[v] == 0) continue;  // NorMuon state untouched
     float* part = J.rowpart + v * J.tiles_c * J.rows;
     float* fac = J.rowfac + v * J.rows;
     double tot = 0.0, tot2 = 0.0;
@@ -777,6 +834,14 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
     case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_COPYOUT: ew_kernel<EW_COPYOUT><<<grid, kEwThreads, 0, s>>>(p); break;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_view_active(const ActiveParams& p, int num_sms, cudaStream_t s) {
+  if (p.total_chunks <= 0) return cudaSuccess;
+  const int64_t want = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(p.total_chunks < want ? p.total_chunks : want);
+  view_active_kernel<<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

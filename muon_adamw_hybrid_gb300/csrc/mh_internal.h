@@ -39,6 +39,7 @@ struct ViewRec {
   int32_t vec;          // param and grad 16-byte aligned and cols % 8 == 0
   int32_t psr;          // bf16 parameter written stochastically rounded
   uint32_t psr_key;     // its rounding key
+  int32_t inactive;     // zero gradient under the inactive-expert rule: leave it alone
 };
 
 struct EwJob {
@@ -69,6 +70,7 @@ struct EwJob {
   int32_t mom_dtype;     // momentum: MH_F32, or MH_BF16 stored stochastically rounded
   int32_t param_sr;      // bf16 parameter written stochastically rounded
   uint32_t mom_key, param_key;  // rounding keys (momentum, parameter streams)
+  const int32_t* active;  // per view: 1 if its gradient has a nonzero entry; null: all active
 };
 
 struct EwParams {
@@ -117,6 +119,7 @@ struct RowFinJob {
   float* rowfac;
   int64_t rows, cols, views, tiles_c;
   int64_t view_begin;  // prefix over views
+  const int32_t* active;  // per view, or null (see EwJob)
 };
 constexpr int kMaxRowFinJobs = 96;
 struct RowFinParams {
@@ -159,6 +162,25 @@ struct NormParams {
   int64_t total_views;
   const int32_t* skip;
 };
+
+// Inactive-expert rule: per view of a flagged tensor, whether its gradient
+// has any nonzero entry (chunks of a view already known active are skipped).
+constexpr int kMaxActiveJobs = 256;
+constexpr int64_t kActiveChunk = 8192;
+struct ActiveJob {
+  const void* grad;
+  int32_t* active;       // this tensor's first view
+  int64_t view_elems, views;
+  int64_t chunk_begin;   // global chunk index of this tensor's first chunk
+  int32_t gdt;
+  int32_t vec;           // 16-byte aligned and view_elems % 8 == 0
+};
+struct ActiveParams {
+  ActiveJob jobs[kMaxActiveJobs];
+  int32_t njobs;
+  int64_t total_chunks;
+};
+cudaError_t launch_view_active(const ActiveParams& p, int num_sms, cudaStream_t s);
 
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_row_finalize(const RowFinParams& p, cudaStream_t s);

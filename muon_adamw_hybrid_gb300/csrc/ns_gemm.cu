@@ -194,6 +194,7 @@ __device__ __forceinline__ void store_f32x32(void* base, int dt, int64_t off, in
 // stored row starting at element `off`; u holds the Newton-Schulz output.
 __device__ __forceinline__ void update_w32(const ViewRec& R, int64_t off, int nvalid,
                                            const float (&u)[32], int cautious) {
+  if (R.inactive) return;  // zero gradient under the inactive-expert rule
   const bool vec = R.vec && nvalid == 32;
   float w[32];
   load_f32x32(R.param, R.pdt, off, nvalid, vec, w);

@@ -95,12 +95,15 @@ def _view_dims(param: torch.Tensor, views: int, rows: int | None = None):
 
 def muon_tensor(param: torch.Tensor, grad: torch.Tensor, momentum: torch.Tensor, views: int = 1,
                 normuon_sm: torch.Tensor | None = None, lr_mult: float = 1.0,
-                wd: float = 0.0, rows: int | None = None, param_sr: bool = False) -> MuonTensor:
+                wd: float = 0.0, rows: int | None = None, param_sr: bool = False,
+                skip_zero_grad: bool = False) -> MuonTensor:
     """One Muon-routed tensor: ``views`` independent matrices of rows x cols.
 
     ``param`` is (views*rows, cols) or (views, rows, cols), contiguous. The
     momentum buffer is float32, or bfloat16 (kept stochastically rounded);
-    ``param_sr`` writes a bf16 parameter stochastically rounded.
+    ``param_sr`` writes a bf16 parameter stochastically rounded;
+    ``skip_zero_grad`` (routed experts) leaves a view whose gradient is zero
+    everywhere untouched.
     """
     v, r, c = _view_dims(param, views, rows)
     if grad.numel() != param.numel() or momentum.numel() != param.numel():
@@ -114,7 +117,7 @@ def muon_tensor(param: torch.Tensor, grad: torch.Tensor, momentum: torch.Tensor,
                     momentum=_dev_ptr(momentum, "momentum"), normuon_sm=sm,
                     param_dtype=dtype_code(param), grad_dtype=dtype_code(grad), views=v,
                     rows=r, cols=c, lr_mult=lr_mult, wd=wd, momentum_dtype=dtype_code(momentum),
-                    param_sr=int(bool(param_sr)))
+                    param_sr=int(bool(param_sr)), skip_zero_grad=int(bool(skip_zero_grad)))
     return _keep(st, param, grad, momentum, normuon_sm)
 
 
@@ -225,6 +228,7 @@ class MuonGroupEntry:
     views: int = 1
     lr_mult: float = 1.0
     wd: float = 0.0
+    skip_zero_grad: bool = False   # routed experts: no momentum or decay without gradient
 
 
 @dataclass
@@ -294,7 +298,8 @@ class HybridMuonAdamW:
 
     def _muon_structs(self, grads):
         return [muon_tensor(e.param, g, m, e.views, sm, e.lr_mult, e.wd,
-                            param_sr=self.param_sr and e.param.dtype == torch.bfloat16)
+                            param_sr=self.param_sr and e.param.dtype == torch.bfloat16,
+                            skip_zero_grad=e.skip_zero_grad)
                 for e, g, m, sm in zip(self.muon, grads, self.momentum, self.normuon_sm)]
 
     def _adam_structs(self, grads):

@@ -55,7 +55,7 @@ def test_struct_layout_matches_header(tmp_path):
         " offsetof(mh_muon_hparams, skip), sizeof(mh_grad_ref), sizeof(mh_grad_control),"
         " offsetof(mh_grad_control, step)); printf(\"%zu %zu %zu %zu\\n\","
         " offsetof(mh_muon_hparams, sr_seed), offsetof(mh_muon_hparams, coeff_schedule),"
-        " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, momentum_dtype));"
+        " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, skip_zero_grad));"
         " return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -69,7 +69,7 @@ def test_struct_layout_matches_header(tmp_path):
             mh.MuonHparams.skip.offset, ctypes.sizeof(mh.GradRef),
             ctypes.sizeof(mh.GradControl), mh.GradControl.step.offset,
             mh.MuonHparams.sr_seed.offset, mh.MuonHparams.coeff_schedule.offset,
-            mh.MuonHparams.norm_scale.offset, mh.MuonTensor.momentum_dtype.offset]
+            mh.MuonHparams.norm_scale.offset, mh.MuonTensor.skip_zero_grad.offset]
     assert got == want
 
 
@@ -95,6 +95,9 @@ def _step(tensors, hp=None, ws=0, wsb=0):
     (dict(cols=1 << 25), _lib.MH_ESHAPE),
     (dict(rows=40000, cols=40000), _lib.MH_EUNSUPPORTED),
     (dict(lr_mult=float("nan")), _lib.MH_EINVAL),
+    (dict(skip_zero_grad=2), _lib.MH_EINVAL),
+    (dict(param_sr=1), _lib.MH_EINVAL),            # param_sr needs a bf16 parameter
+    (dict(momentum_dtype=3), _lib.MH_EDTYPE),
 ])
 def test_muon_rejects_bad_tensor(kw, code):
     assert _step([_tensor(**kw)]) == code
