@@ -16,6 +16,7 @@ from .muon import (NS_COEFFS, NS_EPS, NS_STEPS, CAUTIOUS_OFF, CAUTIOUS_UPDATE, C
 from .adamw import adamw_step
 from .bf16 import round_bf16
 from .grad_control import CLIP_EPS, GradControl, grad_control
+from .qk_clip import ClipEntry, gamma, qk_clip
 from .stochastic_round import (MOMENT_FIRST, MOMENT_PARAM, MOMENT_SECOND, round_bf16_with_noise,
                                fmix32, sr_key, sr_noise16, sr_stream, stochastic_round_bf16)
 
@@ -25,5 +26,5 @@ __all__ = [
     "muon_step_view", "newton_schulz", "normuon", "shape_scale", "adamw_step", "round_bf16",
     "CLIP_EPS", "GradControl", "grad_control", "MOMENT_FIRST", "MOMENT_PARAM", "MOMENT_SECOND",
     "round_bf16_with_noise", "fmix32", "sr_key", "sr_noise16", "sr_stream",
-    "stochastic_round_bf16",
+    "stochastic_round_bf16", "ClipEntry", "gamma", "qk_clip",
 ]
