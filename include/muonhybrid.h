@@ -281,6 +281,36 @@ int mh_grad_prepare(const mh_grad_ref* grads, int32_t n, float inv_loss_scale, f
 int mh_adamw_step_ctl(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1,
                       float beta2, float eps, const mh_grad_control* ctl, void* stream);
 
+/* ---- QK-Clip after the update ---------------------------------------------
+ * kimi-k3 "Optimization", "QK-Clip watches a different failure mode";
+ * dew.training.optim "scale_by_qk_clip" (Kimi K2's MuonClip): each head h has
+ * an observed maximum query-key score s_h (scaled by the square root of the
+ * query-key dimension, maxed over microbatches by the caller). For s_h > tau,
+ * selected rows of the head's query and key projections are multiplied by
+ * gamma_h^exponent, gamma_h = tau / s_h; other heads are not touched. Give
+ * query and key rows of a head exponents summing to 1 (0.5 each) so its
+ * scores scale by gamma_h; an MLA rotary query whose key is shared takes 1.
+ * One entry describes a weight stored (rows, cols) with one block of
+ * head_stride rows per head, of which scaled_rows rows starting at
+ * row_offset are scaled; several entries may name one weight (disjoint rows). */
+typedef struct {
+  void* param;            /* (rows, cols), param_dtype, DEVICE, scaled in place */
+  int32_t param_dtype;    /* mh_dtype; bf16 is rounded to nearest even */
+  int32_t heads;          /* heads in this entry */
+  int64_t rows, cols;     /* stored shape; heads * head_stride <= rows */
+  int64_t head_stride;    /* rows from one head's block to the next */
+  int64_t row_offset;     /* first scaled row inside a block */
+  int64_t scaled_rows;    /* rows scaled per head; row_offset + scaled_rows <= head_stride */
+  int32_t head_index0;    /* s_max index of this entry's first head */
+  float exponent;         /* >= 0 */
+} mh_qk_clip_entry;
+
+/* s_max: DEVICE float array (head_index0 + heads entries at least for every
+ * entry). tau > 0. skip: the gradient-control flag (DEVICE, may be NULL):
+ * nothing is clipped after a skipped step. */
+int mh_qk_clip(const mh_qk_clip_entry* entries, int32_t n, const float* s_max, float tau,
+               const int32_t* skip, void* stream);
+
 /* Optional per-kernel timing. When enabled, every kernel the library launches
  * is bracketed by two CUDA events recorded on its own stream, and the
  * launch's algorithmic work is noted: bytes that must cross HBM at least

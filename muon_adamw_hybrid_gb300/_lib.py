@@ -23,7 +23,7 @@ EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_
             "mh_newton_schulz_batched", "mh_adamw_step", "mh_workspace_status", "mh_last_error",
             "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read",
             "mh_newton_schulz_batched_noalloc", "mh_grad_prepare_workspace_bytes",
-            "mh_grad_prepare", "mh_adamw_step_ctl", "mh_newton_schulz_batched_ex")
+            "mh_grad_prepare", "mh_adamw_step_ctl", "mh_newton_schulz_batched_ex", "mh_qk_clip")
 NS_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -63,6 +63,13 @@ class GradRef(ctypes.Structure):
 class GradControl(ctypes.Structure):
     _fields_ = [("grad_mult", c_void_p), ("skip", c_void_p), ("norm", c_void_p),
                 ("step", c_void_p)]
+
+
+class QkClipEntry(ctypes.Structure):
+    _fields_ = [("param", c_void_p), ("param_dtype", c_int32), ("heads", c_int32),
+                ("rows", c_int64), ("cols", c_int64), ("head_stride", c_int64),
+                ("row_offset", c_int64), ("scaled_rows", c_int64), ("head_index0", c_int32),
+                ("exponent", c_float)]
 
 
 class KernelStats(ctypes.Structure):
@@ -112,6 +119,9 @@ def _load() -> ctypes.CDLL:
     lib.mh_grad_prepare.argtypes = [POINTER(GradRef), c_int32, c_float, c_float,
                                     POINTER(GradControl), c_void_p, c_size_t, c_void_p]
     lib.mh_grad_prepare.restype = c_int
+    lib.mh_qk_clip.argtypes = [POINTER(QkClipEntry), c_int32, c_void_p, c_float, c_void_p,
+                               c_void_p]
+    lib.mh_qk_clip.restype = c_int
     lib.mh_workspace_status.argtypes = [c_void_p, c_void_p]
     lib.mh_workspace_status.restype = c_int
     lib.mh_last_error.argtypes = []
@@ -220,6 +230,11 @@ def grad_prepare(grads, inv_loss_scale: float, max_norm: float, control: GradCon
     arr, n = _array(GradRef, grads)
     _check(LIB.mh_grad_prepare(arr, n, inv_loss_scale, max_norm, ctypes.byref(control),
                                workspace, workspace_bytes, stream))
+
+
+def qk_clip(entries, s_max: int, tau: float, skip: int, stream: int) -> None:
+    arr, n = _array(QkClipEntry, entries)
+    _check(LIB.mh_qk_clip(arr, n, s_max, tau, skip, stream))
 
 
 def workspace_status(workspace: int, stream: int) -> None:

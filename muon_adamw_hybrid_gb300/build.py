@@ -31,7 +31,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxe
 LIBS = {
     os.path.join(PKG, "libmuonhybrid.so"): [
         os.path.join(CSRC, f) for f in ("api.cu", "adamw.cu", "elementwise.cu", "ns_gemm.cu",
-                                             "noalloc.cu", "grad_control.cu")
+                                             "noalloc.cu", "grad_control.cu", "qk_clip.cu")
     ],
     os.path.join(ROOT, "synth", "libmhsynth.so"): [os.path.join(ROOT, "synth", "synth.cu")],
 }

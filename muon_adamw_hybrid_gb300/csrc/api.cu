@@ -1102,6 +1102,69 @@ int mh_adamw_step_ctl(const mh_adamw_tensor* tensors, int32_t n, float lr, float
   return adamw_impl(tensors, n, lr, beta1, beta2, eps, 0, ctl, stream);
 }
 
+// ---- QK-Clip ---------------------------------------------------------------------
+
+int mh_qk_clip(const mh_qk_clip_entry* entries, int32_t n, const float* s_max, float tau,
+               const int32_t* skip, void* stream_) {
+  if (n < 0) return fail(MH_EINVAL, "n must be >= 0 (got %d)", n);
+  if (n > 0 && (!entries || !s_max)) return fail(MH_EINVAL, "entries and s_max must be non-NULL");
+  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(MH_EINVAL, "tau must be finite and > 0");
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    const mh_qk_clip_entry& E = entries[i];
+    if (!valid_dtype(E.param_dtype)) return fail(MH_EDTYPE, "entries[%d]: fp32 or bf16 only", i);
+    if (E.heads < 0 || E.rows < 0 || E.cols < 0 || E.head_stride < 0 || E.row_offset < 0 ||
+        E.scaled_rows < 0 || E.head_index0 < 0)
+      return fail(MH_ESHAPE, "entries[%d]: negative size or index", i);
+    if (int64_t(E.heads) * E.head_stride > E.rows || E.row_offset + E.scaled_rows > E.head_stride)
+      return fail(MH_ESHAPE, "entries[%d]: head blocks do not fit the weight", i);
+    if (!(E.exponent >= 0.0f) || !std::isfinite(E.exponent))
+      return fail(MH_EINVAL, "entries[%d]: exponent must be finite and >= 0", i);
+    if (E.heads > 0 && E.scaled_rows > 0 && E.cols > 0 && !E.param)
+      return fail(MH_EINVAL, "entries[%d]: param is NULL", i);
+    total += int64_t(E.heads) * E.scaled_rows;
+  }
+  if (total == 0) return MH_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int sms = 0;
+  int rc = device_sms(&sms);
+  if (rc != MH_OK) return rc;
+  QkClipParams qp;
+  std::memset(&qp, 0, sizeof(qp));
+  qp.s_max = s_max;
+  qp.tau = tau;
+  qp.skip = skip;
+  int64_t rows = 0;
+  auto flush = [&]() -> int {
+    qp.total_rows = rows;
+    ProfScope ps(stream, "qk_clip", 0.0);
+    cudaError_t e = launch_qk_clip(qp, sms, stream);
+    qp.nentries = 0;
+    rows = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "QK-Clip launch");
+    return MH_OK;
+  };
+  for (int i = 0; i < n; ++i) {
+    const mh_qk_clip_entry& E = entries[i];
+    if (E.heads == 0 || E.scaled_rows == 0 || E.cols == 0) continue;
+    QkClipEntry& Q = qp.entries[qp.nentries++];
+    Q.param = E.param;
+    Q.cols = E.cols;
+    Q.head_stride = E.head_stride;
+    Q.row_offset = E.row_offset;
+    Q.scaled_rows = E.scaled_rows;
+    Q.head_index0 = E.head_index0;
+    Q.dt = E.param_dtype;
+    Q.vec = aligned16(E.param) ? 1 : 0;
+    Q.exponent = E.exponent;
+    Q.row_begin = rows;
+    rows += int64_t(E.heads) * E.scaled_rows;
+    if (qp.nentries == kMaxQkClipEntries && (rc = flush()) != MH_OK) return rc;
+  }
+  if (qp.nentries > 0 && (rc = flush()) != MH_OK) return rc;
+  return MH_OK;
+}
+
 // ---- gradient control --------------------------------------------------------
 
 static int check_grads(const mh_grad_ref* grads, int32_t n, int64_t* chunks) {

@@ -326,6 +326,31 @@ struct GradFinParams {
 };
 
 cudaError_t launch_grad_sumsq(const GradParams& p, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// QK-Clip: rows of query / key projections of heads past tau scaled by
+// min(1, tau / s_h)^exponent.
+// ---------------------------------------------------------------------------
+constexpr int kMaxQkClipEntries = 256;
+struct QkClipEntry {
+  void* param;
+  int64_t cols;
+  int64_t head_stride, row_offset, scaled_rows;
+  int64_t row_begin;     // prefix over entries of heads * scaled_rows
+  int32_t head_index0;
+  int32_t dt;
+  int32_t vec;           // 16-byte aligned
+  float exponent;
+};
+struct QkClipParams {
+  QkClipEntry entries[kMaxQkClipEntries];
+  int32_t nentries;
+  int64_t total_rows;
+  const float* s_max;    // device, per head
+  float tau;
+  const int32_t* skip;   // gradient control: clip nothing after a skipped step
+};
+cudaError_t launch_qk_clip(const QkClipParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_grad_finalize(const GradFinParams& p, cudaStream_t s);
 
 // Sets the calling thread's message returned by mh_last_error().

@@ -12,7 +12,7 @@ import torch
 
 from . import _lib
 from ._lib import (MH_BF16, MH_F32, AdamwTensor, GradControl, GradRef, MuonHparams, MuonTensor,
-                   NsProblem)
+                   NsProblem, QkClipEntry)
 
 # Speedtronic docs "v2 optimizers", "Newton-Schulz": coefficients, steps, eps.
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
@@ -220,6 +220,32 @@ def grad_prepare(grads, control: GradientControl, inv_loss_scale: float = 1.0,
     _lib.grad_prepare(refs, inv_loss_scale, max_norm, control.struct(), workspace.data_ptr(),
                       workspace.numel(), _stream_ptr(stream))
     return workspace
+
+
+def qk_clip_entry(param: torch.Tensor, heads: int, head_stride: int, scaled_rows: int,
+                  row_offset: int = 0, head_index0: int = 0,
+                  exponent: float = 0.5) -> QkClipEntry:
+    """Rows of a (rows, cols) query / key projection that QK-Clip rescales:
+    for each of ``heads`` blocks of ``head_stride`` rows, ``scaled_rows`` rows
+    from ``row_offset`` are multiplied by gamma_h ** exponent."""
+    if param.dim() != 2:
+        raise ValueError("a QK-Clip entry names a 2-D weight")
+    st = QkClipEntry(param=_dev_ptr(param, "param"), param_dtype=dtype_code(param), heads=heads,
+                     rows=param.shape[0], cols=param.shape[1], head_stride=head_stride,
+                     row_offset=row_offset, scaled_rows=scaled_rows, head_index0=head_index0,
+                     exponent=exponent)
+    return _keep(st, param)
+
+
+def qk_clip(entries, s_max: torch.Tensor, tau: float = 100.0,
+            control: "GradientControl | None" = None, stream=None) -> None:
+    """kimi-k3 "QK-Clip" / dew "scale_by_qk_clip": rescale the listed rows of
+    every head with s_max[h] > tau by (tau / s_max[h]) ** exponent, after the
+    optimizer update; nothing happens after a step the control block skipped."""
+    if s_max.dtype != torch.float32:
+        raise TypeError("s_max must be float32")
+    skip = control.skip.data_ptr() if control is not None else None
+    _lib.qk_clip(list(entries), _dev_ptr(s_max, "s_max"), tau, skip, _stream_ptr(stream))
 
 
 @dataclass

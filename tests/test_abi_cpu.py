@@ -251,3 +251,26 @@ def test_ns_ex_rejects_bad_args():
 def test_schedule_length_is_checked_in_python():
     with pytest.raises(ValueError):
         mh.make_hparams(ns_steps=3, coeffs=[(1.0, 0.0, 0.0)] * 2)
+
+
+def test_qk_clip_rejects_bad_args():
+    L = _lib.LIB
+    e = mh.QkClipEntry(param=256, param_dtype=0, heads=4, rows=64, cols=32, head_stride=16,
+                       row_offset=0, scaled_rows=8, head_index0=0, exponent=0.5)
+    arr = (mh.QkClipEntry * 1)(e)
+    assert L.mh_qk_clip(arr, 1, 512, 0.0, None, None) == _lib.MH_EINVAL           # tau
+    assert L.mh_qk_clip(arr, 1, None, 100.0, None, None) == _lib.MH_EINVAL        # s_max
+    too_tall = (mh.QkClipEntry * 1)(mh.QkClipEntry(param=256, param_dtype=0, heads=5, rows=64,
+                                                   cols=32, head_stride=16, row_offset=0,
+                                                   scaled_rows=8, head_index0=0, exponent=0.5))
+    assert L.mh_qk_clip(too_tall, 1, 512, 100.0, None, None) == _lib.MH_ESHAPE
+    past_block = (mh.QkClipEntry * 1)(mh.QkClipEntry(param=256, param_dtype=0, heads=4, rows=64,
+                                                     cols=32, head_stride=16, row_offset=10,
+                                                     scaled_rows=8, head_index0=0, exponent=0.5))
+    assert L.mh_qk_clip(past_block, 1, 512, 100.0, None, None) == _lib.MH_ESHAPE
+    bad_exp = (mh.QkClipEntry * 1)(mh.QkClipEntry(param=256, param_dtype=0, heads=4, rows=64,
+                                                  cols=32, head_stride=16, row_offset=0,
+                                                  scaled_rows=8, head_index0=0,
+                                                  exponent=float("nan")))
+    assert L.mh_qk_clip(bad_exp, 1, 512, 100.0, None, None) == _lib.MH_EINVAL
+    assert L.mh_qk_clip(arr, 0, None, 100.0, None, None) == _lib.MH_OK               # nothing to do
