@@ -107,36 +107,56 @@ struct TileInfo {
   int64_t v, r0, c0;
 };
 
+// Tile -> (job, view, first row, first col). 32-bit arithmetic: the host
+// rejects tensors with 2^31 or more tiles, and a 64-bit division per tile is
+// dozens of instructions in every thread.
 __device__ __forceinline__ TileInfo tile_info(const EwParams& p, int64_t tile) {
   TileInfo t;
   t.job = find_job(p, tile);
   const EwJob& J = p.jobs[t.job];
-  const int64_t local = tile - J.tile_begin;
-  const int64_t per_view = static_cast<int64_t>(J.tiles_r) * J.tiles_c;
-  t.v = local / per_view;
-  const int64_t w = local - t.v * per_view;
-  t.r0 = (w / J.tiles_c) * kEwTileR;
-  t.c0 = (w % J.tiles_c) * kEwTileC;
+  const uint32_t local = static_cast<uint32_t>(tile - J.tile_begin);
+  const uint32_t tc = static_cast<uint32_t>(J.tiles_c);
+  const uint32_t per_view = static_cast<uint32_t>(J.tiles_r) * tc;
+  const uint32_t v = local / per_view;
+  const uint32_t w = local - v * per_view;
+  const uint32_t tr = w / tc;
+  t.v = v;
+  t.r0 = static_cast<int64_t>(tr) * kEwTileR;
+  t.c0 = static_cast<int64_t>(w - tr * tc) * kEwTileC;
   return t;
 }
 
-// Loads this thread's 4 x 4 block of U (rows r0+4*warp+i, cols c0+4*lane+k)
+// Loads this thread's 4 x 8 block of U (rows r0+4*warp+i, cols c0+8*lane+k)
 // from the Newton-Schulz output buffer, which holds every view in its stored
-// layout (row pitch ldx).
-__device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t, float u[4][4]) {
+// layout (row pitch ldx, a multiple of 8: every row load is 16-byte aligned).
+// All four loads are issued before any is used.
+__device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t, float u[4][8]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bf16* xv = J.xf + t.v * J.x_view_stride;
+  const int64_t col = t.c0 + lane * 8;
+  const int64_t nv = J.cols - col;
+  const int nvalid = nv >= 8 ? 8 : (nv > 0 ? static_cast<int>(nv) : 0);
+  uint4 raw[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = t.r0 + warp * 4 + i;
-    const int64_t col = t.c0 + lane * 4;
-    const int64_t nv = J.cols - col;
-    const int nvalid = nv >= 4 ? 4 : (nv > 0 ? static_cast<int>(nv) : 0);
-    if (row < J.rows && nvalid > 0) {
-      load4(xv + row * J.ldx, MH_BF16, col, nvalid, true, u[i]);
-    } else {
+    raw[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < J.rows && nvalid == 8)
+      raw[i] = __ldcs(reinterpret_cast<const uint4*>(xv + row * J.ldx + col));
+  }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) u[i][k] = 0.0f;
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t wd[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      u[i][2 * k] = __uint_as_float(wd[k] << 16);
+      u[i][2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+    }
+    const int64_t row = t.r0 + warp * 4 + i;
+    if (row < J.rows && nvalid > 0 && nvalid < 8) {  // ragged last columns
+      const bf16* src = xv + row * J.ldx + col;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) u[i][k] = k < nvalid ? __bfloat162float(src[k]) : 0.0f;
     }
   }
 }
@@ -513,7 +533,7 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ EwParams p) {
+__global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant__ EwParams p) {
   __shared__ float sRed[kEwThreads / 32][kEwTileC];
   // The tile's job record, copied once per tile from the parameter space:
   // indexing a large parameter table per access would keep missing the small
@@ -537,98 +557,124 @@ __global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ 
     }
     const EwJob& J = sJ;
     const int64_t view_elem0 = t.v * J.rows * J.cols;
-    const int64_t col = t.c0 + lane * 4;
+    const int64_t col = t.c0 + lane * 8;
     const int64_t ncol = J.cols - col;
-    const int nvalid = ncol >= 4 ? 4 : (ncol > 0 ? static_cast<int>(ncol) : 0);
+    const int nvalid = ncol >= 8 ? 8 : (ncol > 0 ? static_cast<int>(ncol) : 0);
 
-    {
-      float u[4][4];
-      load_u_block(J, t, u);
+    float u[4][8];
+    load_u_block(J, t, u);
 
-      if constexpr (KIND == EW_ROWSQ) {
+    if constexpr (KIND == EW_ROWSQ) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += u[i][k] * u[i][k];
+        s = warp_sum(s);
+        const int64_t row = t.r0 + warp * 4 + i;
+        if (lane == 0 && row < J.rows)
+          J.rowpart[(t.v * J.tiles_c + t.c0 / kEwTileC) * J.rows + row] = s;
+      }
+    } else if constexpr (KIND == EW_COLSQ) {
+      float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t row = t.r0 + warp * 4 + i;
+        const float f = row < J.rows ? J.rowfac[t.v * J.rows + row] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float x = f * u[i][k];
+          cs[k] += x * x;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sRed[warp][lane * 8 + k] = cs[k];
+      __syncthreads();
+      {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kEwThreads / 32; ++w) s += sRed[w][threadIdx.x];
+        const int64_t c = t.c0 + threadIdx.x;
+        if (c < J.cols) J.colpart[(t.v * J.tiles_r + t.r0 / kEwTileR) * J.cols + c] = s;
+      }
+      __syncthreads();
+    } else {
+      // EW_APPLY / EW_COPYOUT: final update direction U_ij.
+      float uscale = 1.0f;
+      if (p.u_scale_from_sumsq) uscale = ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps);
+      float h[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+      if (p.use_colfac) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < nvalid) h[k] = J.colfac[t.v * J.cols + col + k];
+      }
+      // 16-byte access needs 8-element rows for bf16 and 4-element rows for fp32.
+      const bool dvec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
+      const bool svec = J.src_vec && (J.src_dtype == MH_F32 || (J.cols % 8) == 0);
+      const bool active = J.active == nullptr || J.active[t.v] != 0;
+      float w[4][8];
+      float fr[4];
+      // Every load of the block (parameters, row factors) is in flight before
+      // any is used: the stores below may alias them, so nothing may be
+      // loaded between stores.
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t row = t.r0 + warp * 4 + i;
+        fr[i] = p.use_rowfac && row < J.rows ? J.rowfac[t.v * J.rows + row] : 1.0f;
+        if constexpr (KIND == EW_APPLY || KIND == EW_APPLY_CU) {
+          if (row < J.rows && nvalid > 0 && active)
+            load8(J.dst, J.dst_dtype, view_elem0 + row * J.cols + col, nvalid, dvec, w[i]);
+        }
+      }
+      // The cautious-update mask needs the gradient: a separate instantiation
+      // keeps its 32 registers out of the common path.
+      float gr[KIND == EW_APPLY_CU ? 4 : 1][8];
+      if constexpr (KIND == EW_APPLY_CU) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          float s = u[i][0] * u[i][0] + u[i][1] * u[i][1] + u[i][2] * u[i][2] + u[i][3] * u[i][3];
-          s = warp_sum(s);
           const int64_t row = t.r0 + warp * 4 + i;
-          if (lane == 0 && row < J.rows)
-            J.rowpart[(t.v * J.tiles_c + t.c0 / kEwTileC) * J.rows + row] = s;
+          if (row < J.rows && nvalid > 0 && active)
+            load8(J.src, J.src_dtype, view_elem0 + row * J.cols + col, nvalid, svec, gr[i]);
         }
-      } else if constexpr (KIND == EW_COLSQ) {
-        float cs[4] = {0.f, 0.f, 0.f, 0.f};
+      }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int64_t row = t.r0 + warp * 4 + i;
-          const float f = row < J.rows ? J.rowfac[t.v * J.rows + row] : 0.0f;
+      for (int i = 0; i < 4; ++i) {
+        const int64_t row = t.r0 + warp * 4 + i;
+        if (row >= J.rows || nvalid == 0) continue;
+        const float f = fr[i];
+        float uu[8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float x = f * u[i][k];
-            cs[k] += x * x;
-          }
-        }
+        for (int k = 0; k < 8; ++k) uu[k] = (u[i][k] * uscale) * f * h[k];
+        const int64_t off = view_elem0 + row * J.cols + col;
+        if constexpr (KIND == EW_COPYOUT) {
+          const bool ovec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
+          store8(J.dst, J.dst_dtype, off, nvalid, ovec, uu);
+        } else if (active) {
+          const float lr = J.lr, wd = J.wd, s = J.shape_scale;
+          float* wi = w[i];
+          if constexpr (KIND == EW_APPLY_CU) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sRed[warp][lane * 4 + k] = cs[k];
-        __syncthreads();
-        if (threadIdx.x < kEwTileC) {
-          float s = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kEwThreads / 32; ++w) s += sRed[w][threadIdx.x];
-          const int64_t c = t.c0 + threadIdx.x;
-          if (c < J.cols) J.colpart[(t.v * J.tiles_r + t.r0 / kEwTileR) * J.cols + c] = s;
-        }
-        __syncthreads();
-      } else {
-        // EW_APPLY / EW_COPYOUT: final update direction U_ij.
-        float uscale = 1.0f;
-        if (p.u_scale_from_sumsq)
-          uscale = ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps);
-        float h[4] = {1.f, 1.f, 1.f, 1.f};
-        if (p.use_colfac) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (k < nvalid) h[k] = J.colfac[t.v * J.cols + col + k];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int64_t row = t.r0 + warp * 4 + i;
-          if (row >= J.rows || nvalid == 0) continue;
-          const float f = p.use_rowfac ? J.rowfac[t.v * J.rows + row] : 1.0f;
-          float uu[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) uu[k] = (u[i][k] * uscale) * f * h[k];
-          const int64_t off = view_elem0 + row * J.cols + col;
-          if constexpr (KIND == EW_COPYOUT) {
-            store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, uu);
-          } else if (J.active == nullptr || J.active[t.v] != 0) {
-            float w[4];
-            load4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
-            const float lr = J.lr, wd = J.wd, s = J.shape_scale;
-            if (p.cautious == MH_CAUTIOUS_OFF) {
-              const float decay = 1.0f - lr * wd;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) w[k] = decay * w[k] - (lr * s) * uu[k];
-            } else if (p.cautious == MH_CAUTIOUS_WD) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float g = s * uu[k];
-                const float mask = (g * w[k] >= 0.0f) ? 1.0f : 0.0f;
-                w[k] = w[k] - lr * (g + wd * w[k] * mask);
-              }
-            } else {
-              float gr[4];
-              load4(J.src, J.src_dtype, off, nvalid, J.src_vec, gr);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float delta = lr * wd * w[k] + (lr * s) * uu[k];
-                if (delta * gr[k] > 0.0f) w[k] = w[k] - delta;
-              }
+            for (int k = 0; k < 8; ++k) {
+              const float delta = lr * wd * wi[k] + (lr * s) * uu[k];
+              if (delta * gr[i][k] > 0.0f) wi[k] = wi[k] - delta;
             }
-            if (J.param_sr && J.dst_dtype == MH_BF16)
-              store_bf16_sr<4>(static_cast<bf16*>(J.dst) + off, nvalid, J.dst_vec, w, J.param_key,
-                               static_cast<uint64_t>(off));
-            else
-              store4(J.dst, J.dst_dtype, off, nvalid, J.dst_vec, w);
+          } else if (p.cautious == MH_CAUTIOUS_WD) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float g = s * uu[k];
+              const float mask = (g * wi[k] >= 0.0f) ? 1.0f : 0.0f;
+              wi[k] = wi[k] - lr * (g + wd * wi[k] * mask);
+            }
+          } else {
+            const float decay = 1.0f - lr * wd;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) wi[k] = decay * wi[k] - (lr * s) * uu[k];
           }
+          if (J.param_sr && J.dst_dtype == MH_BF16)
+            store_bf16_sr<8>(static_cast<bf16*>(J.dst) + off, nvalid, dvec, w[i], J.param_key,
+                             static_cast<uint64_t>(off));
+          else
+            store8(J.dst, J.dst_dtype, off, nvalid, dvec, w[i]);
         }
       }
     }
@@ -799,7 +845,7 @@ cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s) {
 // Resident blocks per SM of each elementwise kernel (queried once per kind),
 // so that the persistent grids are exactly one wave.
 int blocks_per_sm(EwKind kind, const void* kernel) {
-  static int cached[6] = {0, 0, 0, 0, 0, 0};
+  static int cached[kEwKinds] = {};
   if (cached[kind] == 0) {
     int b = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kEwThreads, 0) != cudaSuccess ||
@@ -814,6 +860,7 @@ int blocks_per_sm(EwKind kind, const void* kernel) {
 
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
+  if (kind == EW_APPLY && p.cautious == MH_CAUTIOUS_UPDATE) kind = EW_APPLY_CU;
   const void* fn = nullptr;
   switch (kind) {
     case EW_PROLOGUE: fn = reinterpret_cast<const void*>(prologue_kernel); break;
@@ -821,6 +868,7 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
     case EW_ROWSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_ROWSQ>); break;
     case EW_COLSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_COLSQ>); break;
     case EW_APPLY: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY>); break;
+    case EW_APPLY_CU: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY_CU>); break;
     case EW_COPYOUT: fn = reinterpret_cast<const void*>(ew_kernel<EW_COPYOUT>); break;
   }
   const int per_sm = blocks_per_sm(kind, fn);
@@ -832,6 +880,7 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
     case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_APPLY_CU: ew_kernel<EW_APPLY_CU><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_COPYOUT: ew_kernel<EW_COPYOUT><<<grid, kEwThreads, 0, s>>>(p); break;
   }
   return cudaGetLastError();

@@ -20,7 +20,7 @@ typedef __nv_bfloat16 bf16;
 // one Newton-Schulz shape class, and occupy consecutive class slots.
 // ---------------------------------------------------------------------------
 constexpr int kEwTileR = 32;   // tile rows (stored orientation)
-constexpr int kEwTileC = 128;  // tile cols (stored orientation)
+constexpr int kEwTileC = 256;  // tile cols (stored orientation): 8 per lane
 constexpr int kProTileC = 256; // prologue tile cols: 8 per lane
 constexpr int kProChunk = 8192;  // prologue chunk of a flat (wide) view: 32 per thread
 constexpr int kEwThreads = 256;
@@ -107,8 +107,11 @@ enum EwKind {
   EW_COLSQ = 2,
   EW_APPLY = 3,
   EW_COPYOUT = 4,
-  EW_PROLOGUE_FLAT = 5   // contiguous chunks (wide views with cols % 8 == 0)
+  EW_PROLOGUE_FLAT = 5,  // contiguous chunks (wide views with cols % 8 == 0)
+  EW_APPLY_CU = 6        // EW_APPLY with the cautious-update mask (reads the gradient);
+                         // chosen by launch_elementwise, never planned on its own
 };
+constexpr int kEwKinds = 7;
 
 // Row finalisation (NorMuon state, NorMuon norm restore, Muon+ row factor):
 // one CTA per view. Every reduction sums per-tile partials in a fixed order,
