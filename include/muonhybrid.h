@@ -24,7 +24,11 @@
  *   - All pointers to tensors are DEVICE pointers into memory the caller owns
  *     (parameters, gradients, optimizer state, workspace). The library never
  *     allocates device memory in these calls and keeps no pointer after the
- *     call returns.
+ *     call returns. A pointer may also be host memory that the device reads
+ *     at the same address (page-locked and mapped, or coherent system memory
+ *     on a Grace-Blackwell system): the kernels then stream it over the
+ *     host link, with no separate copy. mh_pointer_device_accessible tells
+ *     whether a pointer qualifies.
  *   - Tensors are contiguous and row-major. A Muon tensor with views = k is
  *     k independent rows x cols matrices stored back to back, i.e. the array
  *     (k*rows, cols); its momentum buffer has the same layout.
@@ -340,6 +344,12 @@ int mh_profiler_read(mh_kernel_stats* out, int32_t max, int32_t* count);
  * `workspace`, synchronising `stream`. MH_OK, or MH_ETIMEOUT when a kernel's
  * bounded wait gave up (its outputs are then undefined). */
 int mh_workspace_status(const void* workspace, void* stream);
+
+/* *accessible = 1 when the current device can read and write `ptr` at that
+ * very address: device memory, managed memory, or host memory that is
+ * page-locked and mapped into the device's address space (0 otherwise, e.g.
+ * pageable host memory or an unknown pointer). Host-only query. */
+int mh_pointer_device_accessible(const void* ptr, int32_t* accessible);
 
 /* Message for the last non-OK status on this host thread ("" if none). */
 const char* mh_last_error(void);

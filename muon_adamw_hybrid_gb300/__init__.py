@@ -16,8 +16,8 @@ from ._lib import (MH_BF16, MH_CAUTIOUS_OFF, MH_CAUTIOUS_UPDATE, MH_CAUTIOUS_WD,
                    NsProblem, QkClipEntry, adamw_step, adamw_step_ctl,
                    grad_prepare_workspace_bytes,
                    last_error, muon_step_batched, muon_workspace_bytes, newton_schulz_batched,
-                   ns_workspace_bytes, profiler_enable, profiler_read, profiler_reset, version,
-                   workspace_status)
+                   ns_workspace_bytes, pointer_device_accessible, profiler_enable, profiler_read,
+                   profiler_reset, version, workspace_status)
 from .torch_api import (GradientControl, HybridMuonAdamW, adamw_tensor, dtype_code, grad_prepare,
                         grad_ref, make_hparams, muon_tensor, newton_schulz, ns_problem, qk_clip,
                         qk_clip_entry)
@@ -31,5 +31,5 @@ __all__ = [
     "version", "workspace_status", "profiler_enable", "profiler_read", "profiler_reset",
     "GradientControl", "HybridMuonAdamW", "adamw_tensor", "dtype_code", "grad_prepare",
     "grad_ref", "make_hparams", "muon_tensor", "newton_schulz", "ns_problem", "route_parameters",
-    "QkClipEntry", "qk_clip", "qk_clip_entry",
+    "QkClipEntry", "qk_clip", "qk_clip_entry", "pointer_device_accessible",
 ]

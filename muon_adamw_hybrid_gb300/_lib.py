@@ -23,7 +23,8 @@ EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_
             "mh_newton_schulz_batched", "mh_adamw_step", "mh_workspace_status", "mh_last_error",
             "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read",
             "mh_newton_schulz_batched_noalloc", "mh_grad_prepare_workspace_bytes",
-            "mh_grad_prepare", "mh_adamw_step_ctl", "mh_newton_schulz_batched_ex", "mh_qk_clip")
+            "mh_grad_prepare", "mh_adamw_step_ctl", "mh_newton_schulz_batched_ex", "mh_qk_clip",
+            "mh_pointer_device_accessible")
 NS_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -122,6 +123,8 @@ def _load() -> ctypes.CDLL:
     lib.mh_qk_clip.argtypes = [POINTER(QkClipEntry), c_int32, c_void_p, c_float, c_void_p,
                                c_void_p]
     lib.mh_qk_clip.restype = c_int
+    lib.mh_pointer_device_accessible.argtypes = [c_void_p, POINTER(c_int32)]
+    lib.mh_pointer_device_accessible.restype = c_int
     lib.mh_workspace_status.argtypes = [c_void_p, c_void_p]
     lib.mh_workspace_status.restype = c_int
     lib.mh_last_error.argtypes = []
@@ -235,6 +238,14 @@ def grad_prepare(grads, inv_loss_scale: float, max_norm: float, control: GradCon
 def qk_clip(entries, s_max: int, tau: float, skip: int, stream: int) -> None:
     arr, n = _array(QkClipEntry, entries)
     _check(LIB.mh_qk_clip(arr, n, s_max, tau, skip, stream))
+
+
+def pointer_device_accessible(ptr: int) -> bool:
+    """True when the current device reads and writes ``ptr`` at that address
+    (device or managed memory, or mapped page-locked host memory)."""
+    out = c_int32(0)
+    _check(LIB.mh_pointer_device_accessible(ptr, ctypes.byref(out)))
+    return bool(out.value)
 
 
 def workspace_status(workspace: int, stream: int) -> None:

@@ -729,6 +729,34 @@ const char* mh_last_error(void) { return g_err.c_str(); }
 
 const char* mh_version(void) { return "0.1.0"; }
 
+int mh_pointer_device_accessible(const void* ptr, int32_t* accessible) {
+  if (!accessible) return fail(MH_EINVAL, "accessible is NULL");
+  *accessible = 0;
+  if (!ptr) return MH_OK;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // an unknown pointer is simply not accessible
+    return MH_OK;
+  }
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      *accessible = a.device == dev ? 1 : 0;
+      break;
+    case cudaMemoryTypeManaged:
+      *accessible = 1;
+      break;
+    case cudaMemoryTypeHost:
+      *accessible = a.devicePointer == ptr ? 1 : 0;
+      break;
+    default:
+      break;
+  }
+  return MH_OK;
+}
+
 size_t mh_muon_workspace_bytes(const mh_muon_tensor* tensors, int32_t n, const mh_muon_hparams* hp) {
   if (check_muon_args(tensors, n, hp) != MH_OK) return 0;
   return muon_plan(tensors, n, hp).bytes;

@@ -34,11 +34,16 @@ def dtype_code(t: torch.Tensor) -> int:
 
 
 def _dev_ptr(t: torch.Tensor, what: str) -> int:
-    if not t.is_cuda:
-        raise ValueError(f"{what} must be a CUDA tensor")
+    """Device address of a tensor: a CUDA tensor, or a page-locked host
+    tensor that the device reads in place (the kernels then stream it over
+    the host link instead of a separate copy)."""
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
-    return t.data_ptr()
+    if t.is_cuda:
+        return t.data_ptr()
+    if t.is_pinned() and _lib.pointer_device_accessible(t.data_ptr()):
+        return t.data_ptr()
+    raise ValueError(f"{what} must be a CUDA tensor or device-accessible pinned host memory")
 
 
 def _stream_ptr(stream) -> int:

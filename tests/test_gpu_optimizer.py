@@ -75,3 +75,24 @@ def test_routing_helper_and_facade_step():
     torch.cuda.synchronize()
     for k in p:
         assert not torch.equal(before[k], p[k]), k
+
+
+def test_pinned_host_gradients_are_read_in_place():
+    """Gradients in page-locked host memory that the device maps at the same
+    address are read by the kernels directly; the result equals the step on
+    device-resident gradients bit for bit."""
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+    probe = torch.empty(16, pin_memory=True)
+    if not mh.pointer_device_accessible(probe.data_ptr()):
+        pytest.skip("this system does not map page-locked host memory into the device")
+    pa, pb = _params(), _params()
+    a, b = _opt(pa), _opt(pb)
+    for s in range(2):
+        g = _grads(s)
+        host = {k: v.cpu().pin_memory() for k, v in g.items()}
+        a.step([g["q"], g["gate_up"]], [g["embed"], g["norm"]])
+        b.step([host["q"], host["gate_up"]], [host["embed"], host["norm"]])
+    torch.cuda.synchronize()
+    for k in pa:
+        assert torch.equal(pa[k], pb[k]), k
