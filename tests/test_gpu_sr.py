@@ -27,7 +27,7 @@ REL_TERMS = 1e-6   # fp32 arithmetic and fp32 constants (e.g. 1 - 0.9f), relativ
 
 def _bits_bf16(t):
     import torch
-    return t.view(torch.int16).cpu().numpy().astype(np.uint16).astype(np.uint32)
+    return t.contiguous().view(torch.int16).cpu().numpy().astype(np.uint16).astype(np.uint32)
 
 
 def _expected_bits(x64, seed, stream, terms=None, index0=0):
@@ -51,9 +51,9 @@ def _expected_bits(x64, seed, stream, terms=None, index0=0):
     return bits.astype(np.uint32), ambiguous
 
 
-def _check_state(got_t, x64, seed, stream, what, terms=None):
+def _check_state(got_t, x64, seed, stream, what, terms=None, index0=0):
     got = _bits_bf16(got_t).ravel()
-    want, amb = _expected_bits(x64, seed, stream, terms)
+    want, amb = _expected_bits(x64, seed, stream, terms, index0)
     clear = ~amb
     mism = np.flatnonzero(got[clear] != want[clear])
     assert mism.size == 0, (what, mism.size, int(clear.sum()))
