@@ -126,6 +126,34 @@ __device__ __forceinline__ void load_bf16x32(const bf16* src, float (&x)[32]) {
   }
 }
 
+// 32 bf16 of row r from column c0 of a (row pitch ld) into four 16-byte
+// registers, when the row exists and all 32 columns are inside n_cols
+// (ragged chunks are read element by element where they are used).
+__device__ __forceinline__ void prefetch_aux32(const bf16* a, int64_t ld, int r, int c0,
+                                               int n_rows, int n_cols, bool use,
+                                               uint4 (&dst)[4]) {
+  if (use && r < n_rows && c0 + 32 <= n_cols) {
+    const uint4* s = reinterpret_cast<const uint4*>(a + static_cast<int64_t>(r) * ld + c0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = s[q];
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&u)[4], float (&x)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[q * 8 + 2 * k] = __uint_as_float(w[k] << 16);
+      x[q * 8 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+}
+
 __device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&x)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -424,23 +452,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     for (int64_t t = pair; t < p.total_tiles; t += npairs) {
       const TileCoord tc = map_tile<MODE>(p, t, rank);
       const GemmClass& C = p.cls[tc.cls];
+      const int r0 = tc.tm * kBM + ew * 32;  // first row of this warp
+      const int r = r0 + lane;
+      const int rows_out = apply ? C.out_rows : C.m;
+      const int n_out = apply ? C.out_cols : C.m;
+      const bf16* aux = C.aux + static_cast<int64_t>(tc.view) * C.aux_view_stride;
+      // The epilogue's second operand (a X for apply, b A for poly) is an input
+      // of this launch: the first 32 columns of this lane's row are fetched
+      // before the accumulator is ready, and each later chunk one step ahead,
+      // so no chunk waits for a load it has just issued.
+      const bool use_aux = apply || p.kind == GEMM_POLY;
+      uint4 pf[4];
+      prefetch_aux32(aux, C.ld_aux, r, tc.tn * kBN, rows_out, n_out, use_aux, pf);
       if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPI)) {
         abort_pair(abort_flag);
         break;
       }
       tc_fence_after();
 
-      const int r0 = tc.tm * kBM + ew * 32;  // first row of this warp
-      const int r = r0 + lane;
-      const int rows_out = apply ? C.out_rows : C.m;
-      const int n_out = apply ? C.out_cols : C.m;
       float sc = 1.0f;
       if (p.first_iter) {
         const float s = ns_inv_norm(C.sumsq[tc.view], p.norm_scale, p.eps);
         sc = apply ? s : s * s;
       }
       bf16* out = C.out + static_cast<int64_t>(tc.view) * C.out_view_stride;
-      const bf16* aux = C.aux + static_cast<int64_t>(tc.view) * C.aux_view_stride;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
                              static_cast<uint32_t>(acc * kBN);
 
@@ -448,6 +483,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int cc = 0; cc < kBN / 32; ++cc) {
         const int c0 = tc.tn * kBN + cc * 32;
         if (c0 >= n_out) break;  // warp-uniform
+        uint4 cur[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cur[q] = pf[q];
+        if (cc + 1 < kBN / 32)
+          prefetch_aux32(aux, C.ld_aux, r, c0 + 32, rows_out, n_out, use_aux, pf);
         uint32_t raw[32];
         tmem_ld_32x32b_x32(t_row + cc * 32, raw);
         tmem_ld_wait();
@@ -465,7 +505,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
             if (full_cols) {
               float x[32];
-              load_bf16x32(aux + aoff, x);
+              unpack_bf16x32(cur, x);
 #pragma unroll
               for (int j = 0; j < 32; ++j) u[j] = sc * (p.a * x[j] + v[j]);
             } else {
@@ -494,7 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
             if (full_cols) {
               float x[32];
-              load_bf16x32(aux + aoff, x);
+              unpack_bf16x32(cur, x);
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = sc * (p.a * x[j] + v[j]);
               store_bf16x32(out + off, v);
@@ -516,7 +556,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
             if (full_cols) {
               float x[32];
-              load_bf16x32(aux + aoff, x);
+              unpack_bf16x32(cur, x);
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = p.b * x[j] + p.c * v[j];
             } else {
