@@ -276,18 +276,24 @@ class DeviceWorkload:
         if self.control is not None:
             self.grefs_host = [mh.grad_ref(g) for g in list(muon_host) + list(adam_host)]
 
-    def step(self, stream, host_grads: bool = False) -> None:
+    def step(self, stream, host_grads: bool = False, param_fence=None) -> None:
+        """One step on `stream`. `param_fence` (a torch.cuda.Event) holds back
+        the step's first parameter write until the event has completed."""
         s = stream.cuda_stream
         ts = self.ts_host if host_grads else self.ts
         at = self.at_host if host_grads else self.at
         self.step_count += 1
         self.hp.sr_seed = self.step_count
+        self.hp.param_fence = param_fence.cuda_event if (param_fence is not None and ts) else None
+        if param_fence is not None and not ts:
+            stream.wait_event(param_fence)
         if self.control is not None:
             refs = self.grefs_host if host_grads else self.grefs
             self.mh._lib.grad_prepare(refs, 1.0, float(self.max_grad_norm), self.cstruct,
                                       self.gws.data_ptr(), self.gws.numel(), s)
         if ts:
             self.mh.muon_step_batched(ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
+            self.hp.param_fence = None
         if at:
             hp = self.wl.adam_hp
             if self.control is not None:
@@ -728,40 +734,63 @@ def main():
             nm = len(dw.mG)
             dw.use_host_grads(gin.host[:nm], gin.host[nm:])
 
-        def one_step(k=None):
+        # Step k+1's prologue and Newton-Schulz run while step k's parameters
+        # are copied out on a second stream; step k+1's first parameter write
+        # waits for that copy (param_fence). The timed region ends when the
+        # last copy has landed.
+        copy_stream = torch.cuda.Stream()
+
+        def one_step(k, fence):
             if k is not None:
                 ev[k][0].record(stream)
             if not in_place:
                 gin.h2d()
             if k is not None:
                 ev[k][1].record(stream)
-            dw.step(stream, host_grads=in_place)
+            dw.step(stream, host_grads=in_place, param_fence=fence)
+            done = torch.cuda.Event(enable_timing=k is not None)
+            done.record(stream)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                if k is not None:
+                    ev[k][2].record(copy_stream)
+                pout.d2h()
+                landed = torch.cuda.Event(enable_timing=k is not None)
+                landed.record(copy_stream)
             if k is not None:
-                ev[k][2].record(stream)
-            pout.d2h()
-            if k is not None:
-                ev[k][3].record(stream)
+                ev[k][3] = landed
+                ev[k][4] = done
+            return landed
 
-        one_step()
+        fence = one_step(None, None)
+        stream.wait_event(fence)
         torch.cuda.synchronize()
         barrier(world)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] + [None, None]
+              for _ in range(args.steps)]
+        fence = None
         for k in range(args.steps):
-            one_step(k)
+            fence = one_step(k, fence)
+        end = torch.cuda.Event(enable_timing=True)
+        stream.wait_event(fence)
+        end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        e2e_ms = max_over_ranks(ev[0][0].elapsed_time(ev[-1][3]) / args.steps, world)
+        e2e_ms = max_over_ranks(ev[0][0].elapsed_time(end) / args.steps, world)
         h2d_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-        step_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        step_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in ev)
         d2h_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
         e2e = {"value": round(e2e_ms, 3), "unit": "ms/step", "h2d_bytes_per_step": gin.nbytes,
                "d2h_bytes_per_step": pout.nbytes, "h2d_ms": round(h2d_ms, 2),
                "step_ms": round(step_ms, 2), "d2h_ms": round(d2h_ms, 2),
                "path": ("C ABI calls whose kernels read this step's gradients in place from "
                         "page-locked host memory over the host link; updated parameters copied "
-                        "back each step") if in_place else
+                        "back each step on a second stream, overlapping the next step up to its "
+                        "first parameter write (param_fence)") if in_place else
                        ("C ABI calls with gradients copied in from pinned host memory and "
-                        "updated parameters copied back each step"),
+                        "updated parameters copied back each step on a second stream, "
+                        "overlapping the next step up to its first parameter write "
+                        "(param_fence)"),
                "h2d_in_kernel": in_place,
                "pinned": bool(gin.registered and pout.registered)}
         if in_place:

@@ -127,6 +127,17 @@ typedef struct {
   const float* coeff_schedule;  /* HOST array of ns_steps x 3 floats (a, b, c of each
                                    iteration in order), or NULL: (a, b, c) above every time */
   float norm_scale;             /* > 0; 0 means 1 (the Speedtronic form) */
+  /* Parameter-write fence: a cudaEvent_t, or NULL for none. The call makes its
+   * stream wait for this event (cudaStreamWaitEvent) just before its first
+   * kernel that writes a parameter -- the last Newton-Schulz apply stage, or
+   * the separate apply when NorMuon or Muon+ is on -- and not before. Work
+   * the caller ordered before recording the event on another stream (e.g. a
+   * device-to-host copy of the previous step's parameters) thus runs
+   * alongside this call's momentum, normalisation and Newton-Schulz kernels
+   * and still finishes before any parameter changes; everything enqueued on
+   * the stream after this call is ordered after the wait as well. The event
+   * is only waited on, never recorded or destroyed by the library. */
+  void* param_fence;
 } mh_muon_hparams;
 
 /* Bytes of device workspace mh_muon_step_batched needs for these tensors and

@@ -42,7 +42,8 @@ class MuonHparams(ctypes.Structure):
                 ("normuon", c_int32), ("beta2", c_float), ("muon_plus", c_int32),
                 ("plus_eps", c_float), ("cautious", c_int32),
                 ("grad_mult", c_void_p), ("skip", c_void_p), ("sr_seed", c_uint64),
-                ("coeff_schedule", c_void_p), ("norm_scale", c_float)]
+                ("coeff_schedule", c_void_p), ("norm_scale", c_float),
+                ("param_fence", c_void_p)]
 
 
 class NsProblem(ctypes.Structure):

@@ -349,7 +349,7 @@ class ProfScope {
 int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, float eps, int sms,
            cudaStream_t stream, int* final_buf, bool final_update = false, int cautious = 0,
            const int32_t* skip = nullptr, const float* sched = nullptr,
-           float norm_scale = 1.0f) {
+           float norm_scale = 1.0f, cudaEvent_t fence = nullptr) {
   int cur = 0;
   const int nclass = static_cast<int>(P.classes.size());
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
@@ -381,6 +381,13 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           gp.skip = skip;
           const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
           gp.final_update = fused ? 1 : 0;
+          if (fused && fence) {
+            // First launch that writes parameters (stream order carries the
+            // wait to every later launch).
+            const cudaError_t fe = cudaStreamWaitEvent(stream, fence, 0);
+            if (fe != cudaSuccess) return cuda_fail(fe, "cudaStreamWaitEvent(param_fence)");
+            fence = nullptr;
+          }
           gp.cautious = cautious;
           int64_t tiles = 0;
           int nc = 0;
@@ -849,8 +856,10 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
               sms, stream);
   if (rc != MH_OK) return rc;
   if ((rc = run_view_norm(P, tile_ss, sumsq, stream, hp->skip)) != MH_OK) return rc;
+  cudaEvent_t fence = static_cast<cudaEvent_t>(hp->param_fence);
   rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf,
-              fuse_update, hp->cautious, hp->skip, hp->coeff_schedule, proto.ns_norm_scale);
+              fuse_update, hp->cautious, hp->skip, hp->coeff_schedule, proto.ns_norm_scale,
+              fuse_update ? fence : nullptr);
   if (rc != MH_OK) return rc;
   if (fuse_update) return MH_OK;
   auto fill_final = [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, final_buf); };
@@ -911,6 +920,10 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
         if (e != cudaSuccess) return cuda_fail(e, "column finalisation launch");
       }
     }
+  }
+  if (fence) {
+    e = cudaStreamWaitEvent(stream, fence, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(param_fence)");
   }
   return run_ew(EW_APPLY, P, proto, fill_final, sms, stream);
 }

@@ -342,13 +342,18 @@ class HybridMuonAdamW:
         return _lib.muon_workspace_bytes(self._muon_structs([e.param for e in self.muon]), self.hp)
 
     def step(self, muon_grads=None, adam_grads=None, stream=None,
-             inv_loss_scale: float = 1.0) -> None:
+             inv_loss_scale: float = 1.0, param_fence=None) -> None:
         """One hybrid step. Gradients default to each parameter's ``.grad``.
 
         With gradient control on, the gradients are first unscaled by
         ``inv_loss_scale``, their global norm is taken and clipped to
         ``max_grad_norm``, and the whole step is skipped on the device when one
-        of them is inf or NaN (``self.control.skip``); no host sync happens."""
+        of them is inf or NaN (``self.control.skip``); no host sync happens.
+
+        ``param_fence`` (a recorded ``torch.cuda.Event``): the step's stream
+        waits for it just before the first kernel that writes a parameter, so
+        work ordered before it on another stream (a copy of the previous
+        step's parameters) overlaps the momentum and Newton-Schulz kernels."""
         muon_grads = muon_grads if muon_grads is not None else [e.param.grad for e in self.muon]
         adam_grads = adam_grads if adam_grads is not None else [e.param.grad for e in self.adam]
         s = _stream_ptr(stream)
@@ -364,7 +369,13 @@ class HybridMuonAdamW:
             need = _lib.muon_workspace_bytes(ts, self.hp)
             if self._ws is None or self._ws.numel() < need:
                 self._ws = alloc_workspace(need, self.muon[0].param.device)
-            _lib.muon_step_batched(ts, self.hp, self._ws.data_ptr(), self._ws.numel(), s)
+            self.hp.param_fence = param_fence.cuda_event if param_fence is not None else None
+            try:
+                _lib.muon_step_batched(ts, self.hp, self._ws.data_ptr(), self._ws.numel(), s)
+            finally:
+                self.hp.param_fence = None
+        elif param_fence is not None:
+            (stream or torch.cuda.current_stream()).wait_event(param_fence)
         if self.adam:
             b1, b2 = self.adam_betas
             if self.control is not None:

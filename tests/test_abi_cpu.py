@@ -53,9 +53,10 @@ def test_struct_layout_matches_header(tmp_path):
         " offsetof(mh_muon_tensor, views), offsetof(mh_muon_hparams, cautious),"
         " offsetof(mh_adamw_tensor, numel), offsetof(mh_muon_hparams, grad_mult),"
         " offsetof(mh_muon_hparams, skip), sizeof(mh_grad_ref), sizeof(mh_grad_control),"
-        " offsetof(mh_grad_control, step)); printf(\"%zu %zu %zu %zu\\n\","
+        " offsetof(mh_grad_control, step)); printf(\"%zu %zu %zu %zu %zu\\n\","
         " offsetof(mh_muon_hparams, sr_seed), offsetof(mh_muon_hparams, coeff_schedule),"
-        " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, skip_zero_grad));"
+        " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, skip_zero_grad),"
+        " offsetof(mh_muon_hparams, param_fence));"
         " return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -69,7 +70,8 @@ def test_struct_layout_matches_header(tmp_path):
             mh.MuonHparams.skip.offset, ctypes.sizeof(mh.GradRef),
             ctypes.sizeof(mh.GradControl), mh.GradControl.step.offset,
             mh.MuonHparams.sr_seed.offset, mh.MuonHparams.coeff_schedule.offset,
-            mh.MuonHparams.norm_scale.offset, mh.MuonTensor.skip_zero_grad.offset]
+            mh.MuonHparams.norm_scale.offset, mh.MuonTensor.skip_zero_grad.offset,
+            mh.MuonHparams.param_fence.offset]
     assert got == want
 
 
