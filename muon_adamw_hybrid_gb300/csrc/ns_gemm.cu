@@ -220,12 +220,18 @@ __device__ __forceinline__ void store_f32x32(void* base, int dt, int64_t off, in
 // max(1, rows/cols)^0.5 scale), or one of the cautious forms (flaxchat step
 // 4; Speedtronic "Cautious updates"), on 32 consecutive elements of one
 // stored row starting at element `off`; u holds the Newton-Schulz output.
+// `wpre`: the 32 bf16 parameters at `off`, already loaded (full vector
+// chunks of a bf16 parameter), or null to load them here.
 __device__ __forceinline__ void update_w32(const ViewRec& R, int64_t off, int nvalid,
-                                           const float (&u)[32], int cautious) {
+                                           const float (&u)[32], int cautious,
+                                           const uint4 (*wpre)[4]) {
   if (R.inactive) return;  // zero gradient under the inactive-expert rule
   const bool vec = R.vec && nvalid == 32;
   float w[32];
-  load_f32x32(R.param, R.pdt, off, nvalid, vec, w);
+  if (wpre)
+    unpack_bf16x32(*wpre, w);
+  else
+    load_f32x32(R.param, R.pdt, off, nvalid, vec, w);
   const float lr = R.lr, wd = R.wd, sc = R.shape_scale;
   if (cautious == MH_CAUTIOUS_OFF) {
     const float decay = 1.0f - lr * wd;
@@ -464,6 +470,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const bool use_aux = apply || p.kind == GEMM_POLY;
       uint4 pf[4];
       prefetch_aux32(aux, C.ld_aux, r, tc.tn * kBN, rows_out, n_out, use_aux, pf);
+      // The fused update reads a bf16 parameter the same way, one chunk ahead.
+      // The record's view is stored exactly like this tile's output (tall views
+      // are kept in their stored layout), so row r / columns c0.. of the
+      // output are row r / columns c0.. of the parameter.
+      const bool fin = apply && p.final_update;
+      ViewRec R;
+      if (fin) R = C.vrec[tc.view];
+      const bool w_pf = fin && R.vec && R.pdt == MH_BF16 && !R.inactive;
+      const bf16* wbase = w_pf ? static_cast<const bf16*>(R.param) + R.elem0 : nullptr;
+      uint4 pw[4];
+      prefetch_aux32(wbase, fin ? R.cols : 0, r, tc.tn * kBN, rows_out, n_out, w_pf, pw);
       if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPI)) {
         abort_pair(abort_flag);
         break;
@@ -483,11 +500,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int cc = 0; cc < kBN / 32; ++cc) {
         const int c0 = tc.tn * kBN + cc * 32;
         if (c0 >= n_out) break;  // warp-uniform
-        uint4 cur[4];
+        uint4 cur[4], curw[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) cur[q] = pf[q];
-        if (cc + 1 < kBN / 32)
+        for (int q = 0; q < 4; ++q) {
+          cur[q] = pf[q];
+          curw[q] = pw[q];
+        }
+        if (cc + 1 < kBN / 32) {
           prefetch_aux32(aux, C.ld_aux, r, c0 + 32, rows_out, n_out, use_aux, pf);
+          prefetch_aux32(wbase, fin ? R.cols : 0, r, c0 + 32, rows_out, n_out, w_pf, pw);
+        }
         uint32_t raw[32];
         tmem_ld_32x32b_x32(t_row + cc * 32, raw);
         tmem_ld_wait();
@@ -517,14 +539,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 #pragma unroll
             for (int j = 0; j < 32; ++j) u[j] = 0.0f;
           }
-          // The record's view is stored exactly like this tile's output (tall
-          // views are kept in their stored layout), so row r / columns c0.. of
-          // the output are row r / columns c0.. of the parameter.
-          const ViewRec R = C.vrec[tc.view];
           if (row_ok) {
             const int nvalid = n_out - c0 < 32 ? n_out - c0 : 32;
             update_w32(R, R.elem0 + static_cast<int64_t>(r) * R.cols + c0, nvalid, u,
-                       p.cautious);
+                       p.cautious, w_pf && full_cols ? &curw : nullptr);
           }
           continue;
         }
