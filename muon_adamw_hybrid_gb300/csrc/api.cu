@@ -239,21 +239,35 @@ EncodeTiledFn get_encode_fn() {
 
 // 3-D bf16 map over a stacked class buffer: (inner, rows, views) with the
 // given row pitch; box (64, box_rows, 1), 128-byte swizzle, zero fill.
-int make_tmap(CUtensorMap* tm, const void* base, int64_t inner, int64_t rows, int64_t views,
-              int64_t ld, int box_rows) {
+// bf16 tensor map over `views` stacked (rows x inner) matrices of row pitch
+// `ld` elements, box (box_inner x box_rows x 1).
+int encode_tmap(CUtensorMap* tm, const void* base, int64_t inner, int64_t rows, int64_t views,
+                int64_t ld, int box_inner, int box_rows, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return fail(MH_ECUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(views)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
                            static_cast<cuuint64_t>(ld) * 2 * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MH_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   return MH_OK;
+}
+
+// Operand loads: 64-element (128-byte) rows, 128-byte swizzle.
+int make_tmap(CUtensorMap* tm, const void* base, int64_t inner, int64_t rows, int64_t views,
+              int64_t ld, int box_rows) {
+  return encode_tmap(tm, base, inner, rows, views, ld, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Epilogue stores: 32 x 32 boxes with 64-byte rows, 64-byte swizzle.
+int make_tmap_out(CUtensorMap* tm, const void* base, int64_t inner, int64_t rows, int64_t views,
+                  int64_t ld) {
+  return encode_tmap(tm, base, inner, rows, views, ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int device_sms(int* out) {
@@ -437,6 +451,8 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
                 if ((rc = make_tmap(&G.tmA, A, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
                 G.tmB = G.tmA;
               }
+              if ((rc = make_tmap_out(&G.tmOut, G.out, C.m, C.m, C.count, C.lda)) != MH_OK)
+                return rc;
             } else {
               G.tiles_m = static_cast<int32_t>(ceil_div(G.out_rows, 2 * kBM));
               G.tiles_n = static_cast<int32_t>(ceil_div(G.out_cols, kBN));
@@ -456,6 +472,9 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
                 if ((rc = make_tmap(&G.tmA, Pm, C.m, C.m, C.count, C.lda, kBM)) != MH_OK) return rc;
                 if ((rc = make_tmap(&G.tmB, X, C.n, C.m, C.count, C.ldx, 64)) != MH_OK) return rc;
               }
+              if ((rc = make_tmap_out(&G.tmOut, Xn, G.out_cols, G.out_rows, C.count, C.ldx)) !=
+                  MH_OK)
+                return rc;
             }
             G.tile_begin = tiles;
             tiles += static_cast<int64_t>(G.tiles_per_view) * C.count;

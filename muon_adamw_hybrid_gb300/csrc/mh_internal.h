@@ -222,6 +222,8 @@ struct GemmClass {
   CUtensorMap tmB;         // operand B: 128 of the 256 B rows per CTA of a pair: X (gram),
                            //   A (poly), P (apply, tstore) K-major; X (apply) or T
                            //   (gram, tstore) as MN-major 64 x 64 chunks
+  CUtensorMap tmOut;       // output (A, P or X'): 32 x 32 boxes, 64-byte swizzle, stored
+                           //   by the epilogue from shared memory
   bf16* out;               // output base (first view of the class)
   const bf16* aux;         // poly: A (b*A term); apply: X (a*X term)
   const double* sumsq;     // per view sum of squares of Q (first iteration only)

@@ -59,8 +59,12 @@ constexpr uint32_t kStageBBytes = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kHalfBBytes = kStageBBytes / 2;
 constexpr uint32_t kTmemCols = 2 * kBN;           // two fp32 accumulators
 constexpr uint32_t kApplyChunkBytes = kBK * 64 * 2;  // one 64-col MN-major box: 8 KB
-constexpr int kTPitch = 40;                        // bf16 pitch of the mirror-transpose tile
-constexpr uint32_t kTBytes = 32 * kTPitch * 2;     // per epilogue warp
+// Epilogue staging: each epilogue warp owns two buffers, each holding a 32 x 32
+// bf16 box of the chunk (rows r0.., cols c0..) and one of its transpose (the
+// mirrored block of a symmetric output), laid out as the 64-byte-swizzled
+// boxes the output tensor map stores.
+constexpr uint32_t kOutBoxBytes = 32 * 32 * 2;                 // 2 KB
+constexpr uint32_t kOutWarpBytes = 2 * 2 * kOutBoxBytes;        // 8 KB per epilogue warp
 constexpr uint16_t kPairMask = 0x3;
 
 struct TileCoord {
@@ -279,8 +283,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageABytes;
-  uint8_t* sT = sB + kStages * kStageBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sT + 4 * kTBytes);
+  uint8_t* sO = sB + kStages * kStageBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sO + 4 * kOutWarpBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -452,7 +456,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
     const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
-    bf16* tbuf = reinterpret_cast<bf16*>(sT + ew * kTBytes);
+    uint8_t* obuf = sO + ew * kOutWarpBytes;
+    uint32_t staged = 0;  // chunks this warp has handed to TMA stores (buffer = parity)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = pair; t < p.total_tiles; t += npairs) {
@@ -492,7 +497,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         const float s = ns_inv_norm(C.sumsq[tc.view], p.norm_scale, p.eps);
         sc = apply ? s : s * s;
       }
-      bf16* out = C.out + static_cast<int64_t>(tc.view) * C.out_view_stride;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
                              static_cast<uint32_t>(acc * kBN);
 
@@ -548,28 +552,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
         if (apply) {
           if (row_ok) {
-            const int64_t off = static_cast<int64_t>(r) * C.ld_out + c0;
-            const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
             if (full_cols) {
               float x[32];
               unpack_bf16x32(cur, x);
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = sc * (p.a * x[j] + v[j]);
-              store_bf16x32(out + off, v);
             } else {
+              const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (c0 + j < n_out)
-                  out[off + j] =
-                      __float2bfloat16_rn(sc * (p.a * __bfloat162float(aux[aoff + j]) + v[j]));
+                if (c0 + j < n_out) v[j] = sc * (p.a * __bfloat162float(aux[aoff + j]) + v[j]);
             }
           }
-          continue;
-        }
-
-        // Symmetric output: element (r, c) with c >= r is stored at (r, c)
-        // and, when c > r, mirrored to (c, r).
-        if (p.kind == GEMM_POLY) {
+        } else if (p.kind == GEMM_POLY) {
           if (row_ok) {
             const int64_t aoff = static_cast<int64_t>(r) * C.ld_aux + c0;
             if (full_cols) {
@@ -587,45 +582,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= sc;
         }
-        if (row_ok) {
-          const int64_t off = static_cast<int64_t>(r) * C.ld_out + c0;
-          if (full_cols && c0 >= r) {
-            store_bf16x32(out + off, v);
-          } else {
+
+        // Store through shared memory and TMA (rows and columns outside the
+        // output are dropped by the tensor map). A symmetric output (gram,
+        // poly) holds the upper block triangle only: the chunk on the diagonal
+        // (c0 == r0) is stored whole, a chunk above it (c0 > r0) is stored and
+        // mirrored to rows c0.., columns r0..; chunks below it are the mirror
+        // images of chunks stored by the warp that owns rows c0...
+        const bool direct = apply || c0 >= r0;
+        const bool mirror = !apply && c0 > r0;
+        if (!direct || r0 >= rows_out) continue;  // warp-uniform
+        uint8_t* bd = obuf + (staged & 1u) * (2 * kOutBoxBytes);
+        uint8_t* bm = bd + kOutBoxBytes;
+        // The stores issued from this buffer two chunks ago have read it.
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        {
+          // Row `lane` of the box: 16-byte piece q goes to slot q ^ ((lane >> 1) & 3).
+          const uint32_t swz = (static_cast<uint32_t>(lane) >> 1) & 3u;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c0 + j < n_out && c0 + j >= r) out[off + j] = __float2bfloat16_rn(v[j]);
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+            u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+            u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+            u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+            *reinterpret_cast<uint4*>(bd + lane * 64 + ((static_cast<uint32_t>(q) ^ swz) << 4)) = u;
           }
         }
-        if (c0 + 31 > r0) {  // some element of the chunk lies above the diagonal (warp-uniform)
-          // Transpose the 32 x 32 chunk in shared memory: lane L then owns
-          // output row c0 + L and writes columns r0 .. r0+31 of it.
+        if (mirror) {
+          // Element (r0 + lane, c0 + j) is row j, column lane of the mirror box.
+          const uint32_t piece = static_cast<uint32_t>(lane) >> 3;
+          const uint32_t within = (static_cast<uint32_t>(lane) & 7u) << 1;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tbuf[j * kTPitch + lane] = __float2bfloat16_rn(v[j]);
-          __syncwarp();
-          const int c = c0 + lane;
-          if (c < n_out) {
-            bf16* dst = out + static_cast<int64_t>(c) * C.ld_out + r0;
-            const bf16* src = tbuf + lane * kTPitch;
-            if (r0 + 32 <= c && r0 + 32 <= C.m) {
-              const uint4* s4 = reinterpret_cast<const uint4*>(src);
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) d4[q] = s4[q];
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (r0 + i < c && r0 + i < C.m) dst[i] = src[i];
-            }
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t slot = piece ^ ((static_cast<uint32_t>(j) >> 1) & 3u);
+            *reinterpret_cast<bf16*>(bm + j * 64 + (slot << 4) + within) =
+                __float2bfloat16_rn(v[j]);
           }
-          __syncwarp();
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&C.tmOut, bd, c0, r0, tc.view);
+          if (mirror) tma_store_3d(&C.tmOut, bm, r0, c0, tc.view);
+          bulk_commit();
+        }
+        ++staged;
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    // Every TMA store of this warp has landed before the kernel ends.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // Neither CTA of the pair leaves while the other may still multicast into
@@ -641,7 +653,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 }  // namespace
 
 size_t gemm_smem_bytes() {
-  return 1024 + kStages * (kStageABytes + kStageBBytes) + 4 * kTBytes +
+  return 1024 + kStages * (kStageABytes + kStageBBytes) + 4 * kOutWarpBytes +
          (2 * kStages + 5) * sizeof(uint64_t) + 16;
 }
 
