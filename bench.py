@@ -53,8 +53,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama7b",
-                    help="llama7b (default), gpt124m, moe_mla, single, adamw_2p30, or ns "
-                         "(Newton-Schulz only, see --ns-n/--ns-aspect/--ns-batch)")
+                    help="llama7b (default), gpt124m, moe_mla, single, adamw_2p30, ns "
+                         "(Newton-Schulz only, see --ns-n/--ns-aspect/--ns-batch), or ns_sweep "
+                         "(every Newton-Schulz sweep point, one JSON line each)")
     ap.add_argument("--ns-n", type=int, default=4096)
     ap.add_argument("--ns-aspect", default="1:1", choices=["1:1", "1:4", "4:1"])
     ap.add_argument("--ns-batch", type=int, default=8)
@@ -615,11 +616,90 @@ def run_ns_only(args):
     return 0
 
 
+def run_ns_sweep(args):
+    """The Newton-Schulz-only sweep (n x n, n x 4n, 4n x n for n = 512..8192,
+    batches 1..256) in one process: one JSON line per point with the call time,
+    nominal and executed TFLOP/s and each stage's time. X is capped at 16 GiB
+    per point: with its output and the workspace (two X buffers, A and P) a
+    point holds about 4x X on the device. Not the driver's one-line contract."""
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+    from synth import workloads as W
+    from synth.gpu import fill_normal
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = load_peaks()
+    a_, b_, c_ = 3.4445, -4.7750, 2.0315
+    for aspect, n, batch, r, c in W.ns_sweep_shapes(16 * 2 ** 30):
+        x = torch.empty(batch * r, c, dtype=torch.bfloat16, device=device)
+        fill_normal(x, 0, 5000 + n, 1.0)
+        out = torch.empty_like(x)
+        probs = [mh.ns_problem(x, out, batch)]
+        need = mh.ns_workspace_bytes(probs)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+
+        def call():
+            mh.newton_schulz_batched(probs, 5, a_, b_, c_, 1e-7, ws.data_ptr(), need,
+                                     stream.cuda_stream)
+        call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        once = e0.elapsed_time(e1)
+        reps = max(3, min(args.steps * 20, int(200.0 / max(once, 1e-3))))
+        mh.profiler_reset()
+        mh.profiler_enable(True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mh.profiler_enable(False)
+        ms = e0.elapsed_time(e1) / reps
+        st = mh.profiler_read()
+        m_, n_ = min(r, c), max(r, c)
+        flops = batch * 5 * (4.0 * m_ * m_ * n_ + 2.0 * m_ ** 3)
+        fexec = sum(v["flops_executed"] for k, v in st.items() if k.startswith("ns_gemm"))
+        print(json.dumps({
+            "point": f"ns_{aspect}_n{n}_batch{batch}", "rows": r, "cols": c, "batch": batch,
+            "x_gb": round(batch * r * c * 2 / 1e9, 3), "reps": reps, "ms_per_call": round(ms, 4),
+            "tflops_nominal": round(flops / (ms * 1e-3) / 1e12, 1),
+            "tflops_executed": round(fexec / reps / (ms * 1e-3) / 1e12, 1),
+            "frac_executed_of_burst": round(fexec / reps / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "peak_source": f"bf16 burst, of {peak_src}",
+            "stage_ms": {k: round(v["total_ms"] / reps, 4) for k, v in st.items()},
+            "launches_per_call": sum(v["launches"] for v in st.values()) // reps}), flush=True)
+        del x, out, ws
+        torch.cuda.empty_cache()
+    return 0
+
+
+def launch_floor_us(stream, n: int = 2000) -> float:
+    """Device time per launch of n back-to-back minimal kernels on `stream`: the
+    floor a chain of dependent launches cannot go below."""
+    import torch
+    for _ in range(100):
+        torch.cuda._sleep(0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        torch.cuda._sleep(0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n
+
+
 def main():
     args = parse_args()
     from synth import workloads as W
     if args.workload == "ns":
         return run_ns_only(args)
+    if args.workload == "ns_sweep":
+        return run_ns_sweep(args)
     if args.workload not in W.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(W.WORKLOADS)}")
     wl = W.WORKLOADS[args.workload]()
@@ -663,6 +743,14 @@ def main():
     dw.check_status(stream)
     kstats = family_stats(stage_stats)
     launches = sum(v["launches"] for v in kstats.values())
+    # Small sets are bound by launch latency: the chain of this step's launches
+    # cannot run faster than launches x the device's per-launch floor.
+    floor_us = launch_floor_us(stream)
+    per_step = launches / max(args.steps, 1)
+    launch_floor = {"us_per_launch": round(floor_us, 3), "launches_per_step": per_step,
+                    "floor_ms_per_step": round(per_step * floor_us * 1e-3, 4),
+                    "frac_of_step": round(per_step * floor_us * 1e-3 / ms_step, 4),
+                    "kernel": "torch.cuda._sleep(0), 2000 back to back"}
 
     # ---- roofline of the dominant kernel and of the top HBM-bound kernel -------------
     kernels = {}
@@ -820,6 +908,7 @@ def main():
             "ns_ms_per_step": round(ns_ms, 3),
             "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,
             "ns_stages": stages,
+            "launch_floor": launch_floor,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "resident_gb": round(dw.resident_bytes / 1e9, 1),
         }

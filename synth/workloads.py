@@ -184,14 +184,15 @@ def moe_mla() -> Workload:
     return Workload("moe64_mla_all_variants", muon, [], hp, dict(ADAM_HP), steps=1)
 
 
-def ns_sweep_shapes():
+def ns_sweep_shapes(max_x_bytes: int = 64 * 2 ** 30):
     """Newton-Schulz-only sweep: square n x n, wide n x 4n and tall 4n x n for
-    n in {512 .. 8192}, batch counts 1..256 capped at 64 GB of operand X."""
+    n in {512 .. 8192}, batch counts 1..256 capped at `max_x_bytes` of bf16
+    operand X (64 GiB by default)."""
     out = []
     for n in (512, 1024, 2048, 4096, 8192):
         for aspect, (r, c) in (("1:1", (n, n)), ("1:4", (n, 4 * n)), ("4:1", (4 * n, n))):
             for batch in (1, 4, 16, 64, 256):
-                if batch * r * c * 2 > 64 * 2 ** 30:
+                if batch * r * c * 2 > max_x_bytes:
                     continue
                 out.append((aspect, n, batch, r, c))
     return out
