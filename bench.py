@@ -277,14 +277,35 @@ class DeviceWorkload:
         if self.control is not None:
             self.grefs_host = [mh.grad_ref(g) for g in list(muon_host) + list(adam_host)]
 
-    def step(self, stream, host_grads: bool = False, param_fence=None) -> None:
+    def step(self, stream, host_grads: bool = False, param_fence=None, between=None) -> None:
         """One step on `stream`. `param_fence` (a torch.cuda.Event) holds back
-        the step's first parameter write until the event has completed."""
+        the step's first parameter write until the event has completed.
+        `between`: the Muon step is split into its gradient phase and the rest,
+        and between() is called in between; it may enqueue work that follows
+        the last gradient read and return an event to use as the fence."""
         s = stream.cuda_stream
         ts = self.ts_host if host_grads else self.ts
         at = self.at_host if host_grads else self.at
         self.step_count += 1
         self.hp.sr_seed = self.step_count
+        if between is not None and ts:
+            if self.control is not None:
+                refs = self.grefs_host if host_grads else self.grefs
+                self.mh._lib.grad_prepare(refs, 1.0, float(self.max_grad_norm), self.cstruct,
+                                          self.gws.data_ptr(), self.gws.numel(), s)
+            self.hp.param_fence = None
+            self.hp.phase = self.mh.MH_STEP_GRADIENTS
+            self.mh.muon_step_batched(ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
+            param_fence = between()
+            self.hp.phase = self.mh.MH_STEP_FINISH
+            self.hp.param_fence = param_fence.cuda_event if param_fence is not None else None
+            self.mh.muon_step_batched(ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
+            self.hp.phase = self.mh.MH_STEP_ALL
+            self.hp.param_fence = None
+            self._adamw(at, s)
+            return
+        if between is not None:            # no Muon tensors: the fence goes before AdamW
+            param_fence = between()
         self.hp.param_fence = param_fence.cuda_event if (param_fence is not None and ts) else None
         if param_fence is not None and not ts:
             stream.wait_event(param_fence)
@@ -295,6 +316,9 @@ class DeviceWorkload:
         if ts:
             self.mh.muon_step_batched(ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
             self.hp.param_fence = None
+        self._adamw(at, s)
+
+    def _adamw(self, at, s) -> None:
         if at:
             hp = self.wl.adam_hp
             if self.control is not None:
@@ -822,63 +846,72 @@ def main():
             nm = len(dw.mG)
             dw.use_host_grads(gin.host[:nm], gin.host[nm:])
 
-        # Step k+1's prologue and Newton-Schulz run while step k's parameters
-        # are copied out on a second stream; step k+1's first parameter write
-        # waits for that copy (param_fence). The timed region ends when the
-        # last copy has landed.
+        # Step k's parameters are copied out on a second stream while step k+1
+        # runs its Newton-Schulz stages: the copy starts once step k+1's
+        # gradient phase has read the gradients (so the two do not share the
+        # host memory's bandwidth) and step k+1's first parameter write waits
+        # for it (param_fence). The timed region ends when the last step's
+        # parameters have landed.
         copy_stream = torch.cuda.Stream()
+        copies = []          # (start, end) events of each timed copy
+        pending = [False]    # a finished step's parameters are not yet copied
 
-        def one_step(k, fence):
+        def copy_out(timed):
+            ready = torch.cuda.Event()
+            ready.record(stream)
+            copy_stream.wait_event(ready)
+            with torch.cuda.stream(copy_stream):
+                c0 = torch.cuda.Event(enable_timing=True)
+                c0.record(copy_stream)
+                pout.d2h()
+                landed = torch.cuda.Event(enable_timing=True)
+                landed.record(copy_stream)
+            if timed:
+                copies.append((c0, landed))
+            pending[0] = False
+            return landed
+
+        def one_step(k):
             if k is not None:
                 ev[k][0].record(stream)
             if not in_place:
                 gin.h2d()
             if k is not None:
                 ev[k][1].record(stream)
-            dw.step(stream, host_grads=in_place, param_fence=fence)
-            done = torch.cuda.Event(enable_timing=k is not None)
-            done.record(stream)
-            copy_stream.wait_event(done)
-            with torch.cuda.stream(copy_stream):
-                if k is not None:
-                    ev[k][2].record(copy_stream)
-                pout.d2h()
-                landed = torch.cuda.Event(enable_timing=k is not None)
-                landed.record(copy_stream)
+            dw.step(stream, host_grads=in_place,
+                    between=lambda: copy_out(k is not None) if pending[0] else None)
             if k is not None:
-                ev[k][3] = landed
-                ev[k][4] = done
-            return landed
+                ev[k][2].record(stream)
+            pending[0] = True
 
-        fence = one_step(None, None)
-        stream.wait_event(fence)
+        one_step(None)
+        stream.wait_event(copy_out(False))
         torch.cuda.synchronize()
         barrier(world)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] + [None, None]
-              for _ in range(args.steps)]
-        fence = None
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         for k in range(args.steps):
-            fence = one_step(k, fence)
+            one_step(k)
         end = torch.cuda.Event(enable_timing=True)
-        stream.wait_event(fence)
+        stream.wait_event(copy_out(True))
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(ev[0][0].elapsed_time(end) / args.steps, world)
         h2d_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-        step_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in ev)
-        d2h_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+        step_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        d2h_ms = statistics.mean(c[0].elapsed_time(c[1]) for c in copies)
         e2e = {"value": round(e2e_ms, 3), "unit": "ms/step", "h2d_bytes_per_step": gin.nbytes,
                "d2h_bytes_per_step": pout.nbytes, "h2d_ms": round(h2d_ms, 2),
                "step_ms": round(step_ms, 2), "d2h_ms": round(d2h_ms, 2),
                "path": ("C ABI calls whose kernels read this step's gradients in place from "
                         "page-locked host memory over the host link; updated parameters copied "
-                        "back each step on a second stream, overlapping the next step up to its "
-                        "first parameter write (param_fence)") if in_place else
+                        "back each step on a second stream, from the end of the next step's "
+                        "gradient phase up to its first parameter write (MH_STEP_GRADIENTS / "
+                        "MH_STEP_FINISH, param_fence)") if in_place else
                        ("C ABI calls with gradients copied in from pinned host memory and "
-                        "updated parameters copied back each step on a second stream, "
-                        "overlapping the next step up to its first parameter write "
-                        "(param_fence)"),
+                        "updated parameters copied back each step on a second stream, from the "
+                        "end of the next step's gradient phase up to its first parameter write "
+                        "(MH_STEP_GRADIENTS / MH_STEP_FINISH, param_fence)"),
                "h2d_in_kernel": in_place,
                "pinned": bool(gin.registered and pout.registered)}
         if in_place:

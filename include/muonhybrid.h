@@ -138,7 +138,25 @@ typedef struct {
    * the stream after this call is ordered after the wait as well. The event
    * is only waited on, never recorded or destroyed by the library. */
   void* param_fence;
+  /* Step phase (MH_STEP_*). A step may be split into two calls on the same
+   * stream with the same tensors, hyperparameters (but for this field) and
+   * workspace, the second enqueued after the first:
+   *   MH_STEP_GRADIENTS clears the workspace status and runs every kernel
+   *                     that reads the gradients (inactive-expert scan,
+   *                     momentum / Nesterov prologue, Frobenius norms);
+   *   MH_STEP_FINISH    runs the Newton-Schulz stages and the update, reading
+   *                     only the momentum, the parameters and the workspace
+   *                     (and the gradients again with MH_CAUTIOUS_UPDATE,
+   *                     whose mask compares the update with the gradient).
+   * Between the two the caller may enqueue work that must follow the last
+   * gradient read: reuse of the gradient buffers, or a copy-out of the
+   * previous step's parameters that should not compete with the gradient
+   * reads for host memory. param_fence applies to MH_STEP_FINISH and
+   * MH_STEP_ALL. */
+  int32_t phase;
 } mh_muon_hparams;
+
+enum { MH_STEP_ALL = 0, MH_STEP_GRADIENTS = 1, MH_STEP_FINISH = 2 };
 
 /* Bytes of device workspace mh_muon_step_batched needs for these tensors and
  * flags (256-byte aligned pointer required). Returns 0 and sets the error

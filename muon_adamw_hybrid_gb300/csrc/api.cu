@@ -696,6 +696,8 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
     return fail(MH_EINVAL, "plus_eps must be > 0 with muon_plus");
   if (hp->cautious < MH_CAUTIOUS_OFF || hp->cautious > MH_CAUTIOUS_UPDATE)
     return fail(MH_EINVAL, "cautious must be 0, 1 or 2 (got %d)", hp->cautious);
+  if (hp->phase < MH_STEP_ALL || hp->phase > MH_STEP_FINISH)
+    return fail(MH_EINVAL, "phase must be 0, 1 or 2 (got %d)", hp->phase);
   for (int i = 0; i < n; ++i) {
     const mh_muon_tensor& T = t[i];
     int rc = check_shape(T.views, T.rows, T.cols, i, "tensors");
@@ -799,9 +801,14 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   int sms = 0;
   if ((rc = device_sms(&sms)) != MH_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool grad_phase = hp->phase != MH_STEP_FINISH;
+  const bool finish_phase = hp->phase != MH_STEP_GRADIENTS;
 
-  cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
+  cudaError_t e = cudaSuccess;
+  if (grad_phase) {
+    e = cudaMemsetAsync(ws, 0, kHeaderBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
+  }
 
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
   float* tile_ss = reinterpret_cast<float*>(ws + P.off_tile_ss);
@@ -811,7 +818,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   float* colfac = reinterpret_cast<float*>(ws + P.off_colfac);
   ViewRec* vrec = reinterpret_cast<ViewRec*>(ws + P.off_vrec);
   int32_t* active = reinterpret_cast<int32_t*>(ws + P.off_active);
-  if ((rc = run_view_active(P, tensors, active, sms, stream)) != MH_OK) return rc;
+  if (grad_phase && (rc = run_view_active(P, tensors, active, sms, stream)) != MH_OK) return rc;
   const bool need_rows = hp->normuon || hp->muon_plus;
   // Without NorMuon / Muon+ the update needs nothing beyond U itself, so the
   // last Newton-Schulz apply stage writes the parameters directly.
@@ -871,10 +878,13 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     J.shape_scale = static_cast<float>(std::sqrt(std::max(1.0, double(T.rows) / double(T.cols))));
   };
 
-  rc = run_ew(EW_PROLOGUE, P, proto, [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, 0); },
-              sms, stream);
-  if (rc != MH_OK) return rc;
-  if ((rc = run_view_norm(P, tile_ss, sumsq, stream, hp->skip)) != MH_OK) return rc;
+  if (grad_phase) {
+    rc = run_ew(EW_PROLOGUE, P, proto,
+                [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, 0); }, sms, stream);
+    if (rc != MH_OK) return rc;
+    if ((rc = run_view_norm(P, tile_ss, sumsq, stream, hp->skip)) != MH_OK) return rc;
+  }
+  if (!finish_phase) return MH_OK;
   cudaEvent_t fence = static_cast<cudaEvent_t>(hp->param_fence);
   rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf,
               fuse_update, hp->cautious, hp->skip, hp->coeff_schedule, proto.ns_norm_scale,

@@ -107,3 +107,50 @@ def test_optimizer_step_takes_a_fence():
         assert not torch.equal(p.detach(), b)
     assert opt.hp.param_fence is None
     np.testing.assert_equal(opt.applied_steps(), 1)
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(normuon=True), dict(cautious=2)])
+def test_two_phase_step_equals_one_call(variant):
+    """MH_STEP_GRADIENTS then MH_STEP_FINISH gives the one-call step bit for
+    bit; a snapshot taken between the two (behind a spin on another stream,
+    ordered after the gradient phase by an event) sees the new momentum and
+    the old parameters, and the finish phase's fence holds its parameter
+    write back until the snapshot is done."""
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    ref = _tensors(torch.bfloat16)
+    _step(mh.make_hparams(**variant), ref, main)
+    torch.cuda.synchronize()
+
+    tens = _tensors(torch.bfloat16)
+    w0 = [d["w"].clone() for d in tens]
+    ts = [mh.muon_tensor(d["w"], d["g"], d["b"], d["views"], d["sm"], 1.0, 0.01) for d in tens]
+    hp = mh.make_hparams(**variant)
+    ws = torch.empty(mh.muon_workspace_bytes(ts, hp), dtype=torch.uint8, device="cuda")
+    snap_w = [torch.empty_like(d["w"]) for d in tens]
+    snap_b = [torch.empty_like(d["b"]) for d in tens]
+    torch.cuda.synchronize()
+    hp.phase = mh.MH_STEP_GRADIENTS
+    mh.muon_step_batched(ts, hp, ws.data_ptr(), ws.numel(), main.cuda_stream)
+    grads_read = torch.cuda.Event()
+    grads_read.record(main)
+    fence = torch.cuda.Event()
+    with torch.cuda.stream(side):
+        side.wait_event(grads_read)
+        torch.cuda._sleep(SPIN_CYCLES)
+        for d, sw, sb in zip(tens, snap_w, snap_b):
+            sw.copy_(d["w"])
+            sb.copy_(d["b"])
+        fence.record(side)
+    hp.phase = mh.MH_STEP_FINISH
+    hp.param_fence = fence.cuda_event
+    mh.muon_step_batched(ts, hp, ws.data_ptr(), ws.numel(), main.cuda_stream)
+    torch.cuda.synchronize()
+    mh.workspace_status(ws.data_ptr(), main.cuda_stream)
+    for d, r, sw, sb, w in zip(tens, ref, snap_w, snap_b, w0):
+        assert torch.equal(sw, w)
+        assert torch.equal(sb, r["b"])
+        assert torch.equal(d["w"], r["w"]) and torch.equal(d["b"], r["b"])
+        assert torch.equal(d["sm"], r["sm"])
