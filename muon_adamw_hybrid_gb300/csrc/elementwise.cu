@@ -44,58 +44,6 @@ __device__ __forceinline__ int find_job(const EwParams& p, int64_t tile) {
   return lo;
 }
 
-// Loads `nvalid` (<= 4) consecutive elements starting at element `off`.
-__device__ __forceinline__ void load4(const void* base, int dt, int64_t off, int nvalid, bool vec,
-                                      float o[4]) {
-  if (vec && nvalid == 4) {
-    if (dt == MH_F32) {
-      const float4 t = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + off));
-      o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
-    } else {
-      const uint2 t = __ldcs(reinterpret_cast<const uint2*>(static_cast<const bf16*>(base) + off));
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
-      o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
-    }
-    return;
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (k < nvalid)
-      o[k] = dt == MH_F32 ? static_cast<const float*>(base)[off + k]
-                          : __bfloat162float(static_cast<const bf16*>(base)[off + k]);
-    else
-      o[k] = 0.0f;
-  }
-}
-
-__device__ __forceinline__ void store4(void* base, int dt, int64_t off, int nvalid, bool vec,
-                                       const float x[4]) {
-  if (vec && nvalid == 4) {
-    if (dt == MH_F32) {
-      __stcs(reinterpret_cast<float4*>(static_cast<float*>(base) + off),
-             make_float4(x[0], x[1], x[2], x[3]));
-    } else {
-      __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
-      __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
-      uint2 t;
-      t.x = *reinterpret_cast<uint32_t*>(&a);
-      t.y = *reinterpret_cast<uint32_t*>(&b);
-      __stcs(reinterpret_cast<uint2*>(static_cast<bf16*>(base) + off), t);
-    }
-    return;
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (k < nvalid) {
-      if (dt == MH_F32)
-        static_cast<float*>(base)[off + k] = x[k];
-      else
-        static_cast<bf16*>(base)[off + k] = __float2bfloat16_rn(x[k]);
-    }
-  }
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -107,36 +55,16 @@ struct TileInfo {
   int64_t v, r0, c0;
 };
 
-// Tile -> (job, view, first row, first col). 32-bit arithmetic: the host
-// rejects tensors with 2^31 or more tiles, and a 64-bit division per tile is
-// dozens of instructions in every thread.
-__device__ __forceinline__ TileInfo tile_info(const EwParams& p, int64_t tile) {
-  TileInfo t;
-  t.job = find_job(p, tile);
-  const EwJob& J = p.jobs[t.job];
-  const uint32_t local = static_cast<uint32_t>(tile - J.tile_begin);
-  const uint32_t tc = static_cast<uint32_t>(J.tiles_c);
-  const uint32_t per_view = static_cast<uint32_t>(J.tiles_r) * tc;
-  const uint32_t v = local / per_view;
-  const uint32_t w = local - v * per_view;
-  const uint32_t tr = w / tc;
-  t.v = v;
-  t.r0 = static_cast<int64_t>(tr) * kEwTileR;
-  t.c0 = static_cast<int64_t>(w - tr * tc) * kEwTileC;
-  return t;
-}
-
-// Loads this thread's 4 x 8 block of U (rows r0+4*warp+i, cols c0+8*lane+k)
-// from the Newton-Schulz output buffer, which holds every view in its stored
-// layout (row pitch ldx, a multiple of 8: every row load is 16-byte aligned).
-// All four loads are issued before any is used.
-__device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t, float u[4][8]) {
+// Issues this thread's loads of its 4 x 8 block of U (rows r0+4*warp+i, cols
+// c0+8*lane+k) from the Newton-Schulz output buffer, which holds every view in
+// its stored layout (row pitch ldx, a multiple of 8: every row load is
+// 16-byte aligned). All four loads are issued before any is used.
+__device__ __forceinline__ void load_u_raw(const EwJob& J, const TileInfo& t, uint4 (&raw)[4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bf16* xv = J.xf + t.v * J.x_view_stride;
   const int64_t col = t.c0 + lane * 8;
   const int64_t nv = J.cols - col;
   const int nvalid = nv >= 8 ? 8 : (nv > 0 ? static_cast<int>(nv) : 0);
-  uint4 raw[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = t.r0 + warp * 4 + i;
@@ -144,6 +72,16 @@ __device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t, 
     if (row < J.rows && nvalid == 8)
       raw[i] = __ldcs(reinterpret_cast<const uint4*>(xv + row * J.ldx + col));
   }
+}
+
+// Unpacks the block issued by load_u_raw (ragged last columns are read here).
+__device__ __forceinline__ void unpack_u_block(const EwJob& J, const TileInfo& t,
+                                               const uint4 (&raw)[4], float u[4][8]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bf16* xv = J.xf + t.v * J.x_view_stride;
+  const int64_t col = t.c0 + lane * 8;
+  const int64_t nv = J.cols - col;
+  const int nvalid = nv >= 8 ? 8 : (nv > 0 ? static_cast<int>(nv) : 0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t wd[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
@@ -159,6 +97,32 @@ __device__ __forceinline__ void load_u_block(const EwJob& J, const TileInfo& t, 
       for (int k = 0; k < 8; ++k) u[i][k] = k < nvalid ? __bfloat162float(src[k]) : 0.0f;
     }
   }
+}
+
+// Tile -> (view, first row, first col) within the job record held in shared
+// memory. 32-bit arithmetic: the host rejects tensors with 2^31 or more tiles,
+// and a 64-bit division per tile is dozens of instructions in every thread.
+__device__ __forceinline__ TileInfo tile_info_in(const EwJob& J, int job, int64_t tile) {
+  TileInfo t;
+  t.job = job;
+  const uint32_t local = static_cast<uint32_t>(tile - J.tile_begin);
+  const uint32_t tc = static_cast<uint32_t>(J.tiles_c);
+  const uint32_t per_view = static_cast<uint32_t>(J.tiles_r) * tc;
+  const uint32_t v = local / per_view;
+  const uint32_t w = local - v * per_view;
+  const uint32_t tr = w / tc;
+  t.v = v;
+  t.r0 = static_cast<int64_t>(tr) * kEwTileR;
+  t.c0 = static_cast<int64_t>(w - tr * tc) * kEwTileC;
+  return t;
+}
+
+// This block's contiguous share [begin, end) of `total` tiles: consecutive
+// tiles mostly belong to one tensor, so the job record changes rarely.
+__device__ __forceinline__ void block_tile_range(int64_t total, int64_t& begin, int64_t& end) {
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  begin = min(total, static_cast<int64_t>(blockIdx.x) * per);
+  end = min(total, begin + per);
 }
 
 __device__ __forceinline__ void load8(const void* base, int dt, int64_t off, int nvalid, bool vec,
@@ -542,27 +506,36 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
   if (step_skipped(p.skip)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int cur_job = -1;
+  int64_t job_end = 0;
+  int64_t tile_begin, tile_end;
+  block_tile_range(p.total_tiles, tile_begin, tile_end);
 
-  for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-    const TileInfo t = tile_info(p, tile);
-    if (t.job != cur_job) {  // block-uniform
+  for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
+    if (cur_job < 0 || tile >= job_end) {  // block-uniform
+      const int jb = find_job(p, tile);
       __syncthreads();
       constexpr int kWords = sizeof(EwJob) / 4;
       static_assert(sizeof(EwJob) % 4 == 0, "EwJob must be a whole number of words");
       if (threadIdx.x < kWords)
         reinterpret_cast<uint32_t*>(&sJ)[threadIdx.x] =
-            reinterpret_cast<const uint32_t*>(&p.jobs[t.job])[threadIdx.x];
+            reinterpret_cast<const uint32_t*>(&p.jobs[jb])[threadIdx.x];
       __syncthreads();
-      cur_job = t.job;
+      cur_job = jb;
+      job_end = sJ.tile_begin + sJ.views * sJ.tiles_r * sJ.tiles_c;
     }
     const EwJob& J = sJ;
+    const TileInfo t = tile_info_in(J, cur_job, tile);
     const int64_t view_elem0 = t.v * J.rows * J.cols;
     const int64_t col = t.c0 + lane * 8;
     const int64_t ncol = J.cols - col;
     const int nvalid = ncol >= 8 ? 8 : (ncol > 0 ? static_cast<int>(ncol) : 0);
 
+    // The U block's loads are issued here; the apply issues its parameter
+    // loads before unpacking them, so both are in flight together.
+    uint4 uraw[4];
+    load_u_raw(J, t, uraw);
     float u[4][8];
-    load_u_block(J, t, u);
+    if constexpr (KIND != EW_APPLY) unpack_u_block(J, t, uraw, u);
 
     if constexpr (KIND == EW_ROWSQ) {
 #pragma unroll
@@ -602,28 +575,54 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
       // EW_APPLY / EW_COPYOUT: final update direction U_ij.
       float uscale = 1.0f;
       if (p.u_scale_from_sumsq) uscale = ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps);
-      float h[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-      if (p.use_colfac) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < nvalid) h[k] = J.colfac[t.v * J.cols + col + k];
-      }
       // 16-byte access needs 8-element rows for bf16 and 4-element rows for fp32.
       const bool dvec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
       const bool svec = J.src_vec && (J.src_dtype == MH_F32 || (J.cols % 8) == 0);
       const bool active = J.active == nullptr || J.active[t.v] != 0;
       float w[4][8];
       float fr[4];
-      // Every load of the block (parameters, row factors) is in flight before
-      // any is used: the stores below may alias them, so nothing may be
-      // loaded between stores.
+      // Every load of the block (U, parameters, row and column factors) is in
+      // flight before any is used: the stores below may alias the parameter
+      // loads, so nothing may be loaded between stores. A vector bf16
+      // parameter is loaded raw and unpacked after U.
+      // (The cautious-update instantiation also holds the gradient block and
+      // has no registers to spare for the raw parameter block.)
+      const bool wraw = KIND == EW_APPLY && dvec && J.dst_dtype == MH_BF16 && nvalid == 8 &&
+                        active;
+      uint4 wr[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int64_t row = t.r0 + warp * 4 + i;
         fr[i] = p.use_rowfac && row < J.rows ? J.rowfac[t.v * J.rows + row] : 1.0f;
+        wr[i] = make_uint4(0u, 0u, 0u, 0u);
         if constexpr (KIND == EW_APPLY || KIND == EW_APPLY_CU) {
-          if (row < J.rows && nvalid > 0 && active)
-            load8(J.dst, J.dst_dtype, view_elem0 + row * J.cols + col, nvalid, dvec, w[i]);
+          if (row < J.rows && nvalid > 0 && active) {
+            const int64_t off = view_elem0 + row * J.cols + col;
+            if (wraw)
+              wr[i] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const bf16*>(J.dst) + off));
+            else
+              load8(J.dst, J.dst_dtype, off, nvalid, dvec, w[i]);
+          }
+        }
+      }
+      float h[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+      if (p.use_colfac) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < nvalid) h[k] = J.colfac[t.v * J.cols + col + k];
+      }
+      if constexpr (KIND == EW_APPLY) {
+        unpack_u_block(J, t, uraw, u);
+        if (wraw) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t wd[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              w[i][2 * k] = __uint_as_float(wd[k] << 16);
+              w[i][2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+            }
+          }
         }
       }
       // The cautious-update mask needs the gradient: a separate instantiation
