@@ -154,6 +154,11 @@ typedef struct {
    * reads for host memory. param_fence applies to MH_STEP_FINISH and
    * MH_STEP_ALL. */
   int32_t phase;
+  /* NorMuon floor (flaxchat "Muon Algorithm" step 3): each row is scaled by
+   * 1/sqrt(max(second moment, normuon_eps)). >= 0, finite; 0 means 1e-10.
+   * (The Frobenius-norm restore that follows divides by the norm after the
+   * row scaling, floored at 1e-10 against division by zero.) */
+  float normuon_eps;
 } mh_muon_hparams;
 
 enum { MH_STEP_ALL = 0, MH_STEP_GRADIENTS = 1, MH_STEP_FINISH = 2 };

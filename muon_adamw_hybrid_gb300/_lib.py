@@ -44,7 +44,7 @@ class MuonHparams(ctypes.Structure):
                 ("plus_eps", c_float), ("cautious", c_int32),
                 ("grad_mult", c_void_p), ("skip", c_void_p), ("sr_seed", c_uint64),
                 ("coeff_schedule", c_void_p), ("norm_scale", c_float),
-                ("param_fence", c_void_p), ("phase", c_int32)]
+                ("param_fence", c_void_p), ("phase", c_int32), ("normuon_eps", c_float)]
 
 
 class NsProblem(ctypes.Structure):

@@ -696,6 +696,8 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
     return fail(MH_EINVAL, "plus_eps must be > 0 with muon_plus");
   if (hp->cautious < MH_CAUTIOUS_OFF || hp->cautious > MH_CAUTIOUS_UPDATE)
     return fail(MH_EINVAL, "cautious must be 0, 1 or 2 (got %d)", hp->cautious);
+  if (!(hp->normuon_eps >= 0.0f) || !std::isfinite(hp->normuon_eps))
+    return fail(MH_EINVAL, "normuon_eps must be finite and >= 0 (0 means 1e-10)");
   if (hp->phase < MH_STEP_ALL || hp->phase > MH_STEP_FINISH)
     return fail(MH_EINVAL, "phase must be 0, 1 or 2 (got %d)", hp->phase);
   for (int i = 0; i < n; ++i) {
@@ -901,6 +903,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
       rp.normuon = hp->normuon ? 1 : 0;
       rp.muon_plus = hp->muon_plus ? 1 : 0;
       rp.beta2 = hp->beta2;
+      rp.normuon_eps = hp->normuon_eps > 0.0f ? hp->normuon_eps : 1e-10f;
       rp.plus_eps = hp->plus_eps;
       rp.skip = hp->skip;
       int64_t views = 0;

@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(256) row_finalize_kernel(const __grid_constant
         const float mean = q / static_cast<float>(J.cols);
         const float smn = sm[i] + (1.0f - p.beta2) * (mean - sm[i]);
         sm[i] = smn;
-        f = 1.0f / sqrtf(fmaxf(smn, 1e-10f));
+        f = 1.0f / sqrtf(fmaxf(smn, p.normuon_eps));
       }
       // fac holds f for now; the row sum q is needed again below, so keep it
       // in the first tile's partial slot (this view's partials are not read

@@ -131,6 +131,7 @@ struct RowFinParams {
   int64_t total_views;
   int32_t normuon, muon_plus;
   float beta2, plus_eps;
+  float normuon_eps;     // floor of the NorMuon second moment inside the rsqrt
   const int32_t* skip;   // gradient control: return at once when set, or null
 };
 

@@ -61,7 +61,7 @@ def _keep(struct, *tensors):
 
 def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_STEPS,
                  coeffs=NS_COEFFS, normuon=False, beta2=0.95, muon_plus=False, plus_eps=NS_EPS,
-                 cautious=0, norm_scale=1.0) -> MuonHparams:
+                 cautious=0, norm_scale=1.0, normuon_eps=1e-10) -> MuonHparams:
     """Muon hyperparameters. ``coeffs`` is one (a, b, c) for every iteration, or
     a sequence of ``ns_steps`` triples (flaxchat's Polar Express schedule);
     ``norm_scale`` gives X0 = Q / (||Q|| * norm_scale + eps)."""
@@ -77,7 +77,7 @@ def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_
     hp = MuonHparams(lr=lr, momentum=momentum, nesterov=int(bool(nesterov)), eps=eps,
                      ns_steps=ns_steps, a=a, b=b, c=c, normuon=int(bool(normuon)), beta2=beta2,
                      muon_plus=int(bool(muon_plus)), plus_eps=plus_eps, cautious=int(cautious),
-                     norm_scale=norm_scale)
+                     norm_scale=norm_scale, normuon_eps=normuon_eps)
     if sched is not None:
         hp.coeff_schedule = ctypes.addressof(sched)
         hp._sched = sched          # the library reads it during each call
@@ -283,11 +283,12 @@ class HybridMuonAdamW:
                  ns_steps=NS_STEPS, coeffs=NS_COEFFS, eps=NS_EPS, normuon=False,
                  normuon_beta2=0.95, muon_plus=False, plus_eps=NS_EPS, cautious=0,
                  adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8, max_grad_norm=None,
-                 state_dtype=torch.float32, param_sr=False):
+                 state_dtype=torch.float32, param_sr=False, normuon_eps=1e-10):
         self.muon = [e if isinstance(e, MuonGroupEntry) else MuonGroupEntry(**e) for e in muon_params]
         self.adam = [e if isinstance(e, AdamGroupEntry) else AdamGroupEntry(**e) for e in adamw_params]
         self.hp = make_hparams(lr, momentum, nesterov, eps, ns_steps, coeffs, normuon,
-                               normuon_beta2, muon_plus, plus_eps, cautious)
+                               normuon_beta2, muon_plus, plus_eps, cautious,
+                               normuon_eps=normuon_eps)
         self.adam_lr, self.adam_betas, self.adam_eps = adam_lr, adam_betas, adam_eps
         self.step_count = 0
         # dew.training.optim "bf16_moments": bf16 state is kept stochastically

@@ -10,7 +10,8 @@ something other than itself: closed forms, the SVD of the input, invariances
 the iteration must respect, brute force on tiny inputs, and PyTorch's own
 AdamW and gradient clipping in float64.
 """
-from .muon import (NS_COEFFS, NS_EPS, NS_STEPS, CAUTIOUS_OFF, CAUTIOUS_UPDATE, CAUTIOUS_WD,
+from .muon import (NS_COEFFS, NS_EPS, NS_STEPS, NORMUON_FLOOR, CAUTIOUS_OFF, CAUTIOUS_UPDATE,
+                   CAUTIOUS_WD,
                    MuonHparams, momentum_nesterov, muon_apply, muon_plus_row_col,
                    muon_step_tensor, muon_step_view, newton_schulz, normuon, shape_scale)
 from .adamw import adamw_step
@@ -21,7 +22,8 @@ from .stochastic_round import (MOMENT_FIRST, MOMENT_PARAM, MOMENT_SECOND, round_
                                fmix32, sr_key, sr_noise16, sr_stream, stochastic_round_bf16)
 
 __all__ = [
-    "NS_COEFFS", "NS_EPS", "NS_STEPS", "CAUTIOUS_OFF", "CAUTIOUS_UPDATE", "CAUTIOUS_WD",
+    "NS_COEFFS", "NS_EPS", "NS_STEPS", "NORMUON_FLOOR", "CAUTIOUS_OFF", "CAUTIOUS_UPDATE",
+    "CAUTIOUS_WD",
     "MuonHparams", "momentum_nesterov", "muon_apply", "muon_plus_row_col", "muon_step_tensor",
     "muon_step_view", "newton_schulz", "normuon", "shape_scale", "adamw_step", "round_bf16",
     "CLIP_EPS", "GradControl", "grad_control", "MOMENT_FIRST", "MOMENT_PARAM", "MOMENT_SECOND",

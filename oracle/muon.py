@@ -24,8 +24,10 @@ the design notes):
   * The shape scale uses the stored view's rows/cols: max(1, rows/cols)**0.5.
   * NorMuon [FLX step 3]: statistics per row of the stored view (mean over
     columns); state zero-initialised, no bias correction; the per-row factor
-    is rsqrt(max(sm, 1e-10)) and "normalize" restores the Frobenius norm the
-    update had before the per-row rescale (guarded by 1e-10).
+    is rsqrt(max(sm, normuon_eps)) (normuon_eps = 1e-10 unless the caller
+    sets it) and "normalize" restores the Frobenius norm the update had before
+    the per-row rescale (the norm ratio's denominator floored at 1e-10 only
+    against division by zero).
   * Muon+ row_col [SPD]: rows to unit L2 norm, then columns, each with eps
     inside the square root; eps defaults to the NS eps (1e-7).
   * Order when several are on: NS -> NorMuon -> Muon+ -> apply.
@@ -65,6 +67,7 @@ class MuonHparams:
     muon_plus: bool = False
     plus_eps: float = NS_EPS
     cautious: int = CAUTIOUS_OFF
+    normuon_eps: float = NORMUON_FLOOR
 
 
 def momentum_nesterov(B: np.ndarray, G: np.ndarray, mu: float, nesterov: bool = True):
@@ -119,17 +122,17 @@ def newton_schulz(Q: np.ndarray, steps: int = NS_STEPS, coeffs=NS_COEFFS,
     return X.T.copy() if tall else X
 
 
-def normuon(U: np.ndarray, sm: np.ndarray, beta2: float):
+def normuon(U: np.ndarray, sm: np.ndarray, beta2: float, eps: float = NORMUON_FLOOR):
     """[FLX step 3] NorMuon per-row second moment (reading: rows of the stored view).
 
     v_i = mean_j U_ij^2; sm <- lerp(sm, v, 1 - beta2); each row is scaled by
-    rsqrt(max(sm_i, 1e-10)); then the whole matrix is rescaled so that its
-    Frobenius norm equals the norm U had before the per-row scaling.
-    Returns (U_new, sm_new).
+    rsqrt(max(sm_i, eps)); then the whole matrix is rescaled so that its
+    Frobenius norm equals the norm U had before the per-row scaling (the
+    ratio's denominator floored at 1e-10). Returns (U_new, sm_new).
     """
     v = np.mean(U * U, axis=1)
     sm_new = sm + (1.0 - beta2) * (v - sm)
-    row_scale = 1.0 / np.sqrt(np.maximum(sm_new, NORMUON_FLOOR))
+    row_scale = 1.0 / np.sqrt(np.maximum(sm_new, eps))
     U1 = U * row_scale[:, None]
     norm_before = np.sqrt(np.sum(U * U))
     norm_after = np.sqrt(np.sum(U1 * U1))
@@ -205,7 +208,7 @@ def muon_step_view(W, G, B, hp: MuonHparams, lr_mult: float = 1.0, wd: float = 0
     sm_new = None
     if hp.normuon:
         U, sm_new = normuon(U, np.zeros(W.shape[0]) if sm is None else np.asarray(sm, np.float64),
-                            hp.beta2)
+                            hp.beta2, hp.normuon_eps)
     if hp.muon_plus:
         U = muon_plus_row_col(U, hp.plus_eps)
     lr = hp.lr * lr_mult

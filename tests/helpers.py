@@ -29,7 +29,8 @@ def oracle_hparams(wl: W.Workload) -> oracle.MuonHparams:
                               normuon=hp.get("normuon", False), beta2=hp.get("beta2", 0.95),
                               muon_plus=hp.get("muon_plus", False),
                               plus_eps=hp.get("plus_eps", hp["eps"]),
-                              cautious=hp.get("cautious", 0))
+                              cautious=hp.get("cautious", 0),
+                              normuon_eps=hp.get("normuon_eps", oracle.NORMUON_FLOOR))
 
 
 def oracle_muon_tensor(wl: W.Workload, i: int, steps: int, views=None, keep_unrounded=False):
@@ -96,7 +97,8 @@ class GpuRun:
                                   normuon=hp.get("normuon", False), beta2=hp.get("beta2", 0.95),
                                   muon_plus=hp.get("muon_plus", False),
                                   plus_eps=hp.get("plus_eps", hp["eps"]),
-                                  cautious=hp.get("cautious", 0))
+                                  cautious=hp.get("cautious", 0),
+                                  normuon_eps=hp.get("normuon_eps", oracle.NORMUON_FLOOR))
         self.mW = [W.device_tensor(wl, W.KIND_W, i, device=device) for i in range(len(wl.muon))]
         self.mG = [W.device_tensor(wl, W.KIND_G, i, 0, device=device) for i in range(len(wl.muon))]
         self.mB = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.muon]

@@ -53,10 +53,11 @@ def test_struct_layout_matches_header(tmp_path):
         " offsetof(mh_muon_tensor, views), offsetof(mh_muon_hparams, cautious),"
         " offsetof(mh_adamw_tensor, numel), offsetof(mh_muon_hparams, grad_mult),"
         " offsetof(mh_muon_hparams, skip), sizeof(mh_grad_ref), sizeof(mh_grad_control),"
-        " offsetof(mh_grad_control, step)); printf(\"%zu %zu %zu %zu %zu %zu\\n\","
+        " offsetof(mh_grad_control, step)); printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\","
         " offsetof(mh_muon_hparams, sr_seed), offsetof(mh_muon_hparams, coeff_schedule),"
         " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, skip_zero_grad),"
-        " offsetof(mh_muon_hparams, param_fence), offsetof(mh_muon_hparams, phase));"
+        " offsetof(mh_muon_hparams, param_fence), offsetof(mh_muon_hparams, phase),"
+        " offsetof(mh_muon_hparams, normuon_eps));"
         " return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -71,7 +72,8 @@ def test_struct_layout_matches_header(tmp_path):
             ctypes.sizeof(mh.GradControl), mh.GradControl.step.offset,
             mh.MuonHparams.sr_seed.offset, mh.MuonHparams.coeff_schedule.offset,
             mh.MuonHparams.norm_scale.offset, mh.MuonTensor.skip_zero_grad.offset,
-            mh.MuonHparams.param_fence.offset, mh.MuonHparams.phase.offset]
+            mh.MuonHparams.param_fence.offset, mh.MuonHparams.phase.offset,
+            mh.MuonHparams.normuon_eps.offset]
     assert got == want
 
 
@@ -111,7 +113,8 @@ def test_muon_rejects_bad_tensor(kw, code):
                                 dict(ns_steps=2, coeffs=[(1.0, 0.0, 0.0), (float("nan"), 0, 0)]),
                                 dict(ns_steps=17), dict(ns_steps=-1), dict(cautious=3),
                                 dict(coeffs=(float("inf"), 0, 0)),
-                                dict(normuon=True, beta2=1.0)])
+                                dict(normuon=True, beta2=1.0),
+                                dict(normuon_eps=-1.0), dict(normuon_eps=float("inf"))])
 def test_muon_rejects_bad_hparams(kw):
     assert _step([_tensor()], hp=mh.make_hparams(**kw)) == _lib.MH_EINVAL
 

@@ -117,6 +117,31 @@ def test_normuon_state_is_lerp():
     np.testing.assert_allclose(sm_new, 0.9 * sm + 0.1 * v, rtol=1e-14)
 
 
+def test_normuon_floor_above_every_moment_is_the_identity():
+    # With the floor above every row's second moment all rows get the same
+    # factor 1/sqrt(eps), and restoring the Frobenius norm undoes it exactly.
+    U = _n(3, 6, (7, 11)) * np.linspace(0.2, 4.0, 7)[:, None]
+    out, sm_new = oracle.normuon(U, np.zeros(7), 0.95, eps=1e6)
+    np.testing.assert_allclose(out, U, rtol=1e-13)
+    np.testing.assert_allclose(sm_new, 0.05 * np.mean(U * U, axis=1), rtol=1e-14)
+
+
+def test_normuon_floor_clamps_only_the_small_rows():
+    # Rows whose moment is under the floor keep their relative size; rows above
+    # it are equalised. Row 0 is tiny (moment 1e-8), rows 1.. are O(1).
+    U = _n(3, 7, (5, 40))
+    U[0] *= 1e-4
+    eps = 1e-4
+    out, sm_new = oracle.normuon(U, np.zeros(5), 0.0, eps=eps)
+    f = 1.0 / np.sqrt(np.maximum(sm_new, eps))
+    assert f[0] == pytest.approx(1.0 / np.sqrt(eps))
+    U1 = U * f[:, None]
+    kappa = np.linalg.norm(U) / np.linalg.norm(U1)
+    np.testing.assert_allclose(out, kappa * U1, rtol=1e-13)
+    big = np.linalg.norm(out[1:], axis=1)
+    np.testing.assert_allclose(big, big[0], rtol=1e-12)
+
+
 def test_normuon_zero_update_stays_zero():
     out, sm_new = oracle.normuon(np.zeros((3, 5)), np.zeros(3), 0.95)
     assert np.all(out == 0) and np.all(np.isfinite(out)) and np.all(sm_new == 0)
