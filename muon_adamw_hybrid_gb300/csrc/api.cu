@@ -37,6 +37,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "mh_internal.h"
 #include "mh_sr.cuh"
 #include "muonhybrid.h"
@@ -322,11 +324,15 @@ cudaEvent_t prof_event(Profiler& P) {
 }
 
 // Brackets one launch with events on its stream when profiling is on.
+// Around each launch: an NVTX range named after the stage (for nsys / ncu
+// --nvtx filtering; a no-op unless a tool is attached) and, while the
+// profiler is on, a pair of CUDA events on the launch stream.
 class ProfScope {
  public:
   ProfScope(cudaStream_t s, const char* name, double bytes, double flops = 0.0,
             double flops_exec = 0.0)
       : s_(s) {
+    nvtxRangePushA(name);
     Profiler& P = profiler();
     std::lock_guard<std::mutex> lock(P.mu);
     if (!P.on) return;
@@ -340,6 +346,7 @@ class ProfScope {
     active_ = cudaEventRecord(rec_.begin, s_) == cudaSuccess;
   }
   ~ProfScope() {
+    nvtxRangePop();
     if (!active_) return;
     Profiler& P = profiler();
     std::lock_guard<std::mutex> lock(P.mu);
