@@ -277,12 +277,16 @@ class DeviceWorkload:
         if self.control is not None:
             self.grefs_host = [mh.grad_ref(g) for g in list(muon_host) + list(adam_host)]
 
-    def step(self, stream, host_grads: bool = False, param_fence=None, between=None) -> None:
+    def step(self, stream, host_grads: bool = False, param_fence=None, between=None,
+             adam_grads=None) -> None:
         """One step on `stream`. `param_fence` (a torch.cuda.Event) holds back
         the step's first parameter write until the event has completed.
         `between`: the Muon step is split into its gradient phase and the rest,
         and between() is called in between; it may enqueue work that follows
-        the last gradient read and return an event to use as the fence."""
+        the last gradient read and return an event to use as the fence.
+        `adam_grads`: called before AdamW; an event it returns means the AdamW
+        gradients have been copied into the device buffers, which AdamW then
+        reads (after waiting for the event) instead of the host ones."""
         s = stream.cuda_stream
         ts = self.ts_host if host_grads else self.ts
         at = self.at_host if host_grads else self.at
@@ -302,7 +306,7 @@ class DeviceWorkload:
             self.mh.muon_step_batched(ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
             self.hp.phase = self.mh.MH_STEP_ALL
             self.hp.param_fence = None
-            self._adamw(at, s)
+            self._adamw(self._adam_structs(at, stream, adam_grads), s)
             return
         if between is not None:            # no Muon tensors: the fence goes before AdamW
             param_fence = between()
@@ -316,7 +320,14 @@ class DeviceWorkload:
         if ts:
             self.mh.muon_step_batched(ts, self.hp, self.ws.data_ptr(), self.ws.numel(), s)
             self.hp.param_fence = None
-        self._adamw(at, s)
+        self._adamw(self._adam_structs(at, stream, adam_grads), s)
+
+    def _adam_structs(self, at, stream, adam_grads):
+        ready = adam_grads() if adam_grads is not None else None
+        if ready is None:
+            return at
+        stream.wait_event(ready)
+        return self.at
 
     def _adamw(self, at, s) -> None:
         if at:
@@ -389,6 +400,98 @@ class PinnedMirror:
     def close(self):
         self.host = []
         self.buf = None
+
+
+class HostPipeline:
+    """The end-to-end step through pinned host buffers, as a user overlapping
+    transfers with compute would run it.
+
+    Each step reads this step's gradients from page-locked host memory: in
+    place (on a GPU that maps that memory, the kernels read it over the host
+    link) or through explicit copies otherwise. It also copies the previous
+    step's parameters back to the host. The copy-out starts when this step's
+    gradient phase has read the Muon gradients, so the two do not compete for
+    host memory bandwidth. It runs on a second stream beside the
+    Newton-Schulz stages, and this step's first parameter write waits for it
+    (param_fence). With in-place reads the AdamW gradients are copied into
+    the device buffers at the same point, on a third stream, and AdamW reads
+    them there. finish() copies out the last step's parameters."""
+
+    def __init__(self, dw):
+        import torch
+        self.dw, self.torch = dw, torch
+        self.gin = PinnedMirror(dw.mG + dw.aG)
+        self.pout = PinnedMirror(dw.mW + dw.aW)
+        self.gin.fill_from_device()
+        torch.cuda.synchronize()
+        mh = dw.mh
+        self.in_place = all(mh.pointer_device_accessible(h.data_ptr()) for h in self.gin.host)
+        self.nm = len(dw.mG)
+        if self.in_place:
+            dw.use_host_grads(self.gin.host[:self.nm], self.gin.host[self.nm:])
+        self.copy_stream = torch.cuda.Stream()
+        self.h2d_stream = torch.cuda.Stream()
+        self.pending = False
+        self.timed = False
+        self.copies = []       # (start, end) events of the timed copy-outs
+        self.last_copy = None
+        self._adam_ready = None
+
+    def _after(self, stream, side):
+        ready = self.torch.cuda.Event()
+        ready.record(stream)
+        side.wait_event(ready)
+
+    def copy_out(self, stream):
+        torch = self.torch
+        self._after(stream, self.copy_stream)
+        with torch.cuda.stream(self.copy_stream):
+            c0 = torch.cuda.Event(enable_timing=True)
+            c0.record(self.copy_stream)
+            self.pout.d2h()
+            landed = torch.cuda.Event(enable_timing=True)
+            landed.record(self.copy_stream)
+        if self.timed:
+            self.copies.append((c0, landed))
+        self.pending = False
+        self.last_copy = landed
+        return landed
+
+    def _fetch_adam_grads(self, stream):
+        torch, dw = self.torch, self.dw
+        self._after(stream, self.h2d_stream)
+        with torch.cuda.stream(self.h2d_stream):
+            for h, t in zip(self.gin.host[self.nm:], dw.aG):
+                t.copy_(h, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(self.h2d_stream)
+        return ready
+
+    def step(self, stream) -> None:
+        dw = self.dw
+        if not self.in_place:
+            self.gin.h2d()
+
+        def between():
+            fence = self.copy_out(stream) if self.pending else None
+            self._adam_ready = (self._fetch_adam_grads(stream)
+                                if self.in_place and dw.aG else None)
+            return fence
+        self._adam_ready = None
+        dw.step(stream, host_grads=self.in_place, between=between,
+                adam_grads=lambda: self._adam_ready)
+        self.pending = True
+
+    def finish(self, stream):
+        landed = self.copy_out(stream)
+        stream.wait_event(landed)
+        return landed
+
+    def close(self):
+        if self.in_place:
+            self.dw.ts_host = self.dw.at_host = None
+        self.gin.close()
+        self.pout.close()
 
 
 # ---- oracle (CPU baseline / reference arm) ------------------------------------------------
@@ -831,93 +934,42 @@ def main():
     # ---- end to end with host buffers --------------------------------------------------
     e2e = None
     if not args.no_e2e:
-        grads = dw.mG + dw.aG
-        params = dw.mW + dw.aW
-        gin = PinnedMirror(grads)
-        pout = PinnedMirror(params)
-        gin.fill_from_device()
-        torch.cuda.synchronize()
-        # On a GPU that reads page-locked host memory in place (NVLink-C2C on
-        # Grace-Blackwell) the kernels stream this step's gradients straight
-        # from the host buffer: the transfer happens inside the prologue and
-        # AdamW instead of as a separate copy. Otherwise: explicit copies.
-        in_place = all(mh.pointer_device_accessible(h.data_ptr()) for h in gin.host)
-        if in_place:
-            nm = len(dw.mG)
-            dw.use_host_grads(gin.host[:nm], gin.host[nm:])
-
-        # Step k's parameters are copied out on a second stream while step k+1
-        # runs its Newton-Schulz stages: the copy starts once step k+1's
-        # gradient phase has read the gradients (so the two do not share the
-        # host memory's bandwidth) and step k+1's first parameter write waits
-        # for it (param_fence). The timed region ends when the last step's
-        # parameters have landed.
-        copy_stream = torch.cuda.Stream()
-        copies = []          # (start, end) events of each timed copy
-        pending = [False]    # a finished step's parameters are not yet copied
-
-        def copy_out(timed):
-            ready = torch.cuda.Event()
-            ready.record(stream)
-            copy_stream.wait_event(ready)
-            with torch.cuda.stream(copy_stream):
-                c0 = torch.cuda.Event(enable_timing=True)
-                c0.record(copy_stream)
-                pout.d2h()
-                landed = torch.cuda.Event(enable_timing=True)
-                landed.record(copy_stream)
-            if timed:
-                copies.append((c0, landed))
-            pending[0] = False
-            return landed
-
-        def one_step(k):
-            if k is not None:
-                ev[k][0].record(stream)
-            if not in_place:
-                gin.h2d()
-            if k is not None:
-                ev[k][1].record(stream)
-            dw.step(stream, host_grads=in_place,
-                    between=lambda: copy_out(k is not None) if pending[0] else None)
-            if k is not None:
-                ev[k][2].record(stream)
-            pending[0] = True
-
-        one_step(None)
-        stream.wait_event(copy_out(False))
+        pipe = HostPipeline(dw)
+        in_place = pipe.in_place
+        gin, pout = pipe.gin, pipe.pout
+        pipe.step(stream)                   # warm-up step and its copy-out
+        pipe.finish(stream)
         torch.cuda.synchronize()
         barrier(world)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        pipe.timed = True
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         for k in range(args.steps):
-            one_step(k)
+            ev[k][0].record(stream)
+            pipe.step(stream)
+            ev[k][1].record(stream)
         end = torch.cuda.Event(enable_timing=True)
-        stream.wait_event(copy_out(True))
+        pipe.finish(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(ev[0][0].elapsed_time(end) / args.steps, world)
-        h2d_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-        step_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-        d2h_ms = statistics.mean(c[0].elapsed_time(c[1]) for c in copies)
+        step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        d2h_ms = statistics.mean(c[0].elapsed_time(c[1]) for c in pipe.copies)
         e2e = {"value": round(e2e_ms, 3), "unit": "ms/step", "h2d_bytes_per_step": gin.nbytes,
-               "d2h_bytes_per_step": pout.nbytes, "h2d_ms": round(h2d_ms, 2),
+               "d2h_bytes_per_step": pout.nbytes,
                "step_ms": round(step_ms, 2), "d2h_ms": round(d2h_ms, 2),
-               "path": ("C ABI calls whose kernels read this step's gradients in place from "
-                        "page-locked host memory over the host link; updated parameters copied "
-                        "back each step on a second stream, from the end of the next step's "
-                        "gradient phase up to its first parameter write (MH_STEP_GRADIENTS / "
-                        "MH_STEP_FINISH, param_fence)") if in_place else
+               "path": ("C ABI calls whose kernels read this step's Muon gradients in place "
+                        "from page-locked host memory over the host link; the AdamW gradients "
+                        "copied in and the previous step's parameters copied out on two more "
+                        "streams from the end of the gradient phase, beside the Newton-Schulz "
+                        "stages (MH_STEP_GRADIENTS / MH_STEP_FINISH, param_fence)") if in_place else
                        ("C ABI calls with gradients copied in from pinned host memory and "
                         "updated parameters copied back each step on a second stream, from the "
                         "end of the next step's gradient phase up to its first parameter write "
                         "(MH_STEP_GRADIENTS / MH_STEP_FINISH, param_fence)"),
                "h2d_in_kernel": in_place,
                "pinned": bool(gin.registered and pout.registered)}
-        if in_place:
-            dw.ts_host = dw.at_host = None
-        gin.close()
-        pout.close()
+        pipe.close()
 
     # ---- CPU oracle baseline (rank 0, one GPU) -------------------------------------------
     cpu = None
