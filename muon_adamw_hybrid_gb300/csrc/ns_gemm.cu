@@ -5,9 +5,10 @@
 // One quintic step (Speedtronic "v2 optimizers", "Newton-Schulz"; flaxchat
 // "Optimizer", "Muon Algorithm" step 2) is three launches of this kernel:
 //
-//   GEMM_GRAM   A = X X^T             (m x m; only tiles touching the upper
-//                                      triangle are computed, each element
-//                                      c >= r is stored and mirrored to (c, r))
+//   GEMM_GRAM   A = X X^T             (m x m; only the upper block triangle is
+//                                      computed: a 32 x 32 chunk above the
+//                                      diagonal is stored and mirrored, one on
+//                                      it stored whole)
 //   GEMM_POLY   P = b A + c A A       (A symmetric, so A A = A A^T: both
 //                                      operands are K-major rows of A; same
 //                                      triangle scheme; b A read in the epilogue)
@@ -32,10 +33,12 @@
 //
 // Warp roles per CTA: warp 0 issues TMA loads into a 4-stage ring, warp 1
 // issues tcgen05.mma into one of two TMEM accumulators, warp 2 owns the TMEM
-// allocation, warps 4-7 drain an accumulator with tcgen05.ld, apply the
-// stage's epilogue in fp32 and store bf16 while the MMA warp fills the other
-// accumulator. Mirrored halves of the symmetric outputs are transposed in
-// shared memory so that they are written as 64-byte row segments.
+// allocation, warps 4-7 drain an accumulator with tcgen05.ld (one row per
+// lane, 32 columns at a time), apply the stage's epilogue in fp32 and, while
+// the MMA warp fills the other accumulator, write each bf16 chunk (and its
+// transpose, for the mirrored half of a symmetric output) into swizzled
+// shared-memory boxes that one lane stores with TMA. The fused parameter
+// update of the last apply stage reads and writes the parameters directly.
 //
 // Every mbarrier wait is bounded; on timeout the CTA records a status code in
 // the workspace, raises the abort flag of both CTAs of its pair, drains what
