@@ -85,7 +85,7 @@ struct TensorInfo {
   int64_t class_slot = 0;  // slot of the first view within its class
   int64_t view_slot = 0;   // global view index (sumsq)
   int64_t tile_off = 0;    // first prologue tile (tile_ss index)
-  int64_t tiles_r = 0, tiles_c = 0;  // 32 x 128 tiles of the statistics/apply passes
+  int64_t tiles_r = 0, tiles_c = 0;  // 32 x 256 tiles of the statistics/apply passes
   int64_t ptiles_c = 0;              // 32 x 256 tiles of the prologue
   bool flat = false;                 // prologue streams the view as contiguous chunks
   int64_t pro_tiles_per_view = 0;    // prologue work items per view
