@@ -467,6 +467,99 @@ class HostPipeline:
             ready.record(self.h2d_stream)
         return ready
 
+    def plan_groups(self, tflops: float = 2.0e3, link_gbs: float = 190.0):
+        """Splits the Muon tensors in two for the grouped step: group A (most
+        Newton-Schulz work per gradient byte first) reads its gradients in
+        place; its Newton-Schulz stages must last long enough to cover the
+        copy-in of every other gradient (group B and AdamW) at `link_gbs`."""
+        wl, dw = self.dw.wl, self.dw
+        items = []
+        for i, spec in enumerate(wl.muon):
+            m, n = min(spec.rows, spec.cols), max(spec.rows, spec.cols)
+            flops = spec.views * wl.muon_hp["ns_steps"] * (4.0 * m * m * n + 2.0 * m ** 3)
+            gbytes = dw.mG[i].numel() * dw.mG[i].element_size()
+            items.append((gbytes / max(flops, 1.0), i, flops, gbytes))
+        items.sort()
+        rest = sum(g.numel() * g.element_size() for g in dw.mG + dw.aG)
+        a, fa = [], 0.0
+        for _, i, f, g in items:
+            if fa / (tflops * 1e12) >= rest / (link_gbs * 1e9):
+                break
+            a.append(i)
+            fa += f
+            rest -= g
+        b = [i for i in range(len(wl.muon)) if i not in set(a)]
+        return sorted(a), b
+
+    def _copy_tensors(self, idx, side, event_stream):
+        """D2H of the listed parameter tensors on `side` (after event_stream's
+        current work); returns the event recorded after them."""
+        torch = self.torch
+        with torch.cuda.stream(side):
+            for i in idx:
+                self.pout.host[i].copy_(self.pout.tensors[i], non_blocking=True)
+            done = torch.cuda.Event(enable_timing=True)
+            done.record(side)
+        return done
+
+    def step_grouped(self, stream, groups) -> None:
+        """One step with the Muon tensors in two groups (plan_groups): group A
+        runs its gradient phase on in-place host gradients; then the other
+        gradients are copied into device memory (h2d stream) and the previous
+        step's parameters out (copy stream, group A's first) while group A's
+        Newton-Schulz stages run; group B and AdamW then run on device
+        gradients. Each group's update is fenced on the copy-out of its own
+        parameters."""
+        torch, dw, mh = self.torch, self.dw, self.dw.mh
+        a, b = groups
+        s = stream.cuda_stream
+        dw.step_count += 1
+        dw.hp.sr_seed = dw.step_count
+        if dw.control is not None:
+            dw.mh._lib.grad_prepare(dw.grefs_host, 1.0, float(dw.max_grad_norm), dw.cstruct,
+                                    dw.gws.data_ptr(), dw.gws.numel(), s)
+        ts_a = [dw.ts_host[i] for i in a]
+        dw.hp.param_fence = None
+        dw.hp.phase = mh.MH_STEP_GRADIENTS
+        dw.mh.muon_step_batched(ts_a, dw.hp, dw.ws.data_ptr(), dw.ws.numel(), s)
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        self.h2d_stream.wait_event(ready)
+        with torch.cuda.stream(self.h2d_stream):
+            for i in b:
+                dw.mG[i].copy_(self.gin.host[i], non_blocking=True)
+            for j, t in enumerate(dw.aG):
+                t.copy_(self.gin.host[self.nm + j], non_blocking=True)
+            grads_in = torch.cuda.Event()
+            grads_in.record(self.h2d_stream)
+        fence_a = fence_rest = None
+        if self.pending:
+            self.copy_stream.wait_event(ready)
+            with torch.cuda.stream(self.copy_stream):
+                c0 = torch.cuda.Event(enable_timing=True)
+                c0.record(self.copy_stream)
+            fence_a = self._copy_tensors(a, self.copy_stream, stream)
+            fence_rest = self._copy_tensors(b + [self.nm + j for j in range(len(dw.aW))],
+                                            self.copy_stream, stream)
+            if self.timed:
+                self.copies.append((c0, fence_rest))
+            self.last_copy = fence_rest
+            self.pending = False
+        dw.hp.phase = mh.MH_STEP_FINISH
+        dw.hp.param_fence = fence_a.cuda_event if fence_a is not None else None
+        dw.mh.muon_step_batched(ts_a, dw.hp, dw.ws.data_ptr(), dw.ws.numel(), s)
+        stream.wait_event(grads_in)
+        dw.hp.phase = mh.MH_STEP_ALL
+        if b:
+            dw.hp.param_fence = fence_rest.cuda_event if fence_rest is not None else None
+            dw.mh.muon_step_batched([dw.ts[i] for i in b], dw.hp, dw.ws.data_ptr(),
+                                    dw.ws.numel(), s)
+        elif fence_rest is not None:
+            stream.wait_event(fence_rest)
+        dw.hp.param_fence = None
+        dw._adamw(dw.at, s)
+        self.pending = True
+
     def step(self, stream) -> None:
         dw = self.dw
         if not self.in_place:
@@ -937,7 +1030,15 @@ def main():
         pipe = HostPipeline(dw)
         in_place = pipe.in_place
         gin, pout = pipe.gin, pipe.pout
-        pipe.step(stream)                   # warm-up step and its copy-out
+        groups = pipe.plan_groups() if in_place and dw.ts else None
+        grouped = groups is not None and bool(groups[0]) and bool(groups[1])
+
+        def run_step():
+            if grouped:
+                pipe.step_grouped(stream, groups)
+            else:
+                pipe.step(stream)
+        run_step()                          # warm-up step and its copy-out
         pipe.finish(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -945,7 +1046,7 @@ def main():
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         for k in range(args.steps):
             ev[k][0].record(stream)
-            pipe.step(stream)
+            run_step()
             ev[k][1].record(stream)
         end = torch.cuda.Event(enable_timing=True)
         pipe.finish(stream)
@@ -968,6 +1069,7 @@ def main():
                         "end of the next step's gradient phase up to its first parameter write "
                         "(MH_STEP_GRADIENTS / MH_STEP_FINISH, param_fence)"),
                "h2d_in_kernel": in_place,
+               "muon_groups": [len(groups[0]), len(groups[1])] if grouped else None,
                "pinned": bool(gin.registered and pout.registered)}
         pipe.close()
 
