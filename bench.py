@@ -63,6 +63,10 @@ def parse_args():
                     help="run the gradient control (global norm, clip to this value, overflow "
                          "skip) ahead of both halves; 0 observes the norm only")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-groups", action="store_true",
+                    help="end to end: split the Muon tensors in two groups and copy the second "
+                         "group's gradients in while the first computes (fast only where the "
+                         "copy engines keep their rate beside the GEMMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -1030,7 +1034,12 @@ def main():
         pipe = HostPipeline(dw)
         in_place = pipe.in_place
         gin, pout = pipe.gin, pipe.pout
-        groups = pipe.plan_groups() if in_place and dw.ts else None
+        # The grouped step (--e2e-groups) copies most gradients in on the copy
+        # engines while group A computes. On some hosts those copies keep
+        # ~200 GB/s beside the GEMMs (7B end to end 359 ms against 385 ms
+        # read in place); on others they fall to ~40 GB/s under load
+        # (675-740 ms), so the in-place path is the default.
+        groups = pipe.plan_groups() if args.e2e_groups and in_place and dw.ts else None
         grouped = groups is not None and bool(groups[0]) and bool(groups[1])
 
         def run_step():
