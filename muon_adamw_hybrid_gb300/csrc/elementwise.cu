@@ -283,7 +283,12 @@ __device__ __forceinline__ float prologue_chunk_fast(const EwJob& J, const EwPar
 // kProChunk-element chunk of one view; each thread handles 8 consecutive
 // elements per step, the block 2048 per step, four steps per chunk. One
 // ||Q||_F^2 partial per warp and chunk.
-__global__ void __launch_bounds__(kEwThreads, 2) prologue_flat_kernel(const __grid_constant__ EwParams p) {
+// kB16: every job keeps bf16 momentum. Its chunks move 8 B per element
+// instead of 12, so a thread has fewer bytes in flight; the instantiation
+// carries only the bf16-momentum fast paths and runs three blocks per SM.
+template <bool kB16>
+__global__ void __launch_bounds__(kEwThreads, kB16 ? 3 : 2)
+    prologue_flat_kernel(const __grid_constant__ EwParams p) {
   __shared__ __align__(16) EwJob sJ;
   if (step_skipped(p.skip)) return;
   const float gmul = p.grad_mult != nullptr ? *p.grad_mult : 1.0f;
@@ -347,12 +352,16 @@ __global__ void __launch_bounds__(kEwThreads, 2) prologue_flat_kernel(const __gr
     if (p.use_momentum && J.src_vec && J.mom_vec && base + kProChunk <= vsz) {
       const int64_t e0 = view_elem0 + base + 8 * static_cast<int64_t>(threadIdx.x);
       bf16* xd = xv + base + 8 * static_cast<int64_t>(threadIdx.x);
-      if (J.src_dtype == MH_BF16)
+      if constexpr (kB16) {
+        ss = J.src_dtype == MH_BF16 ? prologue_chunk_fast<MH_BF16, MH_BF16>(J, p, gmul, e0, xd)
+                                    : prologue_chunk_fast<MH_F32, MH_BF16>(J, p, gmul, e0, xd);
+      } else if (J.src_dtype == MH_BF16) {
         ss = J.mom_dtype == MH_BF16 ? prologue_chunk_fast<MH_BF16, MH_BF16>(J, p, gmul, e0, xd)
                                     : prologue_chunk_fast<MH_BF16, MH_F32>(J, p, gmul, e0, xd);
-      else
+      } else {
         ss = J.mom_dtype == MH_BF16 ? prologue_chunk_fast<MH_F32, MH_BF16>(J, p, gmul, e0, xd)
                                     : prologue_chunk_fast<MH_F32, MH_F32>(J, p, gmul, e0, xd);
+      }
       ss = warp_sum(ss);
       if (lane == 0) J.tile_ss[static_cast<int64_t>(local) * (kEwThreads / 32) + warp] = ss;
       continue;
@@ -868,10 +877,18 @@ int blocks_per_sm(EwKind kind, const void* kernel) {
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
   if (kind == EW_APPLY && p.cautious == MH_CAUTIOUS_UPDATE) kind = EW_APPLY_CU;
+  if (kind == EW_PROLOGUE_FLAT && p.use_momentum) {
+    bool all_b16 = p.njobs > 0;
+    for (int j = 0; j < p.njobs; ++j) all_b16 = all_b16 && p.jobs[j].mom_dtype == MH_BF16;
+    if (all_b16) kind = EW_PROLOGUE_FLAT_B16;
+  }
   const void* fn = nullptr;
   switch (kind) {
     case EW_PROLOGUE: fn = reinterpret_cast<const void*>(prologue_kernel); break;
-    case EW_PROLOGUE_FLAT: fn = reinterpret_cast<const void*>(prologue_flat_kernel); break;
+    case EW_PROLOGUE_FLAT: fn = reinterpret_cast<const void*>(prologue_flat_kernel<false>); break;
+    case EW_PROLOGUE_FLAT_B16:
+      fn = reinterpret_cast<const void*>(prologue_flat_kernel<true>);
+      break;
     case EW_ROWSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_ROWSQ>); break;
     case EW_COLSQ: fn = reinterpret_cast<const void*>(ew_kernel<EW_COLSQ>); break;
     case EW_APPLY: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY>); break;
@@ -883,7 +900,8 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
   const int grid = static_cast<int>(p.total_tiles < want ? p.total_tiles : want);
   switch (kind) {
     case EW_PROLOGUE: prologue_kernel<<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_PROLOGUE_FLAT: prologue_flat_kernel<<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_PROLOGUE_FLAT: prologue_flat_kernel<false><<<grid, kEwThreads, 0, s>>>(p); break;
+    case EW_PROLOGUE_FLAT_B16: prologue_flat_kernel<true><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(p); break;
     case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;

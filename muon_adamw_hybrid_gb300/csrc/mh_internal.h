@@ -108,10 +108,12 @@ enum EwKind {
   EW_APPLY = 3,
   EW_COPYOUT = 4,
   EW_PROLOGUE_FLAT = 5,  // contiguous chunks (wide views with cols % 8 == 0)
-  EW_APPLY_CU = 6        // EW_APPLY with the cautious-update mask (reads the gradient);
+  EW_APPLY_CU = 6,       // EW_APPLY with the cautious-update mask (reads the gradient);
                          // chosen by launch_elementwise, never planned on its own
+  EW_PROLOGUE_FLAT_B16 = 7  // EW_PROLOGUE_FLAT when every job keeps bf16 momentum: a leaner
+                            // instantiation at three blocks per SM; chosen by launch_elementwise
 };
-constexpr int kEwKinds = 7;
+constexpr int kEwKinds = 8;
 
 // Row finalisation (NorMuon state, NorMuon norm restore, Muon+ row factor):
 // one CTA per view. Every reduction sums per-tile partials in a fixed order,
