@@ -186,18 +186,23 @@ __device__ __forceinline__ void adam_chunk_fast(const AdamJob& J, int64_t start,
   }
 }
 
-template <int PDT, int GDT>
+template <bool kB16, int PDT, int GDT>
 __device__ __forceinline__ void adam_chunk_fast_s(const AdamJob& J, int64_t start, float gmul,
                                                   float lr, float decay, const AdamConsts& k,
                                                   bool psr, uint32_t kp, uint32_t km,
                                                   uint32_t kv) {
-  if (J.sdt == MH_BF16)
+  if (kB16 || J.sdt == MH_BF16)
     adam_chunk_fast<PDT, GDT, MH_BF16>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
   else
     adam_chunk_fast<PDT, GDT, MH_F32>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
 }
 
-__global__ void __launch_bounds__(256, 2) adamw_kernel(const __grid_constant__ AdamParams p) {
+// kB16: every job keeps bf16 moments. That path is bound by the rounding
+// arithmetic rather than by bytes in flight; the instantiation carries only
+// its fast paths and runs three blocks per SM to hide more of it.
+template <bool kB16>
+__global__ void __launch_bounds__(256, kB16 ? 3 : 2)
+    adamw_kernel(const __grid_constant__ AdamParams p) {
   __shared__ float s_bc[2];
   __shared__ uint64_t s_seed;
   if (step_skipped(p.skip)) return;
@@ -246,13 +251,13 @@ __global__ void __launch_bounds__(256, 2) adamw_kernel(const __grid_constant__ A
     const uint32_t kp = psr ? sr_key(seed, sr_stream(J.tindex, SR_PARAM)) : 0;
     if (J.vec && end - start == kAdamChunk) {
       if (J.pdt == MH_BF16 && J.gdt == MH_BF16)
-        adam_chunk_fast_s<MH_BF16, MH_BF16>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
+        adam_chunk_fast_s<kB16, MH_BF16, MH_BF16>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
       else if (J.pdt == MH_BF16)
-        adam_chunk_fast_s<MH_BF16, MH_F32>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
+        adam_chunk_fast_s<kB16, MH_BF16, MH_F32>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
       else if (J.gdt == MH_BF16)
-        adam_chunk_fast_s<MH_F32, MH_BF16>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
+        adam_chunk_fast_s<kB16, MH_F32, MH_BF16>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
       else
-        adam_chunk_fast_s<MH_F32, MH_F32>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
+        adam_chunk_fast_s<kB16, MH_F32, MH_F32>(J, start, gmul, lr, decay, k, psr, kp, km, kv);
     } else if (J.vec) {
       for (int64_t i = start + 8 * static_cast<int64_t>(threadIdx.x); i < end; i += 8 * 256) {
         if (i + 8 <= end) {
@@ -283,9 +288,16 @@ __global__ void __launch_bounds__(256, 2) adamw_kernel(const __grid_constant__ A
 
 cudaError_t launch_adamw(const AdamParams& p, int num_sms, cudaStream_t s) {
   if (p.total_chunks <= 0) return cudaSuccess;
-  const int64_t want = static_cast<int64_t>(num_sms) * 2;  // resident blocks (108 registers)
+  bool all_b16 = p.njobs > 0;
+  for (int j = 0; j < p.njobs; ++j) all_b16 = all_b16 && p.jobs[j].sdt == MH_BF16;
+  // One wave of resident blocks: two per SM (108 registers), three for the
+  // bf16-moment instantiation.
+  const int64_t want = static_cast<int64_t>(num_sms) * (all_b16 ? 3 : 2);
   const int grid = static_cast<int>(p.total_chunks < want ? p.total_chunks : want);
-  adamw_kernel<<<grid, 256, 0, s>>>(p);
+  if (all_b16)
+    adamw_kernel<true><<<grid, 256, 0, s>>>(p);
+  else
+    adamw_kernel<false><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
