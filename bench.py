@@ -495,9 +495,10 @@ class HostPipeline:
         b = [i for i in range(len(wl.muon)) if i not in set(a)]
         return sorted(a), b
 
-    def _copy_tensors(self, idx, side, event_stream):
-        """D2H of the listed parameter tensors on `side` (after event_stream's
-        current work); returns the event recorded after them."""
+    def _copy_tensors(self, idx, side):
+        """D2H of the listed parameter tensors on the `side` stream (ordered
+        after whatever that stream already waits for); returns the event
+        recorded after them."""
         torch = self.torch
         with torch.cuda.stream(side):
             for i in idx:
@@ -542,9 +543,9 @@ class HostPipeline:
             with torch.cuda.stream(self.copy_stream):
                 c0 = torch.cuda.Event(enable_timing=True)
                 c0.record(self.copy_stream)
-            fence_a = self._copy_tensors(a, self.copy_stream, stream)
+            fence_a = self._copy_tensors(a, self.copy_stream)
             fence_rest = self._copy_tensors(b + [self.nm + j for j in range(len(dw.aW))],
-                                            self.copy_stream, stream)
+                                            self.copy_stream)
             if self.timed:
                 self.copies.append((c0, fence_rest))
             self.last_copy = fence_rest
