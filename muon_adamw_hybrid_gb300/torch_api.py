@@ -6,7 +6,7 @@ optimizer runs in libmuonhybrid's kernels.
 from __future__ import annotations
 
 import ctypes
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 import torch
 

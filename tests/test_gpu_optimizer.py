@@ -1,9 +1,7 @@
 """The torch-facing optimizer facade and checkpoint continuation."""
-import numpy as np
 import pytest
 
 import synth
-from tests.helpers import rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 

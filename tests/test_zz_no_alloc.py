@@ -11,7 +11,6 @@ call left in the shared array cannot leak into the second.
 
 This file is named to be collected last.
 """
-import ctypes
 
 import numpy as np
 import pytest
