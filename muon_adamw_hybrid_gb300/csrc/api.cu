@@ -527,12 +527,14 @@ double ew_bytes(EwKind kind, const EwParams& p, const EwJob& J) {
   switch (kind) {
     case EW_PROLOGUE:
     case EW_PROLOGUE_FLAT:
+    case EW_PROLOGUE_FLAT_B16:
       return e * (dsize(J.src_dtype) + (p.use_momentum ? 2.0 * dsize(J.mom_dtype) : 0.0) + 2.0);
     case EW_ROWSQ:
       return e * 2.0;
     case EW_COLSQ:
       return e * 2.0;
     case EW_APPLY:
+    case EW_APPLY_CU:
       return e * (2.0 + 2.0 * dsize(J.dst_dtype) +
                   (p.cautious == MH_CAUTIOUS_UPDATE ? dsize(J.src_dtype) : 0.0));
     case EW_COPYOUT:
@@ -544,10 +546,12 @@ double ew_bytes(EwKind kind, const EwParams& p, const EwJob& J) {
 const char* ew_name(EwKind kind, bool muon) {
   switch (kind) {
     case EW_PROLOGUE:
-    case EW_PROLOGUE_FLAT: return muon ? "muon_prologue" : "ns_prologue";
+    case EW_PROLOGUE_FLAT:
+    case EW_PROLOGUE_FLAT_B16: return muon ? "muon_prologue" : "ns_prologue";
     case EW_ROWSQ: return "muon_rowstats";
     case EW_COLSQ: return "muon_colstats";
-    case EW_APPLY: return "muon_apply";
+    case EW_APPLY:
+    case EW_APPLY_CU: return "muon_apply";
     case EW_COPYOUT: return "ns_copyout";
   }
   return "elementwise";
