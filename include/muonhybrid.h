@@ -8,10 +8,12 @@
  *   "Muon+", "Cautious updates"; flaxchat "Optimizer", "Muon Algorithm";
  *   kimi-k3 "Optimization", "A tensor's storage shape can be misleading"):
  *
- *       B <- mu*B + (1-mu)*G                       momentum, fp32 state
+ *       B <- mu*B + (1-mu)*G                       momentum (fp32, or bf16 rounded
+ *                                                  stochastically)
  *       Q <- lerp(G, B, mu) = G + mu*(B - G)        Nesterov form (else Q = B)
- *       X <- T / (||T||_F + eps),  T = Q^T if rows > cols else Q
+ *       X <- T / (||T||_F * norm_scale + eps),  T = Q^T if rows > cols else Q
  *       repeat ns_steps:  A = X X^T;  X <- a X + (b A + c A^2) X
+ *                         (one (a, b, c) for every iteration, or a schedule)
  *       U <- X^T if rows > cols else X
  *       [NorMuon per-row second moment]  [Muon+ row_col]
  *       W <- (1 - lr*wd) W - lr * max(1, rows/cols)^0.5 * U   (or a cautious form)
@@ -264,7 +266,8 @@ typedef struct {
  * correction):
  *   m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2
  *   W <- W (1 - lr*wd) - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
- * in fp32, bf16 parameters rounded to nearest even on store. */
+ * in fp32; bf16 parameters are rounded to nearest even on store, or
+ * stochastically with param_sr, and bf16 moments stochastically (above). */
 int mh_adamw_step(const mh_adamw_tensor* tensors, int32_t n, float lr, float beta1, float beta2,
                   float eps, int64_t step, void* stream);
 
@@ -357,7 +360,9 @@ int mh_qk_clip(const mh_qk_clip_entry* entries, int32_t n, const float* s_max, f
  * plus the FLOPs the tensor cores actually execute (fewer, since only the
  * upper triangle of the symmetric products is computed). Events are host
  * objects created on first use; no device memory is allocated. Disabled by
- * default; when disabled the calls above record nothing. */
+ * default; when disabled the calls above record nothing. Independently of
+ * it, every launch sits inside an NVTX range named after its stage
+ * (e.g. "ns_gemm.gram"), a no-op unless a profiling tool is attached. */
 typedef struct {
   char name[32];          /* kernel family, e.g. "ns_gemm", "muon_prologue" */
   int64_t launches;       /* launches recorded since the last reset */
