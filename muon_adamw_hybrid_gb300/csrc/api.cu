@@ -370,7 +370,7 @@ class ProfScope {
 int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, float eps, int sms,
            cudaStream_t stream, int* final_buf, bool final_update = false, int cautious = 0,
            const int32_t* skip = nullptr, const float* sched = nullptr,
-           float norm_scale = 1.0f, cudaEvent_t fence = nullptr) {
+           float norm_scale = 1.0f, cudaEvent_t fence = nullptr, bool row_sums = false) {
   int cur = 0;
   const int nclass = static_cast<int>(P.classes.size());
   double* sumsq = reinterpret_cast<double*>(ws + P.off_sumsq);
@@ -402,6 +402,7 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
           gp.skip = skip;
           const bool fused = final_update && kind == GEMM_APPLY && it == steps - 1;
           gp.final_update = fused ? 1 : 0;
+          gp.row_sums = row_sums && kind == GEMM_APPLY && it == steps - 1 ? 1 : 0;
           if (fused && fence) {
             // First launch that writes parameters (stream order carries the
             // wait to every later launch).
@@ -872,6 +873,7 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     J.mom_vec = cols4 && aligned16(U.momentum);
     J.ldx = C.ldx;
     J.x_view_stride = C.xrows * C.ldx;
+    J.stat_tiles_c = static_cast<int32_t>(T.tiles_c);
     bf16* xb = reinterpret_cast<bf16*>(ws + C.off_x[xbuf]) + T.class_slot * C.xrows * C.ldx;
     J.x0 = xb;
     J.xf = xb;
@@ -899,15 +901,20 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   }
   if (!finish_phase) return MH_OK;
   cudaEvent_t fence = static_cast<cudaEvent_t>(hp->param_fence);
+  // Under NorMuon / Muon+ the last apply stage also writes the row partials
+  // of U^2, so no separate statistics pass re-reads U.
+  const bool gemm_row_sums = need_rows && hp->ns_steps >= 1;
   rc = run_ns(P, ws, hp->ns_steps, hp->a, hp->b, hp->c, hp->eps, sms, stream, &final_buf,
               fuse_update, hp->cautious, hp->skip, hp->coeff_schedule, proto.ns_norm_scale,
-              fuse_update ? fence : nullptr);
+              fuse_update ? fence : nullptr, gemm_row_sums);
   if (rc != MH_OK) return rc;
   if (fuse_update) return MH_OK;
   auto fill_final = [&](const TensorInfo& T, EwJob& J) { fill_common(T, J, final_buf); };
   if (need_rows) {
-    rc = run_ew(EW_ROWSQ, P, proto, fill_final, sms, stream);
-    if (rc != MH_OK) return rc;
+    if (!gemm_row_sums) {
+      rc = run_ew(EW_ROWSQ, P, proto, fill_final, sms, stream);
+      if (rc != MH_OK) return rc;
+    }
     for (size_t t0 = 0; t0 < P.tensors.size(); t0 += kMaxRowFinJobs) {
       RowFinParams rp;
       std::memset(&rp, 0, sizeof(rp));
@@ -1046,6 +1053,7 @@ static int ns_impl(const mh_ns_problem* problems, int32_t n, int32_t steps, floa
     J.dst_vec = cols4 && aligned16(p.out);
     J.ldx = C.ldx;
     J.x_view_stride = C.xrows * C.ldx;
+    J.stat_tiles_c = static_cast<int32_t>(T.tiles_c);
     bf16* xb = reinterpret_cast<bf16*>(ws + C.off_x[xbuf]) + T.class_slot * C.xrows * C.ldx;
     J.x0 = xb;
     J.xf = xb;

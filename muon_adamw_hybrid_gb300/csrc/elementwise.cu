@@ -332,6 +332,8 @@ __global__ void __launch_bounds__(kEwThreads, kB16 ? 3 : 2)
       rec.psr = J.param_sr;
       rec.psr_key = J.param_key;
       rec.inactive = inactive ? 1 : 0;
+      rec.stat_tiles_c = J.stat_tiles_c;
+      rec.rowpart = J.rowpart != nullptr ? J.rowpart + v * J.stat_tiles_c * J.rows : nullptr;
       J.vrec[v] = rec;
     }
     bf16* xv = J.x0 + v * J.x_view_stride;
@@ -455,6 +457,8 @@ __global__ void __launch_bounds__(kEwThreads) prologue_kernel(const __grid_const
       rec.psr = J.param_sr;
       rec.psr_key = J.param_key;
       rec.inactive = inactive ? 1 : 0;
+      rec.stat_tiles_c = J.stat_tiles_c;
+      rec.rowpart = J.rowpart != nullptr ? J.rowpart + v * J.stat_tiles_c * J.rows : nullptr;
       J.vrec[v] = rec;
     }
 

@@ -40,6 +40,9 @@ struct ViewRec {
   int32_t psr;          // bf16 parameter written stochastically rounded
   uint32_t psr_key;     // its rounding key
   int32_t inactive;     // zero gradient under the inactive-expert rule: leave it alone
+  int32_t stat_tiles_c; // 256-column tiles of the row statistics
+  float* rowpart;       // [stat_tiles_c][rows] partial row sums of U^2 of this view, or
+                        // null; written by the last Newton-Schulz apply stage
 };
 
 struct EwJob {
@@ -61,6 +64,7 @@ struct EwJob {
   int64_t x_view_stride; // elements between views in the X buffers
   int64_t tile_begin;    // first global tile index of this tensor
   int32_t tiles_r, tiles_c;
+  int32_t stat_tiles_c;  // 256-column tiles of the row statistics (tiles_c of the stats passes)
   int32_t tall;          // unused by the kernels (X is always in stored layout)
   int32_t flat;          // prologue: wide view stored like X (cols % 8 == 0): streamed
                          // as contiguous kProChunk-element chunks, tiles_r = 1
@@ -251,6 +255,7 @@ struct GemmParams {
   int32_t mode;            // GemmMode shared by every class of the launch
   int32_t first_iter;      // fold the Frobenius normalisation in
   int32_t final_update;    // apply: update the parameters instead of writing X'
+  int32_t row_sums;        // last apply: also write each view's partial row sums of U^2
   int32_t cautious;        // MH_CAUTIOUS_* for the final update
   int64_t total_tiles;
   float a, b, c, eps;

@@ -502,6 +502,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
                              static_cast<uint32_t>(acc * kBN);
+      // Last apply under NorMuon / Muon+: this lane's row sum of U^2 over the
+      // tile's columns, of the values as stored (bf16).
+      float rsq = 0.0f;
 
 #pragma unroll 1
       for (int cc = 0; cc < kBN / 32; ++cc) {
@@ -565,6 +568,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 if (c0 + j < n_out) v[j] = sc * (p.a * __bfloat162float(aux[aoff + j]) + v[j]);
+            }
+            if (p.row_sums) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float q = __bfloat162float(__float2bfloat16_rn(v[j]));
+                if (c0 + j < n_out) rsq += q * q;
+              }
             }
           }
         } else if (p.kind == GEMM_POLY) {
@@ -632,6 +642,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           bulk_commit();
         }
         ++staged;
+      }
+      if (p.row_sums && r < rows_out) {
+        float* rp = C.vrec[tc.view].rowpart;
+        if (rp != nullptr) rp[static_cast<int64_t>(tc.tn) * rows_out + r] = rsq;
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
