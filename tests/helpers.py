@@ -83,7 +83,7 @@ def oracle_adam_tensor(wl: W.Workload, j: int, steps: int, offset: int = 0, coun
     return dict(W=Wt, m=m, v=v)
 
 
-class GpuRun:
+class DeviceRun:
     """A workload's tensors on the GPU, stepped through the C ABI."""
 
     def __init__(self, wl: W.Workload, device="cuda"):

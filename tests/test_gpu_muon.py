@@ -20,7 +20,7 @@ import pytest
 
 import oracle
 from synth import workloads as W
-from tests.helpers import GpuRun, oracle_muon_tensor, rel_fro, to_np
+from tests.helpers import DeviceRun, oracle_muon_tensor, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,7 @@ def _check(wl, run, tensors=None, w_prev=None):
 
 def test_single_256x1024_fp32():
     wl = W.single_matrix()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     W0 = to_np(run.mW[0])
     run.step()
     run.status_ok()
@@ -91,7 +91,7 @@ MIXED = [W.MuonSpec("sq", 1, 256, 256, "f32", "f32", w_std=1.0, g_std=1.0),
 
 def test_plain_step_mixed_shapes():
     wl = _wl(MIXED)
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     w0 = [to_np(w) for w in run.mW]
     run.step()
     run.status_ok()
@@ -107,7 +107,7 @@ def test_variants(flags):
              W.MuonSpec("b", 1, 384, 128, "bf16", "bf16"),
              W.MuonSpec("c", 4, 64, 96, "f32", "f32", w_std=0.5, g_std=0.3)]
     wl = _wl(specs, **flags)
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     w0 = [to_np(w) for w in run.mW]
     run.step()
     run.status_ok()
@@ -118,7 +118,7 @@ def test_three_steps_carry_state():
     specs = [W.MuonSpec("a", 1, 256, 640, "f32", "f32", w_std=1.0, g_std=1.0),
              W.MuonSpec("b", 2, 300, 128, "bf16", "bf16")]
     wl = _wl(specs, steps=3, normuon=True, muon_plus=True)
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     for _ in range(3):
         run.step()
     run.status_ok()
@@ -129,7 +129,7 @@ def test_zero_gradient_is_pure_decay():
     import torch
     specs = [W.MuonSpec("a", 1, 128, 384, "f32", "f32", w_std=1.0)]
     wl = _wl(specs)
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     run.mG[0].zero_()
     W0 = to_np(run.mW[0])
     run.step()
@@ -144,7 +144,7 @@ def test_views_match_separate_tensors():
     import muon_adamw_hybrid_gb300 as mh
     r, c = 256, 384
     packed = _wl([W.MuonSpec("p", 2, r, c, "f32", "f32", w_std=1.0, g_std=1.0)])
-    run = GpuRun(packed)
+    run = DeviceRun(packed)
     W0 = run.mW[0].clone()
     G0 = run.mG[0].clone()
     run.step()
@@ -164,7 +164,7 @@ def test_repeat_call_same_workspace_is_reproducible():
     import torch
     specs = [W.MuonSpec("a", 1, 256, 512, "f32", "f32", w_std=1.0, g_std=1.0)]
     wl = _wl(specs)
-    r1, r2 = GpuRun(wl), GpuRun(wl)
+    r1, r2 = DeviceRun(wl), DeviceRun(wl)
     r1.step()
     r2.ws.fill_(0xAB)  # stale workspace contents must not matter
     r2.step()
@@ -181,7 +181,7 @@ def test_polar_express_schedule_step():
              W.MuonSpec("b", 1, 384, 128, "bf16", "bf16"),
              W.MuonSpec("c", 1, 96, 200, "f32", "f32", w_std=0.5, g_std=0.3)]
     wl = _wl(specs, coeffs=sched, eps=0.0, norm_scale=1.01)
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     w0 = [to_np(w).copy() for w in run.mW]
     run.step()
     run.status_ok()

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from synth import workloads as W
-from tests.helpers import GpuRun, oracle_adam_tensor, oracle_muon_tensor, rel_fro, to_np
+from tests.helpers import DeviceRun, oracle_adam_tensor, oracle_muon_tensor, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -74,7 +74,7 @@ def _index(wl, name):
 
 def test_llama7b_one_step_sampled():
     wl = W.llama7b()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     run.step()
     run.status_ok()
     _check_muon_views(wl, run, _index(wl, "l0.q"), [0], 1)
@@ -90,7 +90,7 @@ def test_llama7b_one_step_sampled():
 
 def test_gpt124m_ten_steps_sampled():
     wl = W.gpt124m()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     for _ in range(wl.steps):
         run.step()
     run.status_ok()
@@ -105,7 +105,7 @@ def test_gpt124m_ten_steps_sampled():
 
 def test_moe_mla_all_variants_sampled():
     wl = W.moe_mla()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     run.step()
     run.status_ok()
     _check_muon_views(wl, run, _index(wl, "e0.gate_up"), [0, 1], 1)
@@ -117,7 +117,7 @@ def test_moe_mla_all_variants_sampled():
 
 def test_single_matrix_config():
     wl = W.single_matrix()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     run.step()
     run.status_ok()
     _check_muon_views(wl, run, 0, [0], 1)
@@ -126,7 +126,7 @@ def test_single_matrix_config():
 
 def test_adamw_2p30_fp32_sampled():
     wl = W.adamw_2p30()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     run.step()
     n = 1 << 30
     for off in (0, n // 2 + 12345, n - (1 << 20)):
