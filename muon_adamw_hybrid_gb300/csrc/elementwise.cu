@@ -82,9 +82,11 @@ __device__ __forceinline__ void load_u_raw(const EwJob& J, const TileInfo& t, ui
   }
 }
 
-// Unpacks the block issued by load_u_raw (ragged last columns are read here).
+// Unpacks the block issued by load_u_raw (ragged last columns are read here),
+// times `scale`.
 __device__ __forceinline__ void unpack_u_block(const EwJob& J, const TileInfo& t,
-                                               const uint4 (&raw)[4], float u[4][8]) {
+                                               const uint4 (&raw)[4], float u[4][8],
+                                               float scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bf16* xv = J.xf + t.v * J.x_view_stride;
   const int64_t col = t.c0 + lane * 8;
@@ -104,6 +106,8 @@ __device__ __forceinline__ void unpack_u_block(const EwJob& J, const TileInfo& t
 #pragma unroll
       for (int k = 0; k < 8; ++k) u[i][k] = k < nvalid ? __bfloat162float(src[k]) : 0.0f;
     }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) u[i][k] *= scale;
   }
 }
 
@@ -556,7 +560,12 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
     uint4 uraw[4];
     load_u_raw(J, t, uraw);
     float u[4][8];
-    if constexpr (KIND != EW_APPLY) unpack_u_block(J, t, uraw, u);
+    // Without Newton-Schulz steps U is the normalised momentum: the buffer
+    // holds bf16(Q) and every pass scales it by 1/(||Q|| norm_scale + eps).
+    const float uscale = p.u_scale_from_sumsq
+                             ? ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps)
+                             : 1.0f;
+    if constexpr (KIND != EW_APPLY) unpack_u_block(J, t, uraw, u, uscale);
 
     if constexpr (KIND == EW_ROWSQ) {
 #pragma unroll
@@ -594,8 +603,6 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
       __syncthreads();
     } else {
       // EW_APPLY / EW_COPYOUT: final update direction U_ij.
-      float uscale = 1.0f;
-      if (p.u_scale_from_sumsq) uscale = ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps);
       // 16-byte access needs 8-element rows for bf16 and 4-element rows for fp32.
       const bool dvec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
       const bool svec = J.src_vec && (J.src_dtype == MH_F32 || (J.cols % 8) == 0);
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
           if (k < nvalid) h[k] = J.colfac[t.v * J.cols + col + k];
       }
       if constexpr (KIND == EW_APPLY) {
-        unpack_u_block(J, t, uraw, u);
+        unpack_u_block(J, t, uraw, u, uscale);
         if (wraw) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
         const float f = fr[i];
         float uu[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) uu[k] = (u[i][k] * uscale) * f * h[k];
+        for (int k = 0; k < 8; ++k) uu[k] = u[i][k] * f * h[k];
         const int64_t off = view_elem0 + row * J.cols + col;
         if constexpr (KIND == EW_COPYOUT) {
           const bool ovec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);

@@ -1,0 +1,65 @@
+"""Degenerate step configurations against the oracle.
+
+* ns_steps = 0: U is the normalised momentum itself (no GEMM; every pass
+  reading U scales it by 1/(||Q|| + eps), the statistics passes of NorMuon and
+  Muon+ included); with NorMuon the separate row-statistics pass runs instead
+  of the GEMM epilogue's row sums.
+* ns_steps = 1: the first iteration's normalisation and the last apply stage
+  are the same launch (fused update, or row sums under NorMuon).
+* A call mixing empty tensors (zero rows, zero views' worth of elements) with
+  ordinary ones: the empty ones are skipped, the rest match the oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import workloads as W
+from tests.helpers import DeviceRun
+from tests.test_gpu_muon import _check, _wl
+
+pytestmark = pytest.mark.gpu
+
+# fp32 parameters: with ns_steps = 0 the update (Frobenius norm lr) is a
+# fraction of a bf16 spacing of the weights, so bf16 storage would hide it.
+SPECS = [W.MuonSpec("a", 2, 128, 320, "f32", "f32", w_std=1.0, g_std=1.0),
+         W.MuonSpec("b", 1, 300, 96, "f32", "bf16", w_std=0.5),
+         W.MuonSpec("c", 1, 64, 64, "f32", "f32", w_std=0.5, g_std=0.3)]
+
+
+@pytest.mark.parametrize("ns_steps", [0, 1, 2])
+@pytest.mark.parametrize("flags", [dict(), dict(normuon=True), dict(muon_plus=True, cautious=1)])
+def test_few_newton_schulz_steps(ns_steps, flags):
+    from tests.helpers import to_np
+    wl = _wl(SPECS, ns_steps=ns_steps, **flags)
+    run = DeviceRun(wl)
+    w0 = [to_np(w) for w in run.mW]
+    run.step()
+    run.status_ok()
+    _check(wl, run, w_prev=w0)
+
+
+def test_empty_tensors_are_skipped_beside_others():
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+    from tests.helpers import rel_fro, to_np
+    import synth
+    dev = "cuda"
+    w = torch.tensor(synth.normal(95, 0, (256, 512), std=1.0), dtype=torch.float32, device=dev)
+    g = torch.tensor(synth.normal(96, 0, (256, 512), std=1.0), dtype=torch.float32, device=dev)
+    b = torch.zeros_like(w)
+    e_w = torch.empty((0, 64), dtype=torch.float32, device=dev)
+    e_g, e_b = torch.empty_like(e_w), torch.empty_like(e_w)
+    w0 = w.clone()
+    ts = [mh.muon_tensor(e_w, e_g, e_b, 1, None, 1.0, 0.01),
+          mh.muon_tensor(w, g, b, 1, None, 1.0, 0.01),
+          mh.muon_tensor(e_w, e_g, e_b, 1, None, 1.0, 0.01)]
+    hp = mh.make_hparams()
+    ws = torch.empty(mh.muon_workspace_bytes(ts, hp), dtype=torch.uint8, device=dev)
+    mh.muon_step_batched(ts, hp, ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    mh.workspace_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    res = oracle.muon_step_view(to_np(w0), to_np(g), np.zeros((256, 512)), oracle.MuonHparams(),
+                                1.0, 0.01)
+    assert rel_fro(to_np(b), res.B) < 1e-6
+    tol = max(1e-3, 2e-2 * np.linalg.norm(res.W - 0.9998 * to_np(w0)) / np.linalg.norm(res.W))
+    assert rel_fro(to_np(w), res.W) < tol
