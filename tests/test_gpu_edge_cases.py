@@ -6,6 +6,8 @@
   of the GEMM epilogue's row sums.
 * ns_steps = 1: the first iteration's normalisation and the last apply stage
   are the same launch (fused update, or row sums under NorMuon).
+* The cautious-update mask under NorMuon / Muon+ (the separate apply pass's
+  own instantiation, which reads the gradient).
 * A call mixing empty tensors (zero rows, zero views' worth of elements) with
   ordinary ones: the empty ones are skipped, the rest match the oracle.
 """
@@ -27,7 +29,9 @@ SPECS = [W.MuonSpec("a", 2, 128, 320, "f32", "f32", w_std=1.0, g_std=1.0),
 
 
 @pytest.mark.parametrize("ns_steps", [0, 1, 2])
-@pytest.mark.parametrize("flags", [dict(), dict(normuon=True), dict(muon_plus=True, cautious=1)])
+@pytest.mark.parametrize("flags", [dict(), dict(normuon=True), dict(muon_plus=True, cautious=1),
+                                   dict(normuon=True, cautious=2),
+                                   dict(normuon=True, muon_plus=True, cautious=2)])
 def test_few_newton_schulz_steps(ns_steps, flags):
     from tests.helpers import to_np
     wl = _wl(SPECS, ns_steps=ns_steps, **flags)
