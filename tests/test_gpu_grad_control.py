@@ -202,3 +202,56 @@ def test_hybrid_steps_under_clipping_and_a_skipped_step():
         assert rel_fro(to_np(opt.exp_avg[j]), ref["m"][j]) < 1e-6, name
         assert rel_fro(to_np(opt.exp_avg_sq[j]), ref["v"][j]) < 1e-6, name
         assert rel_fro(to_np(pa[j]), ref["Wa"][j]) < 1e-6, name
+
+
+def test_skipped_step_under_normuon_and_muon_plus_changes_nothing():
+    """With NorMuon, Muon+ and the cautious-update mask on (so every separate
+    pass runs: row statistics in the GEMM, column statistics, both
+    finalisations, the apply), a step with an inf gradient leaves parameters,
+    momentum, NorMuon state and AdamW moments bit for bit as they were, and
+    the steps around it equal those of an optimizer that never saw it."""
+    import torch
+    import muon_adamw_hybrid_gb300 as mh
+
+    def make():
+        pm = [torch.tensor(synth.normal(17, i, s, std=0.02), dtype=torch.float32, device="cuda")
+              for i, (_, s, _, _) in enumerate(MUON)]
+        pa = [torch.tensor(synth.normal(18, i, s, std=0.02), dtype=torch.float32, device="cuda")
+              for i, (_, s, _) in enumerate(ADAM)]
+        opt = mh.HybridMuonAdamW([dict(param=p, views=v, wd=MUON_WD)
+                                  for p, (_, _, v, _) in zip(pm, MUON)],
+                                 [dict(param=p, wd=0.1) for p in pa],
+                                 normuon=True, muon_plus=True, cautious=2, max_grad_norm=1.0)
+        return pm, pa, opt
+
+    def grads(step, bad=False):
+        gm = [torch.tensor(synth.normal(19 + step, i, s, std=1e-3), dtype=torch.float32,
+                           device="cuda") for i, (_, s, _, _) in enumerate(MUON)]
+        ga = [torch.tensor(synth.normal(29 + step, i, s, std=1e-3), dtype=torch.float32,
+                           device="cuda") for i, (_, s, _) in enumerate(ADAM)]
+        if bad:
+            gm[0].view(-1)[5] = float("inf")
+        return gm, ga
+
+    pm, pa, opt = make()
+    rm, ra, ref = make()
+    opt.step(*grads(0))
+    ref.step(*grads(0))
+    torch.cuda.synchronize()
+    state = [t.clone() for t in pm + pa + opt.momentum + opt.exp_avg + opt.exp_avg_sq
+             + [s for s in opt.normuon_sm if s is not None]]
+    opt.step(*grads(1, bad=True))
+    torch.cuda.synchronize()
+    after = pm + pa + opt.momentum + opt.exp_avg + opt.exp_avg_sq + \
+        [s for s in opt.normuon_sm if s is not None]
+    for a, b in zip(state, after):
+        assert torch.equal(a, b)
+    assert int(opt.control.skip.item()) == 1 and opt.applied_steps() == 1
+    opt.step(*grads(2))
+    ref.step(*grads(2))
+    torch.cuda.synchronize()
+    for a, b in zip(pm + pa + opt.momentum + opt.exp_avg + opt.exp_avg_sq,
+                    rm + ra + ref.momentum + ref.exp_avg + ref.exp_avg_sq):
+        assert torch.equal(a, b)
+    for a, b in zip(opt.normuon_sm, ref.normuon_sm):
+        assert a is None or torch.equal(a, b)
