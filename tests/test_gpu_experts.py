@@ -49,10 +49,13 @@ def _run(hp_kw):
     return keep
 
 
-@pytest.mark.parametrize("hp_kw", [dict(), dict(normuon=True), dict(cautious=1)])
+@pytest.mark.parametrize("hp_kw", [dict(), dict(normuon=True), dict(cautious=1),
+                                   dict(muon_plus=True), dict(normuon=True, muon_plus=True,
+                                                              cautious=2)])
 def test_inactive_views_are_untouched_and_the_rest_match(hp_kw):
     keep = _run(hp_kw)
     ohp = oracle.MuonHparams(normuon=hp_kw.get("normuon", False),
+                             muon_plus=hp_kw.get("muon_plus", False),
                              cautious=hp_kw.get("cautious", 0))
     for (name, views, r, c, flag, silent), k in zip(SPECS, keep):
         W0 = k["w"].astype(np.float32).astype(np.float64)
@@ -76,6 +79,9 @@ def test_inactive_views_are_untouched_and_the_rest_match(hp_kw):
             assert rel_fro(got_w[rows], Wn[rows]) < tol, (name, v)
             if k["sm"] is not None:
                 assert rel_fro(to_np(k["sm"])[rows], smn.reshape(-1)[rows]) < 3e-2, (name, v)
-    # the unflagged silent tensor did move (decay and momentum)
+    # the unflagged silent tensor did move (decay and momentum), unless the
+    # cautious-update mask is on: it keeps only entries whose update agrees
+    # with a gradient that is zero everywhere here
     dense = keep[-1]
-    assert not np.array_equal(to_np(dense["dw"]), dense["w"].astype(np.float32))
+    moved = not np.array_equal(to_np(dense["dw"]), dense["w"].astype(np.float32))
+    assert moved == (hp_kw.get("cautious", 0) != 2)
