@@ -67,3 +67,26 @@ def test_empty_tensors_are_skipped_beside_others():
     assert rel_fro(to_np(b), res.B) < 1e-6
     tol = max(1e-3, 2e-2 * np.linalg.norm(res.W - 0.9998 * to_np(w0)) / np.linalg.norm(res.W))
     assert rel_fro(to_np(w), res.W) < tol
+
+
+# Column counts that are not multiples of 8 take the tiled prologue (not the
+# flat stream), scalar parameter access and ragged GEMM/statistics tiles.
+RAGGED = [W.MuonSpec("r1", 3, 33, 65, "f32", "f32", w_std=1.0, g_std=1.0),
+          W.MuonSpec("r2", 1, 130, 37, "f32", "bf16", w_std=0.5),
+          W.MuonSpec("r3", 2, 57, 250, "f32", "f32", w_std=0.5, g_std=0.3),
+          W.MuonSpec("r4", 1, 1, 77, "f32", "f32", w_std=1.0),
+          W.MuonSpec("r5", 1, 77, 1, "f32", "f32", w_std=1.0)]
+
+
+@pytest.mark.parametrize("flags", [dict(), dict(normuon=True), dict(muon_plus=True, cautious=1),
+                                   dict(normuon=True, muon_plus=True, cautious=2)])
+def test_ragged_shapes_full_step(flags):
+    from tests.helpers import to_np
+    wl = _wl(RAGGED, steps=2, **flags)
+    run = DeviceRun(wl)
+    run.step()
+    w1 = [to_np(w) for w in run.mW]
+    run.step()
+    run.status_ok()
+    _check(wl, run)
+    assert all(np.isfinite(w).all() for w in w1)

@@ -60,8 +60,10 @@ def _check(wl, run, tensors=None, w_prev=None):
                 bar = 2e-2 if spec.param_dtype == "f32" else 5e-2
                 assert rel_fro(d_got, d_ref) < bar, (spec.name, rel_fro(d_got, d_ref))
         if run.sm[i] is not None:
+            # sm averages U^2: a relative error e in U (the NS bar, 2e-2) moves
+            # it by up to 2e
             got_sm = to_np(run.sm[i]).reshape(spec.views, spec.rows)
-            assert rel_fro(got_sm, ref["sm"]) < 3e-2, (spec.name, rel_fro(got_sm, ref["sm"]))
+            assert rel_fro(got_sm, ref["sm"]) < 4e-2, (spec.name, rel_fro(got_sm, ref["sm"]))
 
 
 def test_single_256x1024_fp32():
