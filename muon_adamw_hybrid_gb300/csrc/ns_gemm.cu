@@ -280,6 +280,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   constexpr bool b_mn = MODE != GEMM_MODE_KK;
   // A skipped step (gradient control): every thread of both CTAs of the pair
   // reads the same flag and leaves before any barrier, TMEM or cluster op.
+  // Launched as a programmatic dependent of the previous kernel on the stream:
+  // wait for it to complete (and its writes to be visible) before anything
+  // else, then let the next stage's grid launch, so that its CTAs are
+  // resident by the time this grid finishes.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (step_skipped(p.skip)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -729,13 +735,15 @@ cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kKernels[p.mode], p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
