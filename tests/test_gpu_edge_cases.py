@@ -90,3 +90,23 @@ def test_ragged_shapes_full_step(flags):
     run.status_ok()
     _check(wl, run)
     assert all(np.isfinite(w).all() for w in w1)
+
+
+# bf16 parameters with fp32 gradients (and the reverse): the cautious-update
+# mask reads the gradient in its own dtype, in the fused GEMM update and in
+# the separate apply pass.
+MIXED = [W.MuonSpec("m1", 1, 256, 512, "bf16", "f32", w_std=1.0, g_std=1.0),
+         W.MuonSpec("m2", 2, 300, 128, "bf16", "f32", w_std=1.0, g_std=1.0),
+         W.MuonSpec("m3", 1, 96, 200, "f32", "bf16", w_std=1.0, g_std=1.0)]
+
+
+@pytest.mark.parametrize("flags", [dict(cautious=2), dict(cautious=1),
+                                   dict(normuon=True, cautious=2)])
+def test_mixed_dtypes_with_cautious_masks(flags):
+    from tests.helpers import to_np
+    wl = _wl(MIXED, **flags)
+    run = DeviceRun(wl)
+    w0 = [to_np(w) for w in run.mW]
+    run.step()
+    run.status_ok()
+    _check(wl, run, w_prev=w0)
