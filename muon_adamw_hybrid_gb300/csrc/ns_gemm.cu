@@ -278,15 +278,6 @@ template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool a_mn = MODE == GEMM_MODE_MM;
   constexpr bool b_mn = MODE != GEMM_MODE_KK;
-  // A skipped step (gradient control): every thread of both CTAs of the pair
-  // reads the same flag and leaves before any barrier, TMEM or cluster op.
-  // Launched as a programmatic dependent of the previous kernel on the stream:
-  // wait for it to complete (and its writes to be visible) before anything
-  // else, then let the next stage's grid launch, so that its CTAs are
-  // resident by the time this grid finishes.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (step_skipped(p.skip)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -337,7 +328,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   const uint32_t tmem_base = *tmem_slot;
   const bool apply = p.kind == GEMM_APPLY;
 
-  if (warp == 0) {
+  // The kernel is launched as a programmatic dependent of the previous one
+  // on the stream: the setup above (barriers, tensor-map prefetch, TMEM,
+  // cluster barrier) touches only shared memory, TMEM and the parameter
+  // block, so it overlaps that kernel's tail. Nothing it writes is read
+  // before this wait. Then the next stage's grid may launch, so its CTAs are
+  // resident by the time this grid finishes.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (step_skipped(p.skip)) {
+    // A skipped step (gradient control): every thread of both CTAs reads the
+    // same flag, no role runs, and the teardown below still pairs the
+    // cluster barrier and frees TMEM.
+  } else if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       int stage = 0;
