@@ -212,7 +212,7 @@ int mh_newton_schulz_batched_ex(const mh_ns_problem* problems, int32_t n, int32_
 #define MH_NS_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /* mh_newton_schulz_batched for callers that cannot allocate device memory.
- * The paper has no counterpart to this entry point; it exists for callers
+ * None of the pages describes this entry point; it exists for callers
  * that have no way to provide a workspace -- for example a plugin that its
  * host application gives only input and output buffers, or a program whose
  * device memory is already fully reserved by its own pool -- and so can
