@@ -27,6 +27,7 @@
 //
 // Plus the per-view row finalisation (NorMuon state update, norm restore,
 // Muon+ row factor; flaxchat step 3, Speedtronic "Muon+").
+#include <atomic>
 #include "mh_internal.h"
 #include "mh_sr.cuh"
 #include "muonhybrid.h"
@@ -870,19 +871,20 @@ cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s) {
 }
 
 // Resident blocks per SM of each elementwise kernel (queried once per kind),
-// so that the persistent grids are exactly one wave.
+// so that the persistent grids are exactly one wave. Calls from several host
+// threads may race to fill an entry; they all store the same value.
 int blocks_per_sm(EwKind kind, const void* kernel) {
-  static int cached[kEwKinds] = {};
-  if (cached[kind] == 0) {
-    int b = 0;
+  static std::atomic<int> cached[kEwKinds] = {};
+  int b = cached[kind].load(std::memory_order_relaxed);
+  if (b == 0) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kEwThreads, 0) != cudaSuccess ||
         b <= 0) {
       (void)cudaGetLastError();
       b = 2;
     }
-    cached[kind] = b;
+    cached[kind].store(b, std::memory_order_relaxed);
   }
-  return cached[kind];
+  return b;
 }
 
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s) {
