@@ -20,11 +20,13 @@ import oracle
 # The submodules by name: the package re-exports functions that share some of
 # their names (grad_control, qk_clip).
 o_adamw = importlib.import_module("oracle.adamw")
+o_bf16 = importlib.import_module("oracle.bf16")
 o_gc = importlib.import_module("oracle.grad_control")
 o_muon = importlib.import_module("oracle.muon")
 o_qk = importlib.import_module("oracle.qk_clip")
 o_sr = importlib.import_module("oracle.stochastic_round")
 from tests import test_oracle_adamw as adam_pins
+from tests import test_oracle_bf16 as bf16_pins
 from tests import test_oracle_grad_control as gc_pins
 from tests import test_oracle_ns as ns_pins
 from tests import test_oracle_qk_clip as qk_pins
@@ -129,10 +131,15 @@ VIEW_PINS = [
     ("silent view per view", up_pins.test_flag_is_per_view_in_a_packed_tensor),
 ]
 
+BF16_PINS = [
+    ("torch cast on float32 values", bf16_pins.test_matches_torch_on_float32_values),
+    ("ties and near ties", bf16_pins.test_ties_and_near_ties_from_float64),
+]
+
 
 def test_every_pin_passes_on_the_real_oracle():
     every = (NS_PINS + MOMENTUM_PINS + APPLY_PINS + NORMUON_PINS + ADAMW_PINS + GC_PINS + QK_PINS
-             + SR_PINS + VIEW_PINS)
+             + SR_PINS + VIEW_PINS + BF16_PINS)
     assert _failing(every) == []
 
 
@@ -406,3 +413,50 @@ def test_hash_constant_typo_is_caught(monkeypatch):
         return np.array([fmix(int(v)) for v in np.asarray(x).ravel()], dtype=np.uint64)
     _plant(monkeypatch, "fmix32", fmix, o_sr)
     assert _failing(SR_PINS)
+
+
+# ---- bf16 storage rounding ----------------------------------------------------------------
+
+def _bf16_with(mistake):
+    def rnd(x):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        if mistake == "double rounding through float32":
+            x = x.astype(np.float32).astype(np.float64)
+        bits = x.reshape(-1).view(np.uint64)
+        drop = np.uint64(45)
+        mask = (np.uint64(1) << drop) - np.uint64(1)
+        low, kept = bits & mask, bits & ~mask
+        half = np.uint64(1) << np.uint64(44)
+        if mistake == "ties away from zero":
+            up = low >= half
+        else:
+            lsb = (bits >> drop) & np.uint64(1)
+            up = (low > half) | ((low == half) & (lsb == np.uint64(1)))
+        out = (kept + np.where(up, np.uint64(1) << drop, np.uint64(0))).view(np.float64)
+        return out.reshape(x.shape)
+    return rnd
+
+
+@pytest.mark.parametrize("mistake", ["ties away from zero", "double rounding through float32"])
+def test_bf16_rounding_mistakes_are_caught(monkeypatch, mistake):
+    _plant(monkeypatch, "round_bf16", _bf16_with(mistake), o_bf16)
+    assert _failing(BF16_PINS), mistake
+
+
+# ---- the order of the stages in one view's step ----------------------------------------------
+
+def test_muon_plus_before_normuon_is_caught(monkeypatch):
+    def step(W, G, B, hp, lr_mult=1.0, wd=0.0, sm=None, skip_zero_grad=False):
+        W, G, B = (np.asarray(a, dtype=np.float64) for a in (W, G, B))
+        B_new, Q = o_muon.momentum_nesterov(B, G, hp.momentum, hp.nesterov)
+        U = o_muon.newton_schulz(Q, hp.ns_steps, hp.coeffs, hp.eps, hp.norm_scale)
+        if hp.muon_plus:
+            U = o_muon.muon_plus_row_col(U, hp.plus_eps)
+        sm_new = None
+        if hp.normuon:
+            U, sm_new = o_muon.normuon(U, np.zeros(W.shape[0]) if sm is None else sm, hp.beta2,
+                                       hp.normuon_eps)
+        W_new = o_muon.muon_apply(W, U, G, hp.lr * lr_mult, wd, hp.cautious)
+        return o_muon.ViewResult(W=W_new, B=B_new, U=U, sm=sm_new)
+    _plant(monkeypatch, "muon_step_view", step, o_muon)
+    assert _failing([("step composes its pieces", up_pins.test_full_view_step_composes_pieces)])
