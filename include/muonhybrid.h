@@ -77,6 +77,17 @@ typedef enum { MH_F32 = 0, MH_BF16 = 1 } mh_dtype;
  *                      entries with update*gradient > 0. */
 enum { MH_CAUTIOUS_OFF = 0, MH_CAUTIOUS_WD = 1, MH_CAUTIOUS_UPDATE = 2 };
 
+/* Shape factor s of the update W <- (1 - lr wd) W - lr s U, from the rows
+ * and cols of the stored view (mh_muon_hparams.shape_rule):
+ *   MH_SHAPE_RATIO      Speedtronic "Muon update": s = max(1, rows/cols)^0.5.
+ *   MH_SHAPE_MOONLIGHT  kimi-k3 "Why treat a matrix differently?" names the
+ *                       Moonlight shape factor as its trainer's default but
+ *                       its formula did not survive on the page; read as the
+ *                       published Moonlight rule s = 0.2 sqrt(max(rows, cols)),
+ *                       which gives a full-rank U with unit singular values an
+ *                       RMS of 0.2. */
+enum { MH_SHAPE_RATIO = 0, MH_SHAPE_MOONLIGHT = 1 };
+
 /* One Muon-routed parameter (a 2-D matrix or a stack of `views` matrices). */
 typedef struct {
   void* param;            /* (views*rows, cols), param_dtype, updated in place */
@@ -161,6 +172,8 @@ typedef struct {
    * (The Frobenius-norm restore that follows divides by the norm after the
    * row scaling, floored at 1e-10 against division by zero.) */
   float normuon_eps;
+  /* Shape factor of the update (MH_SHAPE_*); 0 is the Speedtronic ratio rule. */
+  int32_t shape_rule;
 } mh_muon_hparams;
 
 enum { MH_STEP_ALL = 0, MH_STEP_GRADIENTS = 1, MH_STEP_FINISH = 2 };

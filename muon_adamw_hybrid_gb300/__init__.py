@@ -12,7 +12,8 @@ include/muonhybrid.h). This package is a thin binding:
 Importing the package loads the library and raises if it is missing.
 """
 from ._lib import (MH_BF16, MH_CAUTIOUS_OFF, MH_CAUTIOUS_UPDATE, MH_CAUTIOUS_WD, MH_F32,
-                   MH_STEP_ALL, MH_STEP_FINISH, MH_STEP_GRADIENTS,
+                   MH_SHAPE_MOONLIGHT, MH_SHAPE_RATIO, MH_STEP_ALL, MH_STEP_FINISH,
+                   MH_STEP_GRADIENTS,
                    AdamwTensor, GradControl, GradRef, MuonHparams, MuonHybridError, MuonTensor,
                    NsProblem, QkClipEntry, adamw_step, adamw_step_ctl,
                    grad_prepare_workspace_bytes,
@@ -26,7 +27,8 @@ from .routing import route_parameters
 
 __all__ = [
     "MH_BF16", "MH_CAUTIOUS_OFF", "MH_CAUTIOUS_UPDATE", "MH_CAUTIOUS_WD", "MH_F32",
-    "MH_STEP_ALL", "MH_STEP_FINISH", "MH_STEP_GRADIENTS", "AdamwTensor",
+    "MH_SHAPE_MOONLIGHT", "MH_SHAPE_RATIO", "MH_STEP_ALL", "MH_STEP_FINISH", "MH_STEP_GRADIENTS",
+    "AdamwTensor",
     "GradControl", "GradRef", "MuonHparams", "MuonHybridError", "MuonTensor", "NsProblem",
     "adamw_step", "adamw_step_ctl", "grad_prepare_workspace_bytes", "last_error",
     "muon_step_batched", "muon_workspace_bytes", "newton_schulz_batched", "ns_workspace_bytes",

@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "MH_OK", 1: "MH_EINVAL", 2: "MH_EDTYPE", 3: "MH_ESHAPE", 4: "
 MH_F32, MH_BF16 = 0, 1
 MH_CAUTIOUS_OFF, MH_CAUTIOUS_WD, MH_CAUTIOUS_UPDATE = 0, 1, 2
 MH_STEP_ALL, MH_STEP_GRADIENTS, MH_STEP_FINISH = 0, 1, 2
+MH_SHAPE_RATIO, MH_SHAPE_MOONLIGHT = 0, 1
 
 EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_bytes",
             "mh_newton_schulz_batched", "mh_adamw_step", "mh_workspace_status", "mh_last_error",
@@ -44,7 +45,8 @@ class MuonHparams(ctypes.Structure):
                 ("plus_eps", c_float), ("cautious", c_int32),
                 ("grad_mult", c_void_p), ("skip", c_void_p), ("sr_seed", c_uint64),
                 ("coeff_schedule", c_void_p), ("norm_scale", c_float),
-                ("param_fence", c_void_p), ("phase", c_int32), ("normuon_eps", c_float)]
+                ("param_fence", c_void_p), ("phase", c_int32), ("normuon_eps", c_float),
+                ("shape_rule", c_int32)]
 
 
 class NsProblem(ctypes.Structure):

@@ -712,6 +712,8 @@ int check_muon_args(const mh_muon_tensor* t, int32_t n, const mh_muon_hparams* h
     return fail(MH_EINVAL, "normuon_eps must be finite and >= 0 (0 means 1e-10)");
   if (hp->phase < MH_STEP_ALL || hp->phase > MH_STEP_FINISH)
     return fail(MH_EINVAL, "phase must be 0, 1 or 2 (got %d)", hp->phase);
+  if (hp->shape_rule != MH_SHAPE_RATIO && hp->shape_rule != MH_SHAPE_MOONLIGHT)
+    return fail(MH_EINVAL, "shape_rule must be 0 or 1 (got %d)", hp->shape_rule);
   for (int i = 0; i < n; ++i) {
     const mh_muon_tensor& T = t[i];
     int rc = check_shape(T.views, T.rows, T.cols, i, "tensors");
@@ -890,7 +892,10 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
     }
     J.lr = hp->lr * U.lr_mult;
     J.wd = U.wd;
-    J.shape_scale = static_cast<float>(std::sqrt(std::max(1.0, double(T.rows) / double(T.cols))));
+    J.shape_scale = static_cast<float>(
+        hp->shape_rule == MH_SHAPE_MOONLIGHT
+            ? 0.2 * std::sqrt(static_cast<double>(std::max(T.rows, T.cols)))
+            : std::sqrt(std::max(1.0, double(T.rows) / double(T.cols))));
   };
 
   if (grad_phase) {

@@ -61,10 +61,11 @@ def _keep(struct, *tensors):
 
 def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_STEPS,
                  coeffs=NS_COEFFS, normuon=False, beta2=0.95, muon_plus=False, plus_eps=NS_EPS,
-                 cautious=0, norm_scale=1.0, normuon_eps=1e-10) -> MuonHparams:
+                 cautious=0, norm_scale=1.0, normuon_eps=1e-10, shape_rule=0) -> MuonHparams:
     """Muon hyperparameters. ``coeffs`` is one (a, b, c) for every iteration, or
     a sequence of ``ns_steps`` triples (flaxchat's Polar Express schedule);
-    ``norm_scale`` gives X0 = Q / (||Q|| * norm_scale + eps)."""
+    ``norm_scale`` gives X0 = Q / (||Q|| * norm_scale + eps); ``shape_rule``
+    picks the update's shape factor (MH_SHAPE_RATIO or MH_SHAPE_MOONLIGHT)."""
     sched = None
     if len(coeffs) and not isinstance(coeffs[0], (int, float)):
         if len(coeffs) != ns_steps:
@@ -77,7 +78,8 @@ def make_hparams(lr=0.02, momentum=0.95, nesterov=True, eps=NS_EPS, ns_steps=NS_
     hp = MuonHparams(lr=lr, momentum=momentum, nesterov=int(bool(nesterov)), eps=eps,
                      ns_steps=ns_steps, a=a, b=b, c=c, normuon=int(bool(normuon)), beta2=beta2,
                      muon_plus=int(bool(muon_plus)), plus_eps=plus_eps, cautious=int(cautious),
-                     norm_scale=norm_scale, normuon_eps=normuon_eps)
+                     norm_scale=norm_scale, normuon_eps=normuon_eps,
+                     shape_rule=int(shape_rule))
     if sched is not None:
         hp.coeff_schedule = ctypes.addressof(sched)
         hp._sched = sched          # the library reads it during each call
@@ -283,12 +285,12 @@ class HybridMuonAdamW:
                  ns_steps=NS_STEPS, coeffs=NS_COEFFS, eps=NS_EPS, normuon=False,
                  normuon_beta2=0.95, muon_plus=False, plus_eps=NS_EPS, cautious=0,
                  adam_lr=3e-4, adam_betas=(0.9, 0.95), adam_eps=1e-8, max_grad_norm=None,
-                 state_dtype=torch.float32, param_sr=False, normuon_eps=1e-10):
+                 state_dtype=torch.float32, param_sr=False, normuon_eps=1e-10, shape_rule=0):
         self.muon = [e if isinstance(e, MuonGroupEntry) else MuonGroupEntry(**e) for e in muon_params]
         self.adam = [e if isinstance(e, AdamGroupEntry) else AdamGroupEntry(**e) for e in adamw_params]
         self.hp = make_hparams(lr, momentum, nesterov, eps, ns_steps, coeffs, normuon,
                                normuon_beta2, muon_plus, plus_eps, cautious,
-                               normuon_eps=normuon_eps)
+                               normuon_eps=normuon_eps, shape_rule=shape_rule)
         self.adam_lr, self.adam_betas, self.adam_eps = adam_lr, adam_betas, adam_eps
         self.step_count = 0
         # dew.training.optim "bf16_moments": bf16 state is kept stochastically

@@ -11,7 +11,7 @@ the iteration must respect, brute force on tiny inputs, and PyTorch's own
 AdamW and gradient clipping in float64.
 """
 from .muon import (NS_COEFFS, NS_EPS, NS_STEPS, NORMUON_FLOOR, CAUTIOUS_OFF, CAUTIOUS_UPDATE,
-                   CAUTIOUS_WD,
+                   CAUTIOUS_WD, SHAPE_MOONLIGHT, SHAPE_RATIO,
                    MuonHparams, momentum_nesterov, muon_apply, muon_plus_row_col,
                    muon_step_tensor, muon_step_view, newton_schulz, normuon, shape_scale)
 from .adamw import adamw_step
@@ -23,7 +23,7 @@ from .stochastic_round import (MOMENT_FIRST, MOMENT_PARAM, MOMENT_SECOND, round_
 
 __all__ = [
     "NS_COEFFS", "NS_EPS", "NS_STEPS", "NORMUON_FLOOR", "CAUTIOUS_OFF", "CAUTIOUS_UPDATE",
-    "CAUTIOUS_WD",
+    "CAUTIOUS_WD", "SHAPE_MOONLIGHT", "SHAPE_RATIO",
     "MuonHparams", "momentum_nesterov", "muon_apply", "muon_plus_row_col", "muon_step_tensor",
     "muon_step_view", "newton_schulz", "normuon", "shape_scale", "adamw_step", "round_bf16",
     "CLIP_EPS", "GradControl", "grad_control", "MOMENT_FIRST", "MOMENT_PARAM", "MOMENT_SECOND",

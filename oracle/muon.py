@@ -22,6 +22,10 @@ the design notes):
     with eps 0, and its per-iteration coefficients a schedule of (a, b, c).
   * "tall" means rows > cols strictly; a square matrix is not transposed.
   * The shape scale uses the stored view's rows/cols: max(1, rows/cols)**0.5.
+    [KIMI "Why treat a matrix differently?"] names the Moonlight shape factor
+    as its trainer's default, but the formula did not survive on the page;
+    the optional shape rule SHAPE_MOONLIGHT reads it as the published
+    Moonlight rule 0.2 * sqrt(max(rows, cols)).
   * NorMuon [FLX step 3]: statistics per row of the stored view (mean over
     columns); state zero-initialised, no bias correction; the per-row factor
     is rsqrt(max(sm, normuon_eps)) (normuon_eps = 1e-10 unless the caller
@@ -52,6 +56,9 @@ CAUTIOUS_OFF = 0
 CAUTIOUS_WD = 1       # [FLX step 4]
 CAUTIOUS_UPDATE = 2   # [SPD "Cautious updates"]
 
+SHAPE_RATIO = 0       # [SPD "Muon update"]
+SHAPE_MOONLIGHT = 1   # [KIMI "Why treat a matrix differently?"], reading above
+
 
 @dataclass
 class MuonHparams:
@@ -68,6 +75,7 @@ class MuonHparams:
     plus_eps: float = NS_EPS
     cautious: int = CAUTIOUS_OFF
     normuon_eps: float = NORMUON_FLOOR
+    shape_rule: int = SHAPE_RATIO
 
 
 def momentum_nesterov(B: np.ndarray, G: np.ndarray, mu: float, nesterov: bool = True):
@@ -146,23 +154,28 @@ def muon_plus_row_col(U: np.ndarray, eps: float = NS_EPS) -> np.ndarray:
     return R / np.sqrt(np.sum(R * R, axis=0) + eps)[None, :]
 
 
-def shape_scale(rows: int, cols: int) -> float:
-    """[SPD "Muon update"]: max(1, rows/cols)^0.5 of the stored view."""
+def shape_scale(rows: int, cols: int, rule: int = SHAPE_RATIO) -> float:
+    """[SPD "Muon update"]: max(1, rows/cols)^0.5 of the stored view; with
+    SHAPE_MOONLIGHT, 0.2 * max(rows, cols)^0.5."""
+    if rule == SHAPE_MOONLIGHT:
+        return 0.2 * max(rows, cols) ** 0.5
+    if rule != SHAPE_RATIO:
+        raise ValueError(f"unknown shape rule {rule}")
     return max(1.0, rows / cols) ** 0.5
 
 
 def muon_apply(W: np.ndarray, U: np.ndarray, G: np.ndarray, lr: float, wd: float,
-               cautious: int = CAUTIOUS_OFF) -> np.ndarray:
+               cautious: int = CAUTIOUS_OFF, shape_rule: int = SHAPE_RATIO) -> np.ndarray:
     """Parameter update of one view, fp64.
 
-    Plain [SPD]: W <- (1 - lr*wd) W - lr * s * U, s = max(1, rows/cols)^0.5.
+    Plain [SPD]: W <- (1 - lr*wd) W - lr * s * U, s = shape_scale(rows, cols, shape_rule).
     Cautious mode 1 [FLX step 4], with g = s*U the update direction:
         mask = (g * W >= 0);  W <- W - lr * (g + wd * W * mask).
     Cautious mode 2 [SPD "Cautious updates"], the observed update of the plain
     rule being delta = lr*wd*W + lr*s*U:
         mask = (delta * G > 0);  W <- W - mask * delta.
     """
-    s = shape_scale(W.shape[0], W.shape[1])
+    s = shape_scale(W.shape[0], W.shape[1], shape_rule)
     if cautious == CAUTIOUS_OFF:
         return (1.0 - lr * wd) * W - lr * s * U
     if cautious == CAUTIOUS_WD:
@@ -212,7 +225,7 @@ def muon_step_view(W, G, B, hp: MuonHparams, lr_mult: float = 1.0, wd: float = 0
     if hp.muon_plus:
         U = muon_plus_row_col(U, hp.plus_eps)
     lr = hp.lr * lr_mult
-    W_new = muon_apply(W, U, G, lr, wd, hp.cautious)
+    W_new = muon_apply(W, U, G, lr, wd, hp.cautious, hp.shape_rule)
     return ViewResult(W=W_new, B=B_new, U=U, sm=sm_new)
 
 

@@ -30,7 +30,8 @@ def oracle_hparams(wl: W.Workload) -> oracle.MuonHparams:
                               muon_plus=hp.get("muon_plus", False),
                               plus_eps=hp.get("plus_eps", hp["eps"]),
                               cautious=hp.get("cautious", 0),
-                              normuon_eps=hp.get("normuon_eps", oracle.NORMUON_FLOOR))
+                              normuon_eps=hp.get("normuon_eps", oracle.NORMUON_FLOOR),
+                              shape_rule=hp.get("shape_rule", oracle.SHAPE_RATIO))
 
 
 def oracle_muon_tensor(wl: W.Workload, i: int, steps: int, views=None, keep_unrounded=False):
@@ -98,7 +99,8 @@ class DeviceRun:
                                   muon_plus=hp.get("muon_plus", False),
                                   plus_eps=hp.get("plus_eps", hp["eps"]),
                                   cautious=hp.get("cautious", 0),
-                                  normuon_eps=hp.get("normuon_eps", oracle.NORMUON_FLOOR))
+                                  normuon_eps=hp.get("normuon_eps", oracle.NORMUON_FLOOR),
+                                  shape_rule=hp.get("shape_rule", 0))
         self.mW = [W.device_tensor(wl, W.KIND_W, i, device=device) for i in range(len(wl.muon))]
         self.mG = [W.device_tensor(wl, W.KIND_G, i, 0, device=device) for i in range(len(wl.muon))]
         self.mB = [torch.zeros(s.shape, dtype=torch.float32, device=device) for s in wl.muon]

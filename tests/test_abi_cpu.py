@@ -57,7 +57,8 @@ def test_struct_layout_matches_header(tmp_path):
         " offsetof(mh_muon_hparams, sr_seed), offsetof(mh_muon_hparams, coeff_schedule),"
         " offsetof(mh_muon_hparams, norm_scale), offsetof(mh_muon_tensor, skip_zero_grad),"
         " offsetof(mh_muon_hparams, param_fence), offsetof(mh_muon_hparams, phase),"
-        " offsetof(mh_muon_hparams, normuon_eps));"
+        " offsetof(mh_muon_hparams, normuon_eps)); printf(\"%zu\\n\","
+        " offsetof(mh_muon_hparams, shape_rule));"
         " return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -73,7 +74,7 @@ def test_struct_layout_matches_header(tmp_path):
             mh.MuonHparams.sr_seed.offset, mh.MuonHparams.coeff_schedule.offset,
             mh.MuonHparams.norm_scale.offset, mh.MuonTensor.skip_zero_grad.offset,
             mh.MuonHparams.param_fence.offset, mh.MuonHparams.phase.offset,
-            mh.MuonHparams.normuon_eps.offset]
+            mh.MuonHparams.normuon_eps.offset, mh.MuonHparams.shape_rule.offset]
     assert got == want
 
 
@@ -117,6 +118,13 @@ def test_muon_rejects_bad_tensor(kw, code):
                                 dict(normuon_eps=-1.0), dict(normuon_eps=float("inf"))])
 def test_muon_rejects_bad_hparams(kw):
     assert _step([_tensor()], hp=mh.make_hparams(**kw)) == _lib.MH_EINVAL
+
+
+@pytest.mark.parametrize("rule", [-1, 2])
+def test_muon_rejects_bad_shape_rule(rule):
+    hp = mh.make_hparams(shape_rule=rule)
+    assert _step([_tensor()], hp=hp) == _lib.MH_EINVAL
+    assert "shape_rule" in mh.last_error()
 
 
 @pytest.mark.parametrize("phase", [-1, 3])

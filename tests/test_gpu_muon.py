@@ -103,7 +103,8 @@ def test_plain_step_mixed_shapes():
 @pytest.mark.parametrize("flags", [dict(normuon=True), dict(muon_plus=True), dict(cautious=1),
                                    dict(cautious=2), dict(nesterov=False),
                                    dict(normuon=True, muon_plus=True, cautious=1),
-                                   dict(normuon=True, normuon_eps=1e-4)])
+                                   dict(normuon=True, normuon_eps=1e-4),
+                                   dict(shape_rule=1), dict(normuon=True, shape_rule=1, cautious=1)])
 def test_variants(flags):
     specs = [W.MuonSpec("a", 2, 256, 512, "f32", "f32", w_std=1.0, g_std=1.0),
              W.MuonSpec("b", 1, 384, 128, "bf16", "bf16"),

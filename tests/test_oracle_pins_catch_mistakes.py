@@ -213,7 +213,8 @@ def test_momentum_mistakes_are_caught(monkeypatch, mistake):
 # ---- shape scale and the update -------------------------------------------------------
 
 def test_inverted_shape_scale_is_caught(monkeypatch):
-    _plant(monkeypatch, "shape_scale", lambda rows, cols: max(1.0, cols / rows) ** 0.5, o_muon)
+    _plant(monkeypatch, "shape_scale", lambda rows, cols, rule=0: max(1.0, cols / rows) ** 0.5,
+           o_muon)
     pins = [(f"golden {c['rows']}x{c['cols']}", lambda c=c: up_pins.test_shape_scale(c))
             for c in up_pins.GOLD["shape_scale_cases"]]
     assert _failing(pins + APPLY_PINS)
@@ -460,3 +461,16 @@ def test_muon_plus_before_normuon_is_caught(monkeypatch):
         return o_muon.ViewResult(W=W_new, B=B_new, U=U, sm=sm_new)
     _plant(monkeypatch, "muon_step_view", step, o_muon)
     assert _failing([("step composes its pieces", up_pins.test_full_view_step_composes_pieces)])
+
+
+def test_moonlight_factor_on_the_short_side_is_caught(monkeypatch):
+    real = o_muon.shape_scale
+
+    def scale(rows, cols, rule=0):
+        if rule == oracle.SHAPE_MOONLIGHT:
+            return 0.2 * min(rows, cols) ** 0.5
+        return real(rows, cols, rule)
+    _plant(monkeypatch, "shape_scale", scale, o_muon)
+    pins = [(f"Moonlight RMS {s}", lambda s=s: up_pins.test_moonlight_shape_factor_gives_update_rms_0_2(s))
+            for s in [(64, 64), (48, 200), (200, 48)]]
+    assert _failing(pins)

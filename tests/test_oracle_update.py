@@ -50,6 +50,27 @@ def test_shape_scale(case):
     assert oracle.shape_scale(case["rows"], case["cols"]) == pytest.approx(case["scale"], rel=1e-15)
 
 
+@pytest.mark.parametrize("shape", [(64, 64), (48, 200), (200, 48), (1, 9), (9, 1)])
+def test_moonlight_shape_factor_gives_update_rms_0_2(shape):
+    """kimi-k3 "Why treat a matrix differently?": the Moonlight shape factor,
+    read as Moonlight's published rule, scales an update whose singular
+    values are all one (full rank) to an RMS of 0.2 for any shape. U is built
+    by QR here, independently of the Newton-Schulz oracle."""
+    r, c = shape
+    rng = np.random.default_rng(r * 1000 + c)
+    Qm, _ = np.linalg.qr(rng.standard_normal((max(r, c), min(r, c))))
+    U = Qm if r >= c else Qm.T
+    W = np.zeros(shape)
+    lr = 0.5
+    out = oracle.muon_apply(W, U, U, lr, 0.0, shape_rule=oracle.SHAPE_MOONLIGHT)
+    rms = np.sqrt(np.mean((out / lr) ** 2))
+    assert rms == pytest.approx(0.2, rel=1e-12)
+    # the ratio rule instead gives RMS max(1, r/c)^0.5 / sqrt(max(r, c))
+    out = oracle.muon_apply(W, U, U, lr, 0.0)
+    assert np.sqrt(np.mean((out / lr) ** 2)) == pytest.approx(
+        max(1.0, r / c) ** 0.5 / max(r, c) ** 0.5, rel=1e-12)
+
+
 def test_apply_zero_update_is_pure_decay():
     W = _n(2, 1, (6, 4))
     out = oracle.muon_apply(W, np.zeros_like(W), np.zeros_like(W), lr=0.02, wd=0.01)
