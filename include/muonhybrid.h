@@ -16,7 +16,8 @@
  *                         (one (a, b, c) for every iteration, or a schedule)
  *       U <- X^T if rows > cols else X
  *       [NorMuon per-row second moment]  [Muon+ row_col]
- *       W <- (1 - lr*wd) W - lr * max(1, rows/cols)^0.5 * U   (or a cautious form)
+ *       W <- (1 - lr*wd) W - lr * s * U   (or a cautious form), s = max(1, rows/cols)^0.5
+ *                                          (or the Moonlight factor: MH_SHAPE_*)
  *
  *   AdamW for everything else (dew.training.optim "OPTIMIZER_MAP" names
  *   optax.adamw; Speedtronic "CPU/CUDA/MPS behavior" names PyTorch's fused
