@@ -19,9 +19,10 @@ host buffers (gradients copied in from pinned memory and updated parameters
 copied back every step), the SM clocks sampled during the timed region, and
 the fp64 CPU oracle timed on a bounded sample of the same workload.
 
-Under torchrun with N > 1 every rank runs an independent replica of the
-workload (the step has no exchange between GPUs); the time is the maximum
-over ranks.
+Every call of the library uses one GPU. The Newton-Schulz GEMM loads its
+operands with cluster-multicast TMA copies, which only one-GPU processes may
+run, so --gpus N > 1 (or a torchrun launch with WORLD_SIZE > 1) prints one
+"unavailable" line from rank 0 and exits 0 without touching a GPU.
 
 --impl reference times the oracle (the plain fp64 CPU statement of the
 method) on the host cores instead, each step a bounded sample of the same
@@ -183,37 +184,29 @@ class ClockSampler:
                 "power_w_max": pmax}
 
 
-# ---- distributed plumbing ------------------------------------------------------------
+# ---- one GPU only -------------------------------------------------------------------
 
-def dist_setup(args):
+SINGLE_GPU_REASON = "single-GPU build: the NS GEMM uses cluster-multicast TMA loads"
+
+
+def multi_gpu_request(args) -> bool:
+    """True when the run asks for more than one GPU: --gpus N > 1 or a launch
+    with WORLD_SIZE > 1."""
+    return args.gpus > 1 or int(os.environ.get("WORLD_SIZE", "1")) > 1
+
+
+def refuse_multi_gpu(args) -> int:
+    """Prints the one "unavailable" line (rank 0 only) and launches nothing."""
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps({"impl": args.impl, "metric": METRIC, "n_gpus": max(args.gpus, int(
+            os.environ.get("WORLD_SIZE", "1"))), "unavailable": SINGLE_GPU_REASON}), flush=True)
+    return 0
+
+
+def gpu_setup():
     import torch
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    return world, rank, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
-    """The slowest rank's value (NCCL needs a CUDA tensor; gloo takes a CPU one)."""
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    torch.cuda.set_device(0)
+    return torch.device("cuda", 0)
 
 
 # ---- workload on the device -------------------------------------------------------------
@@ -725,9 +718,7 @@ def sample_desc(wl, views, adam):
 # ---- main ---------------------------------------------------------------------------------
 
 def run_reference(args, wl):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if int(os.environ.get("RANK", "0")) != 0:
         return 0
     # One bounded sample per step: about a second of CPU work.
     views, adam = oracle_sample_plan(wl, muon_flop_budget=2.0e11, adam_elems=1 << 22)
@@ -743,9 +734,9 @@ def run_reference(args, wl):
     cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms/step",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_dict(wl, world, args.max_grad_norm),
+        "data": "synthetic", "config": config_dict(wl, args.max_grad_norm),
         "cpu_baseline": {"value": round(ms, 3), "unit": "ms/step", "cores": cores,
                          "kind": "oracle", "sample": sample_desc(wl, views, adam)},
         "e2e": {"value": round(ms, 3), "unit": "ms/step", "h2d_bytes_per_step": 0,
@@ -755,7 +746,7 @@ def run_reference(args, wl):
     return 0
 
 
-def config_dict(wl, world, max_grad_norm=None):
+def config_dict(wl, max_grad_norm=None):
     extra = {} if max_grad_norm is None else {
         "grad_control": {"max_grad_norm": max_grad_norm, "inv_loss_scale": 1.0}}
     return {**{"workload": wl.name,
@@ -768,7 +759,7 @@ def config_dict(wl, world, max_grad_norm=None):
                          + ("and optimizer state; bf16 params/grads" if wl.state_dtype == "f32"
                             else "; bf16 optimizer state and bf16 params, stochastically rounded; "
                                  "bf16 grads"),
-            "parallelism": "replicas" if world > 1 else "single GPU",
+            "parallelism": "single GPU",
             "l2": "inputs larger than L2 (no flush needed)"}, **extra}
 
 
@@ -778,8 +769,7 @@ def run_ns_only(args):
     import torch
     import muon_adamw_hybrid_gb300 as mh
     from synth.gpu import fill_normal
-    world, rank, local = dist_setup(args)
-    device = torch.device("cuda", local)
+    device = gpu_setup()
     stream = torch.cuda.current_stream(device)
     peaks, peak_src = load_peaks()
     n = args.ns_n
@@ -798,32 +788,29 @@ def run_ns_only(args):
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(0)
     clocks.start()
     mh.profiler_reset()
     mh.profiler_enable(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
         call()
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     mh.profiler_enable(False)
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    ms = e0.elapsed_time(e1) / args.steps
     ks = family_stats(mh.profiler_read())
     m_, n_ = min(r, c), max(r, c)
     flops = b * 5 * (4.0 * m_ * m_ * n_ + 2.0 * m_ ** 3)
     g = ks.get("ns_gemm", {"total_ms": 0.0, "flops": 0.0, "flops_executed": 0.0, "launches": 0})
     peak = peaks["bf16_tflops"]
     ach = g["flops"] / (g["total_ms"] * 1e-3) / 1e12 if g["total_ms"] else 0.0
-    if rank == 0:
-        print(json.dumps({
+    print(json.dumps({
             "metric": "Newton-Schulz TFLOP/s (nominal 4m^2n+2m^3 per iteration)",
-            "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": world,
+            "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
@@ -921,6 +908,8 @@ def launch_floor_us(stream, n: int = 2000) -> float:
 def main():
     args = parse_args()
     from synth import workloads as W
+    if args.impl == "ours" and multi_gpu_request(args):
+        return refuse_multi_gpu(args)
     if args.workload == "ns":
         return run_ns_only(args)
     if args.workload == "ns_sweep":
@@ -934,8 +923,7 @@ def main():
     import torch
     import muon_adamw_hybrid_gb300 as mh
 
-    world, rank, local = dist_setup(args)
-    device = torch.device("cuda", local)
+    device = gpu_setup()
     stream = torch.cuda.current_stream(device)
     peaks, peak_src = load_peaks()
 
@@ -947,23 +935,21 @@ def main():
     dw.check_status(stream)
 
     # ---- timed region: K device-resident steps --------------------------------------
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(0)
     clocks.start()
     mh.profiler_reset()
     mh.profiler_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
     torch.cuda.synchronize()
     ev0.record(stream)
     for _ in range(args.steps):
         dw.step(stream)
     ev1.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     mh.profiler_enable(False)
     clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
-    ms_step = max_over_ranks(ms_total / args.steps, world)
+    ms_step = ms_total / args.steps
     stage_stats = mh.profiler_read()
     dw.check_status(stream)
     kstats = family_stats(stage_stats)
@@ -1051,7 +1037,6 @@ def main():
         run_step()                          # warm-up step and its copy-out
         pipe.finish(stream)
         torch.cuda.synchronize()
-        barrier(world)
         pipe.timed = True
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         for k in range(args.steps):
@@ -1062,8 +1047,7 @@ def main():
         pipe.finish(stream)
         end.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
-        e2e_ms = max_over_ranks(ev[0][0].elapsed_time(end) / args.steps, world)
+        e2e_ms = ev[0][0].elapsed_time(end) / args.steps
         step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
         d2h_ms = statistics.mean(c[0].elapsed_time(c[1]) for c in pipe.copies)
         e2e = {"value": round(e2e_ms, 3), "unit": "ms/step", "h2d_bytes_per_step": gin.nbytes,
@@ -1085,7 +1069,7 @@ def main():
 
     # ---- CPU oracle baseline (rank 0, one GPU) -------------------------------------------
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         views, adam = oracle_sample_plan(wl, muon_flop_budget=1.2e13, adam_elems=1 << 24)
         osample = OracleSample(wl, views, adam, args.max_grad_norm)
         ms_muon, ms_adam, ms_ctl = osample.run()
@@ -1095,24 +1079,20 @@ def main():
                "kind": "oracle", "sample": sample_desc(wl, views, adam),
                "sample_seconds": round(ms_muon + ms_adam + ms_ctl, 2)}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(ms_step, 3), "unit": "ms/step", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
-            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_dict(wl, world, args.max_grad_norm),
-            "ns_tflops": round(nsf / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
-            "ns_ms_per_step": round(ns_ms, 3),
-            "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,
-            "ns_stages": stages,
-            "launch_floor": launch_floor,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
-            "resident_gb": round(dw.resident_bytes / 1e9, 1),
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    line = {
+        "metric": METRIC, "value": round(ms_step, 3), "unit": "ms/step", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(wl, args.max_grad_norm),
+        "ns_tflops": round(nsf / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
+        "ns_ms_per_step": round(ns_ms, 3),
+        "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,
+        "ns_stages": stages,
+        "launch_floor": launch_floor,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "resident_gb": round(dw.resident_bytes / 1e9, 1),
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

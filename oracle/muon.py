@@ -15,8 +15,7 @@ Sources (page title, section):
   [KIMI] kimi-k3, "Optimization": "A tensor's storage shape can be misleading"
          (matrix views) and "Why treat a matrix differently?".
 
-Readings taken where the pages are silent or ambiguous (each also listed in
-the design notes):
+Readings taken where the pages are silent or ambiguous:
   * Frobenius normalisation is X = T / (||T||_F + eps) with eps = 1e-7 [SPD];
     flaxchat's Polar Express form X = g / (||g|| * 1.01) is norm_scale 1.01
     with eps 0, and its per-iteration coefficients a schedule of (a, b, c).

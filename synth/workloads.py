@@ -5,7 +5,7 @@ GPU side) and the benchmark so both run on the same seeded data.
 
 Shapes follow the five benchmark configurations the optimizer is measured
 on. Where the description leaves a value open, the reading used is stated
-next to it (and in the design notes):
+here:
   * parameter init std 0.02 where unstated;
   * Muon lr 0.02, wd 0.01, momentum 0.95 (Nesterov) in every configuration;
   * AdamW lr 3e-4 (the Speedtronic "Configuration" example), betas 0.9/0.95,
