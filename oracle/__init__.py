@@ -16,6 +16,7 @@ from .muon import (NS_COEFFS, NS_EPS, NS_STEPS, NORMUON_FLOOR, CAUTIOUS_OFF, CAU
                    muon_step_tensor, muon_step_view, newton_schulz, normuon, shape_scale)
 from .adamw import adamw_step
 from .bf16 import round_bf16
+from .ns_bf16 import newton_schulz_stored, round_to_bits
 from .grad_control import CLIP_EPS, GradControl, grad_control
 from .qk_clip import ClipEntry, gamma, qk_clip
 from .stochastic_round import (MOMENT_FIRST, MOMENT_PARAM, MOMENT_SECOND, round_bf16_with_noise,
@@ -25,7 +26,8 @@ __all__ = [
     "NS_COEFFS", "NS_EPS", "NS_STEPS", "NORMUON_FLOOR", "CAUTIOUS_OFF", "CAUTIOUS_UPDATE",
     "CAUTIOUS_WD", "SHAPE_MOONLIGHT", "SHAPE_RATIO",
     "MuonHparams", "momentum_nesterov", "muon_apply", "muon_plus_row_col", "muon_step_tensor",
-    "muon_step_view", "newton_schulz", "normuon", "shape_scale", "adamw_step", "round_bf16",
+    "muon_step_view", "newton_schulz", "newton_schulz_stored", "normuon", "round_to_bits",
+    "shape_scale", "adamw_step", "round_bf16",
     "CLIP_EPS", "GradControl", "grad_control", "MOMENT_FIRST", "MOMENT_PARAM", "MOMENT_SECOND",
     "round_bf16_with_noise", "fmix32", "sr_key", "sr_noise16", "sr_stream",
     "stochastic_round_bf16", "ClipEntry", "gamma", "qk_clip",

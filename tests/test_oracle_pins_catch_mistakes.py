@@ -23,12 +23,14 @@ o_adamw = importlib.import_module("oracle.adamw")
 o_bf16 = importlib.import_module("oracle.bf16")
 o_gc = importlib.import_module("oracle.grad_control")
 o_muon = importlib.import_module("oracle.muon")
+o_nsb = importlib.import_module("oracle.ns_bf16")
 o_qk = importlib.import_module("oracle.qk_clip")
 o_sr = importlib.import_module("oracle.stochastic_round")
 from tests import test_oracle_adamw as adam_pins
 from tests import test_oracle_bf16 as bf16_pins
 from tests import test_oracle_grad_control as gc_pins
 from tests import test_oracle_ns as ns_pins
+from tests import test_oracle_ns_bf16 as nsb_pins
 from tests import test_oracle_qk_clip as qk_pins
 from tests import test_oracle_sr as sr_pins
 from tests import test_oracle_update as up_pins
@@ -137,9 +139,23 @@ BF16_PINS = [
 ]
 
 
+NS_STORED_PINS = [
+    ("rounding off is the fp64 oracle", lambda: nsb_pins.test_rounding_off_is_the_fp64_oracle_bit_for_bit((33, 97))),
+    ("rounding off, tall", lambda: nsb_pins.test_rounding_off_is_the_fp64_oracle_bit_for_bit((48, 16))),
+    ("folded normalisation", lambda: nsb_pins.test_folded_normalisation_is_the_same_iteration((24, 40))),
+    ("stored matrices are bf16", lambda: nsb_pins.test_stored_matrices_are_bf16_and_only_those(False)),
+    ("stored matrices are bf16, folded", lambda: nsb_pins.test_stored_matrices_are_bf16_and_only_those(True)),
+    ("copy stage", nsb_pins.test_copy_stage_moves_each_entry_by_half_a_spacing_at_most),
+]
+NS_STORED_SQUARE_PINS = [
+    ("rounding off, square", lambda: nsb_pins.test_rounding_off_is_the_fp64_oracle_bit_for_bit((64, 64))),
+    ("folded normalisation, square", lambda: nsb_pins.test_folded_normalisation_is_the_same_iteration((32, 32))),
+]
+
+
 def test_every_pin_passes_on_the_real_oracle():
     every = (NS_PINS + MOMENTUM_PINS + APPLY_PINS + NORMUON_PINS + ADAMW_PINS + GC_PINS + QK_PINS
-             + SR_PINS + VIEW_PINS + BF16_PINS)
+             + SR_PINS + VIEW_PINS + BF16_PINS + NS_STORED_PINS + NS_STORED_SQUARE_PINS)
     assert _failing(every) == []
 
 
@@ -184,6 +200,53 @@ def test_newton_schulz_mistakes_are_caught(monkeypatch, mistake):
 def test_newton_schulz_operand_order_mistakes_are_caught(monkeypatch, mistake):
     _plant(monkeypatch, "newton_schulz", _ns_with(mistake), o_muon)
     assert _failing(NS_SQUARE_PINS), mistake
+
+
+# ---- Newton-Schulz with bf16 storage (the error model) ----------------------------
+
+def _ns_stored_with(mistake):
+    def ns(Q, steps=oracle.NS_STEPS, coeffs=oracle.NS_COEFFS, eps=oracle.NS_EPS, norm_scale=1.0,
+           round_fn=oracle.round_bf16, fold_norm=False, trace=None):
+        sched = o_muon.coeff_schedule(coeffs, steps)
+        Q = np.asarray(Q, dtype=np.float64)
+        tall = Q.shape[0] > Q.shape[1]
+        T = Q.T if tall else Q
+        den = np.sqrt(np.sum(T * T)) * norm_scale + eps
+        s = 1.0 / den if den > 0 else 0.0
+        X = round_fn(T) if fold_norm else round_fn(T / den if den > 0 else np.zeros_like(T))
+        if trace:
+            trace("X", 0, X)
+        for k, (a, b, c) in enumerate(sched):
+            first = fold_norm and k == 0
+            sa = s if mistake == "fold scales A by s" else s * s
+            G = X.T @ X if mistake == "gram transposed" else X @ X.T
+            A = round_fn(sa * G if first else G)
+            if trace:
+                trace("A", k, A)
+            P = b * A + c * (A @ A)
+            if mistake != "P not rounded":
+                P = round_fn(P)
+            if trace:
+                trace("P", k, P)
+            X = s * (a * X + P @ X) if first else a * X + P @ X
+            if k + 1 < len(sched) or mistake == "last X rounded":
+                X = round_fn(X)
+                if trace and k + 1 < len(sched):
+                    trace("X", k + 1, X)
+        return X.T.copy() if tall else X
+    return ns
+
+
+@pytest.mark.parametrize("mistake", ["fold scales A by s", "P not rounded", "last X rounded"])
+def test_stored_newton_schulz_mistakes_are_caught(monkeypatch, mistake):
+    _plant(monkeypatch, "newton_schulz_stored", _ns_stored_with(mistake), o_nsb, nsb_pins)
+    assert _failing(NS_STORED_PINS), mistake
+
+
+def test_stored_newton_schulz_operand_order_mistake_is_caught(monkeypatch):
+    _plant(monkeypatch, "newton_schulz_stored", _ns_stored_with("gram transposed"), o_nsb,
+           nsb_pins)
+    assert _failing(NS_STORED_SQUARE_PINS)
 
 
 # ---- momentum and Nesterov ----------------------------------------------------------
