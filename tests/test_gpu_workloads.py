@@ -3,9 +3,15 @@ one mh_muon_step_batched call, every AdamW tensor in one mh_adamw_step call),
 checked against the fp64 oracle on sampled views and slices that the oracle
 can compute one by one (each view's update is independent of the others).
 
-Bars as in test_gpu_muon.py: momentum and AdamW state 1e-6; final parameter
-max(1e-3, 2e-2*||dW||/||W||, twice the oracle's own bf16 rounding); NorMuon
-state 3e-2.
+Bars as in test_gpu_muon.py and test_gpu_adamw.py (tests.parity): momentum,
+AdamW moments and fp32 AdamW parameters element by element against the
+running bound on the kernels' fp32 rounding; parameters after a Muon step by
+the update they received (fp32: the Newton-Schulz bar; bf16: one spacing
+from the oracle's rounded value, the flip rate and the update error the
+Newton-Schulz bar predicts through the rounding, no systematic scale error);
+NorMuon state 3e-2. The ten-step 124M run is checked on its last step from
+the device's own state before it, on the momentum over all ten steps, and on
+the parameter's drift over the run.
 """
 import gc
 
@@ -14,7 +20,10 @@ import pytest
 
 import oracle
 from synth import workloads as W
-from tests.helpers import DeviceRun, oracle_adam_tensor, oracle_muon_tensor, rel_fro, to_np
+from tests.helpers import (DeviceRun, check_adam_result, check_muon_views, oracle_adam_step_from,
+                           oracle_adam_tensor, oracle_muon_step_from, oracle_muon_tensor, rel_fro,
+                           to_np)
+from tests.parity import check_fp32, record
 
 pytestmark = pytest.mark.gpu
 
@@ -26,46 +35,49 @@ def _free(run):
     torch.cuda.empty_cache()
 
 
-def _param_tol(w64, w0, dtype, decay, steps):
-    """max(1e-3, the NS bar carried through the total update, the bf16
-    rounding floor); over several steps the independent per-step roundings of
-    the two runs add like a random walk, hence sqrt(steps)."""
-    tol = 1e-3
-    dw = w64 - decay ** steps * w0
-    tol = max(tol, 2e-2 * np.linalg.norm(dw) / np.linalg.norm(w64))
+def _device_views(run, i, views):
+    spec = run.wl.muon[i]
+    shape = (spec.views, spec.rows, spec.cols)
+    w = to_np(run.mW[i]).reshape(shape)[views]
+    b = to_np(run.mB[i]).reshape(shape)[views]
+    sm = None if run.sm[i] is None else to_np(run.sm[i]).reshape(spec.views, spec.rows)[views]
+    return w, b, sm
+
+
+def _check_muon_views(wl, run, i, views, sm_bar=3e-2):
+    """One step from the workload's initial state."""
+    ref = oracle_muon_tensor(wl, i, 1, views=views)
+    w, b, sm = _device_views(run, i, views)
+    check_muon_views(wl, i, ref, w, b, sm, sm_bar=sm_bar)
+
+
+def _drift_tol(w64, w0, dtype, decay, steps):
+    """Bar on a parameter's distance from the oracle's after ``steps`` steps
+    run independently on both sides: max(1e-3, the Newton-Schulz bar carried
+    through the total update, and for bf16 twice the oracle's own rounding
+    error times sqrt(steps)). Each step's roundings can land one spacing
+    apart on the two sides (the flip rate the one-step checks measure), and
+    a plain Muon or AdamW update does not depend on the weight, so those
+    differences persist and add up like a random walk."""
+    tol = max(1e-3, 2e-2 * np.linalg.norm(w64 - decay ** steps * w0) / np.linalg.norm(w64))
     if dtype == "bf16":
         tol = max(tol, 2.0 * np.sqrt(steps) * rel_fro(oracle.round_bf16(w64), w64))
     return tol
 
 
-def _check_muon_views(wl, run, i, views, steps):
-    spec = wl.muon[i]
-    r, c = spec.rows, spec.cols
-    ref = oracle_muon_tensor(wl, i, steps, views=views)
-    got_w = to_np(run.mW[i]).reshape(spec.views, r, c)
-    got_b = to_np(run.mB[i]).reshape(spec.views, r, c)
-    decay = 1 - wl.muon_hp["lr"] * spec.lr_mult * spec.wd
-    for k, v in enumerate(views):
-        assert rel_fro(got_b[v], ref["B"][k]) < 1e-6, (spec.name, v)
-        w0 = W.host_tensor(wl, W.KIND_W, i, offset=v * r * c, count=r * c).reshape(r, c)
-        tol = _param_tol(ref["W64"][k], w0, spec.param_dtype, decay, steps)
-        err = rel_fro(got_w[v], ref["W"][k])
-        assert err < tol, (spec.name, v, err, tol)
-        if run.sm[i] is not None:
-            got_sm = to_np(run.sm[i]).reshape(spec.views, r)
-            assert rel_fro(got_sm[v], ref["sm"][k]) < 3e-2, (spec.name, v)
+def _adam_slice(run, j, offset, n):
+    sl = slice(offset, offset + n)
+    return (to_np(run.aW[j].reshape(-1)[sl]), to_np(run.am[j].reshape(-1)[sl]),
+            to_np(run.av[j].reshape(-1)[sl]))
 
 
 def _check_adam(wl, run, j, steps, offset=0, count=None):
+    """A slice of AdamW tensor j after ``steps`` steps from the initial state."""
     spec = wl.adamw[j]
     n = spec.numel if count is None else count
     ref = oracle_adam_tensor(wl, j, steps, offset=offset, count=n)
-    sl = slice(offset, offset + n)
-    got_w = to_np(run.aW[j].reshape(-1)[sl])
-    assert rel_fro(to_np(run.am[j].reshape(-1)[sl]), ref["m"]) < 1e-6
-    assert rel_fro(to_np(run.av[j].reshape(-1)[sl]), ref["v"]) < 1e-6
-    tol = 1e-6 if spec.param_dtype == "f32" else 1e-3
-    assert rel_fro(got_w, ref["W"]) < tol, (spec.name, rel_fro(got_w, ref["W"]))
+    check_adam_result(*_adam_slice(run, j, offset, n), ref, spec.param_dtype,
+                      f"{wl.name}:{spec.name}[{offset}:{offset + n}]", steps=steps)
 
 
 def _index(wl, name):
@@ -77,10 +89,10 @@ def test_llama7b_one_step_sampled():
     run = DeviceRun(wl)
     run.step()
     run.status_ok()
-    _check_muon_views(wl, run, _index(wl, "l0.q"), [0], 1)
-    _check_muon_views(wl, run, _index(wl, "l0.k"), [0], 1)
-    _check_muon_views(wl, run, _index(wl, "l31.gate_up"), [1], 1)
-    _check_muon_views(wl, run, _index(wl, "l31.down"), [0], 1)
+    _check_muon_views(wl, run, _index(wl, "l0.q"), [0])
+    _check_muon_views(wl, run, _index(wl, "l0.k"), [0])
+    _check_muon_views(wl, run, _index(wl, "l31.gate_up"), [1])
+    _check_muon_views(wl, run, _index(wl, "l31.down"), [0])
     # AdamW: a 4096-row slice of the embedding and of the head, and a norm.
     _check_adam(wl, run, 0, 1, offset=0, count=4096 * 4096)
     _check_adam(wl, run, 1, 1, offset=124160 * 4096, count=4096 * 4096)
@@ -91,15 +103,41 @@ def test_llama7b_one_step_sampled():
 def test_gpt124m_ten_steps_sampled():
     wl = W.gpt124m()
     run = DeviceRun(wl)
-    for _ in range(wl.steps):
+    sample = (("l0.q", [0]), ("l0.gate_up", [0, 1]), ("l0.down", [0]), ("l11.v", [0]),
+              ("l11.gate_up", [1]))
+    adam_sample = ((0, 0, 1 << 20), (0, 50304 * 768 - (1 << 20), 1 << 20), (5, 0, 768))
+    for _ in range(wl.steps - 1):
         run.step()
+    before = {name: _device_views(run, _index(wl, name), views) for name, views in sample}
+    before_adam = {a: _adam_slice(run, *a) for a in adam_sample}
+    run.step()
     run.status_ok()
-    for name, views in (("l0.q", [0]), ("l0.gate_up", [0, 1]), ("l0.down", [0]),
-                        ("l11.v", [0]), ("l11.gate_up", [1])):
-        _check_muon_views(wl, run, _index(wl, name), views, wl.steps)
-    _check_adam(wl, run, 0, wl.steps, offset=0, count=1 << 20)
-    _check_adam(wl, run, 0, wl.steps, offset=50304 * 768 - (1 << 20), count=1 << 20)
-    _check_adam(wl, run, 5, wl.steps)
+    for name, views in sample:
+        i = _index(wl, name)
+        spec = wl.muon[i]
+        w0, b0, sm0 = before[name]
+        # the last step, from the device's own state before it
+        ref = oracle_muon_step_from(wl, i, wl.steps - 1, views, w0, b0, sm0)
+        w, b, sm = _device_views(run, i, views)
+        check_muon_views(wl, i, ref, w, b, sm, what=f"{wl.name} step {wl.steps}")
+        # the whole run: momentum element by element, the parameter's drift
+        traj = oracle_muon_tensor(wl, i, wl.steps, views=views)
+        decay = 1 - wl.muon_hp["lr"] * spec.lr_mult * spec.wd
+        r, c = spec.rows, spec.cols
+        for k, v in enumerate(views):
+            check_fp32(b[k], traj["B"][k], traj["B_atol"][k],
+                       f"{wl.name}:{name}[{v}] momentum over {wl.steps} steps")
+            w_init = W.host_tensor(wl, W.KIND_W, i, offset=v * r * c, count=r * c).reshape(r, c)
+            tol = _drift_tol(traj["W64"][k], w_init, spec.param_dtype, decay, wl.steps)
+            err = rel_fro(w[k], traj["W"][k])
+            record("drift", f"{wl.name}:{name}[{v}] over {wl.steps} steps", w_rel=err, bar=tol)
+            assert err < tol, (name, v, err, tol)
+    for j, off, n in adam_sample:
+        # the last step from the device's own state, then the whole run
+        ref = oracle_adam_step_from(wl, j, wl.steps - 1, off, n, *before_adam[(j, off, n)])
+        check_adam_result(*_adam_slice(run, j, off, n), ref, wl.adamw[j].param_dtype,
+                          f"{wl.name}:{wl.adamw[j].name}[{off}:{off + n}] step {wl.steps}")
+        _check_adam(wl, run, j, wl.steps, offset=off, count=n)
     _free(run)
 
 
@@ -108,10 +146,10 @@ def test_moe_mla_all_variants_sampled():
     run = DeviceRun(wl)
     run.step()
     run.status_ok()
-    _check_muon_views(wl, run, _index(wl, "e0.gate_up"), [0, 1], 1)
-    _check_muon_views(wl, run, _index(wl, "e0.down"), [0], 1)
-    _check_muon_views(wl, run, _index(wl, "e63.down"), [0], 1)
-    _check_muon_views(wl, run, _index(wl, "mla.kv_b"), list(range(64)), 1)
+    _check_muon_views(wl, run, _index(wl, "e0.gate_up"), [0, 1])
+    _check_muon_views(wl, run, _index(wl, "e0.down"), [0])
+    _check_muon_views(wl, run, _index(wl, "e63.down"), [0])
+    _check_muon_views(wl, run, _index(wl, "mla.kv_b"), list(range(64)))
     _free(run)
 
 
@@ -120,7 +158,7 @@ def test_single_matrix_config():
     run = DeviceRun(wl)
     run.step()
     run.status_ok()
-    _check_muon_views(wl, run, 0, [0], 1)
+    _check_muon_views(wl, run, 0, [0])
     _free(run)
 
 
