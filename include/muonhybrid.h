@@ -243,8 +243,9 @@ int mh_newton_schulz_batched_ex(const mh_ns_problem* problems, int32_t n, int32_
  *     every other byte is written before use). Calls whose GPU work overlaps,
  *     e.g. on two unordered streams, race on the array: serialise them.
  *   - The first call on each device looks up the array's device address
- *     with that device current; make that first call before any stream
- *     capture on the device. */
+ *     with that device current, and so does the first call after the
+ *     device's context was destroyed (cudaDeviceReset); make that first call
+ *     before any stream capture on the device. */
 int mh_newton_schulz_batched_noalloc(const mh_ns_problem* problems, int32_t n, int32_t steps,
                                      float a, float b, float c, float eps, void* stream);
 

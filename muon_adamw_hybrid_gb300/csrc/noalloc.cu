@@ -19,13 +19,15 @@
 //     call's contents. Calls whose work overlaps on the GPU (for example on
 //     two streams without ordering between them) race on it and give wrong
 //     results: order them on one stream or with events.
-//   - The first call on each device looks up the array's device address with
-//     that device current (cudaGetSymbolAddress). Make that first call before
-//     starting any stream capture on the device.
+//   - The first call on each device (and again after the device's context
+//     was destroyed, e.g. by cudaDeviceReset) looks up the array's device
+//     address with that device current (cudaGetSymbolAddress). Make that
+//     first call before starting any stream capture on the device.
 #include <cstdio>
 #include <map>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mh_internal.h"
@@ -40,11 +42,39 @@ constexpr size_t kStaticScratchBytes = MH_NS_STATIC_SCRATCH_BYTES;
 // looked up per device with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_ns_scratch[kStaticScratchBytes];
 
-// Device address of g_ns_scratch on the current device, looked up once per
-// device. Returns nullptr and sets the error message on failure.
+// The driver's context calls, looked up once through the runtime (the
+// library links only the runtime).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+bool context_id(unsigned long long* id) {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+         get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_ns_scratch in the current device's context. It is
+// looked up once per device and context: the cache is keyed by the
+// context's unique id, so a context created after cudaDeviceReset (where the
+// array may sit elsewhere) gets a fresh lookup. Returns nullptr and sets the
+// error message on failure.
 void* scratch_for_current_device() {
   static std::mutex mu;
-  static std::map<int, void*> addr;
+  static std::map<std::pair<int, unsigned long long>, void*> addr;
   int dev = 0;
   char msg[256];
   cudaError_t e = cudaGetDevice(&dev);
@@ -53,9 +83,14 @@ void* scratch_for_current_device() {
     mh::set_last_error(msg);
     return nullptr;
   }
+  unsigned long long ctx = 0;
   std::lock_guard<std::mutex> lock(mu);
-  auto it = addr.find(dev);
-  if (it != addr.end()) return it->second;
+  // No context yet (the process's first CUDA call): the lookup below
+  // creates the primary context, and the address is cached under its id.
+  if (context_id(&ctx)) {
+    auto it = addr.find(std::make_pair(dev, ctx));
+    if (it != addr.end()) return it->second;
+  }
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_ns_scratch);
   if (e != cudaSuccess || p == nullptr) {
@@ -64,7 +99,8 @@ void* scratch_for_current_device() {
     mh::set_last_error(msg);
     return nullptr;
   }
-  addr[dev] = p;
+  // Without a context id the address is looked up again on the next call.
+  if (context_id(&ctx)) addr[std::make_pair(dev, ctx)] = p;
   return p;
 }
 
