@@ -26,7 +26,7 @@ EXPORTED = ("mh_muon_workspace_bytes", "mh_muon_step_batched", "mh_ns_workspace_
             "mh_version", "mh_profiler_enable", "mh_profiler_reset", "mh_profiler_read",
             "mh_newton_schulz_batched_noalloc", "mh_grad_prepare_workspace_bytes",
             "mh_grad_prepare", "mh_adamw_step_ctl", "mh_newton_schulz_batched_ex", "mh_qk_clip",
-            "mh_pointer_device_accessible")
+            "mh_pointer_device_accessible", "mh_set_wait_limit", "mh_get_wait_limit")
 NS_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -131,6 +131,10 @@ def _load() -> ctypes.CDLL:
     lib.mh_pointer_device_accessible.restype = c_int
     lib.mh_workspace_status.argtypes = [c_void_p, c_void_p]
     lib.mh_workspace_status.restype = c_int
+    lib.mh_set_wait_limit.argtypes = [c_int64]
+    lib.mh_set_wait_limit.restype = c_int
+    lib.mh_get_wait_limit.argtypes = []
+    lib.mh_get_wait_limit.restype = c_int64
     lib.mh_last_error.argtypes = []
     lib.mh_last_error.restype = c_char_p
     lib.mh_version.argtypes = []
@@ -254,6 +258,15 @@ def pointer_device_accessible(ptr: int) -> bool:
 
 def workspace_status(workspace: int, stream: int) -> None:
     _check(LIB.mh_workspace_status(workspace, stream))
+
+
+def set_wait_limit(cycles: int) -> None:
+    """Bounded-wait limit of the GEMM stages in SM cycles (0: the default)."""
+    _check(LIB.mh_set_wait_limit(int(cycles)))
+
+
+def get_wait_limit() -> int:
+    return int(LIB.mh_get_wait_limit())
 
 
 def profiler_enable(on: bool = True) -> None:

@@ -13,7 +13,8 @@
 // launch per Newton-Schulz stage covers every class.
 //
 // Workspace (256-byte aligned base):
-//   [0, 256)        device status word (bounded-wait timeouts)
+//   [0, 256)        header: device status word (bounded-wait timeouts) at 0,
+//                   the GEMM stages' block counters at kTileCounterOffset
 //   sumsq           double per view: ||Q||_F^2
 //   tile_ss         float per prologue tile and warp: partial ||Q||_F^2
 //   vrec            per view: parameter/gradient pointers, shape, lr, wd (the
@@ -30,6 +31,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -40,6 +42,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "mh_internal.h"
+#include "mh_ptx.cuh"
 #include "mh_sr.cuh"
 #include "muonhybrid.h"
 
@@ -378,21 +381,36 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
   // Global view slot of the first view of each class.
   std::vector<int64_t> class_first(nclass, 0);
   for (int k = 1; k < nclass; ++k) class_first[k] = class_first[k - 1] + P.classes[k - 1].count;
+  // Block counters of the stage launches (see kTileRing): the first two
+  // launches claim from counters zeroed here, every launch zeroes the one
+  // two launches ahead.
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + kTileCounterOffset);
+  static_assert(kTileCounterOffset + kTileCounters * sizeof(uint32_t) <= kHeaderBytes,
+                "tile counters must fit in the workspace header");
+  if (steps > 0) {
+    const cudaError_t me = cudaMemsetAsync(counters, 0, 2 * sizeof(uint32_t), stream);
+    if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(tile counters)");
+  }
+  int launch = 0;
+  const long long wait_limit = gemm_wait_limit();
 
   for (int it = 0; it < steps; ++it) {
     for (int kind = GEMM_GRAM; kind <= GEMM_APPLY; ++kind) {
-      // One launch (or more, kMaxClasses at a time) per operand mode.
-      for (int mode = 0; mode < kGemmModes; ++mode) {
+      // One launch per stage over every class (more only beyond kMaxClasses
+      // classes); each class carries its own operand mode.
+      {
         std::vector<int> ids;
-        for (int k = 0; k < nclass; ++k)
-          if (gemm_mode(kind, P.classes[k].tstore) == mode) ids.push_back(k);
+        for (int k = 0; k < nclass; ++k) ids.push_back(k);
         const int nids = static_cast<int>(ids.size());
         for (int c0 = 0; c0 < nids; c0 += kMaxClasses) {
           GemmParams gp;
           std::memset(&gp, 0, sizeof(gp));
           gp.kind = kind;
-          gp.mode = mode;
           gp.first_iter = it == 0 ? 1 : 0;
+          gp.tile_counter = counters + launch % kTileCounters;
+          gp.next_counter = counters + (launch + 2) % kTileCounters;
+          gp.wait_limit = wait_limit;
+          ++launch;
           gp.a = sched ? sched[3 * it] : a;
           gp.b = sched ? sched[3 * it + 1] : b;
           gp.c = sched ? sched[3 * it + 2] : c;
@@ -424,6 +442,7 @@ int run_ns(const Plan& P, uint8_t* ws, int steps, float a, float b, float c, flo
             G.m = static_cast<int32_t>(C.m);
             G.n = static_cast<int32_t>(C.n);
             G.tstore = C.tstore ? 1 : 0;
+            G.mode = gemm_mode(kind, C.tstore);
             G.out_rows = static_cast<int32_t>(C.tstore ? C.n : C.m);
             G.out_cols = static_cast<int32_t>(C.tstore ? C.m : C.n);
             G.views = static_cast<int32_t>(C.count);
@@ -762,6 +781,10 @@ int check_workspace(const Plan& P, const void* ws, size_t bytes) {
 }  // namespace
 
 void set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
+// Cycles a bounded wait in a GEMM stage may take (mh_set_wait_limit).
+std::atomic<long long> g_wait_limit{kWaitLimitCycles};
+long long gemm_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 }  // namespace mh
 
@@ -1406,6 +1429,15 @@ int mh_profiler_read(mh_kernel_stats* out, int32_t max, int32_t* count) {
   for (int32_t k = 0; k < max && k < static_cast<int32_t>(agg.size()); ++k) out[k] = agg[k];
   return rc;
 }
+
+int mh_set_wait_limit(int64_t cycles) {
+  if (cycles < 0) return fail(MH_EINVAL, "wait limit must be >= 0 (0 restores the default)");
+  g_wait_limit.store(cycles == 0 ? kWaitLimitCycles : static_cast<long long>(cycles),
+                     std::memory_order_relaxed);
+  return MH_OK;
+}
+
+int64_t mh_get_wait_limit(void) { return gemm_wait_limit(); }
 
 int mh_workspace_status(const void* workspace, void* stream_) {
   if (!workspace) return fail(MH_EWORKSPACE, "workspace is NULL");

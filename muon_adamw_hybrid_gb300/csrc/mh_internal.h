@@ -210,11 +210,12 @@ constexpr int kGemmThreads = 256;
 
 enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_APPLY = 2 };
 
-// Operand major-ness of one launch (A, B): K-major (K) or MN-major (M). The
-// gram of a tall view reads both operands as MN-major chunks of T; the apply
-// reads X MN-major as B, except for tall views (T P: both K-major); every
-// other stage is K-major. Each launch covers classes of one mode, so the
-// kernel is specialised on it.
+// Operand major-ness of one shape class in one stage (A, B): K-major (K) or
+// MN-major (M). The gram of a tall view reads both operands as MN-major
+// chunks of T; the apply reads X MN-major as B, except for tall views (T P:
+// both K-major); every other stage is K-major. One launch per stage covers
+// classes of every mode: the kernel selects a mode-specialised k-loop once
+// per tile.
 enum GemmMode { GEMM_MODE_KK = 0, GEMM_MODE_KM = 1, GEMM_MODE_MM = 2 };
 constexpr int kGemmModes = 3;
 inline int gemm_mode(int kind, bool tstore) {
@@ -245,14 +246,25 @@ struct GemmClass {
   int32_t views;
   int32_t tiles_m, tiles_n, tiles_per_view;  // in 256 x 256 pair blocks
   int32_t K;               // contraction length
+  int32_t mode;            // GemmMode of this class in this stage
   int64_t tile_begin;      // first global pair-block index of this class
 };
+
+// Work distribution: CTA 0 of each pair claims the next 256 x 256 block from
+// a per-launch counter in the workspace header and hands its index to both
+// CTAs' roles through a ring of kTileRing shared-memory slots. The header
+// holds kTileCounters counters; launch k of a call claims from counter
+// k mod kTileCounters and zeroes counter k + 2 for a later launch (a launch
+// reads global memory only after the launch before it has completed, so the
+// reset lands before that launch's first claim).
+constexpr int kTileRing = 4;
+constexpr int kTileCounters = 32;
+constexpr int kTileCounterOffset = 64;  // bytes into the workspace header
 
 struct GemmParams {
   GemmClass cls[kMaxClasses];
   int32_t num_classes;
   int32_t kind;            // GemmKind
-  int32_t mode;            // GemmMode shared by every class of the launch
   int32_t first_iter;      // fold the Frobenius normalisation in
   int32_t final_update;    // apply: update the parameters instead of writing X'
   int32_t row_sums;        // last apply: also write each view's partial row sums of U^2
@@ -262,7 +274,14 @@ struct GemmParams {
   float norm_scale;        // first iteration: X0 = Q / (||Q|| * norm_scale + eps)
   int* status;             // device status word (bounded-wait timeouts)
   const int32_t* skip;     // gradient control: every thread returns at once when set
+  uint32_t* tile_counter;  // this launch's block counter (zero at launch)
+  uint32_t* next_counter;  // the counter of the launch after the next one: zeroed here
+  long long wait_limit;    // cycles a bounded wait may take before the launch aborts
 };
+
+// Cycles a bounded wait in a GEMM stage may take before the launch gives up
+// (mh_set_wait_limit; default kWaitLimitCycles).
+long long gemm_wait_limit();
 
 size_t gemm_smem_bytes();
 // Launches one persistent grid of CTA pairs (clusters of two), at most one

@@ -12,9 +12,12 @@ namespace mh {
 enum : int { DEV_OK = 0, DEV_TIMEOUT_TMA = 1, DEV_TIMEOUT_MMA = 2, DEV_TIMEOUT_EPI = 3 };
 
 // A bounded wait gives up after this many SM clock cycles (about 1 s at the
-// GB300's clocks); no legitimate wait in these kernels is longer than a few
-// milliseconds.
+// GB300's clocks) unless the launch sets its own limit; no legitimate wait in
+// these kernels is longer than a few milliseconds. Draining after an abort
+// always uses kDrainLimitCycles, so that copies and MMAs already issued land
+// before a CTA leaves, however short the launch's own limit is.
 constexpr long long kWaitLimitCycles = 2000000000LL;
+constexpr long long kDrainLimitCycles = kWaitLimitCycles / 4;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,21 +56,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, with acquire semantics at cluster scope: for a phase
+// completed by an arrive from the other CTA of the cluster, after which this
+// thread reads data that CTA stored into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete. Returns false if the
-// CTA-wide abort flag is raised, or if the wait exceeds kWaitLimitCycles, in
+// CTA-wide abort flag is raised, or if the wait exceeds `limit` cycles, in
 // which case it raises the abort flag and records `code` in the status word.
+// CLUSTER: acquire at cluster scope (see mbar_try_wait_cluster).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort_flag, int* status,
-                                                  int code) {
+                                                  int code, long long limit) {
   const uint32_t addr = smem_addr(bar);
-  if (mbar_try_wait(addr, parity)) return true;
+  auto poll = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity);
+  };
+  if (poll()) return true;
   const long long t0 = clock64();
+  // The abort flag and the clock are checked every 32 unsuccessful polls, so
+  // that a waiting thread notices the phase as soon as it completes. try_wait
+  // may suspend the thread for a while on each poll, so under a limit
+  // shortened below the default they are checked after every poll instead.
+  const int polls = limit < kWaitLimitCycles ? 1 : 32;
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
+    for (int i = 0; i < polls; ++i)
+      if (poll()) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicCAS(status, DEV_OK, code);
       return false;
@@ -75,13 +105,95 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// Short bounded wait used only while draining after an abort.
+// Bounded wait used only while draining after an abort (kDrainLimitCycles).
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t addr = smem_addr(bar);
   const long long t0 = clock64();
   while (!mbar_try_wait(addr, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles / 4) return;
+    if (clock64() - t0 > kDrainLimitCycles) return;
   }
+}
+
+// Shared-memory address of the same offset as `local` in CTA `cta` of the
+// cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t cta) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote)
+               : "r"(smem_addr(local)), "r"(cta));
+  return remote;
+}
+
+// Arrives once on the mbarrier at the offset of `local_bar` in CTA `cta` of
+// the cluster, releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* local_bar, uint32_t cta) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_map(local_bar, cta))
+               : "memory");
+}
+
+// As mbar_arrive_cluster without release semantics: the arrive orders none of
+// this thread's earlier writes (it does not wait for them to be performed).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint64_t* local_bar, uint32_t cta) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_map(local_bar, cta))
+               : "memory");
+}
+
+// Arrives once on an mbarrier of this CTA without release semantics.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// Loads a 32-bit word of this CTA's shared memory with acquire semantics at
+// CTA scope: no later memory operation of this thread is performed before it.
+__device__ __forceinline__ uint32_t ld_acquire_cta_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p))
+               : "memory");
+  return v;
+}
+
+// Loads a 32-bit word of this CTA's shared memory with acquire semantics at
+// cluster scope: no later memory operation of this thread is performed before
+// it.
+__device__ __forceinline__ uint32_t ld_acquire_cluster_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p))
+               : "memory");
+  return v;
+}
+
+// Arrives once on the mbarrier at the offset of `local_bar` in CTA `cta` of
+// the cluster and adds `bytes` to the transaction count its current phase
+// waits for; relaxed: no earlier write of this thread is ordered by it.
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint64_t* local_bar, uint32_t cta,
+                                                              uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+          cluster_map(local_bar, cta)),
+      "r"(bytes)
+      : "memory");
+}
+
+// Asynchronous store of `v` to the 32-bit word at the offset of `local` in
+// CTA `cta` of the cluster (this CTA included); its completion counts 4
+// bytes of transactions on the mbarrier at the offset of `local_bar` in that
+// CTA, so a thread that sees the barrier's phase complete sees the value.
+__device__ __forceinline__ void st_async_u32(const void* local, uint32_t cta, uint32_t v,
+                                             uint64_t* local_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+          cluster_map(local, cta)),
+      "r"(v), "r"(cluster_map(local_bar, cta))
+      : "memory");
+}
+
+// Stores `v` to the 32-bit word at the offset of `local` in CTA `cta` of the
+// cluster.
+__device__ __forceinline__ void st_cluster_u32(const void* local, uint32_t cta, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_map(local, cta)), "r"(v)
+               : "memory");
 }
 
 // 3-D tiled TMA load into CTA shared memory, completing on `bar`.

@@ -31,6 +31,18 @@
 // MMAs of both CTAs have read it (the MMA completion is multicast to both
 // "empty" barriers).
 //
+// One launch per stage covers every shape class of the call, whatever its
+// operand major-ness (see GemmMode): each role picks a k-loop specialised on
+// the tile's mode once per tile, so nothing is re-read inside the k-loop.
+//
+// Blocks are handed out dynamically: CTA 0 of each pair claims the next block
+// index from a counter in the workspace and publishes it to both CTAs through
+// a small shared-memory ring, so every pair works on the block after the
+// last one claimed. All pairs therefore stay within about one wave of
+// consecutive blocks, which share the m x m operand (apply) or the row blocks
+// of X (gram, poly) in L2; a static deal let fast and slow pairs drift apart
+// by many blocks, and their operands no longer fitted in L2 together.
+//
 // Warp roles per CTA: warp 0 issues TMA loads into a 4-stage ring, warp 1
 // issues tcgen05.mma into one of two TMEM accumulators, warp 2 owns the TMEM
 // allocation, warps 4-7 drain an accumulator with tcgen05.ld (one row per
@@ -40,9 +52,10 @@
 // shared-memory boxes that one lane stores with TMA. The fused parameter
 // update of the last apply stage reads and writes the parameters directly.
 //
-// Every mbarrier wait is bounded; on timeout the CTA records a status code in
-// the workspace, raises the abort flag of both CTAs of its pair, drains what
-// it has in flight, frees TMEM and exits.
+// Every mbarrier wait is bounded (the launch's wait limit); on timeout the CTA
+// records a status code in the workspace, raises the abort flag of both CTAs
+// of its pair, drains what it has in flight (with the fixed, long drain
+// limit), frees TMEM and exits.
 #include <map>
 #include <mutex>
 
@@ -76,7 +89,6 @@ struct TileCoord {
 
 // Maps a pair-tile index to (class, view, 256-row block pm, 256-col block tn)
 // and returns this CTA's 128-row tile tm = 2 pm + rank.
-template <int MODE>
 __device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t, uint32_t rank) {
   int c = 0;
   while (c + 1 < p.num_classes && t >= p.cls[c + 1].tile_begin) ++c;
@@ -91,7 +103,7 @@ __device__ __forceinline__ TileCoord map_tile(const GemmParams& p, int64_t t, ui
     // Consecutive tiles walk the m x m operand P (which stays in L2) and share
     // one block of X: for X = m x n the row blocks of the output, for a tall
     // view's T = n x m (mode KK) its column blocks.
-    if (MODE == GEMM_MODE_KK) {
+    if (C.mode == GEMM_MODE_KK) {
       tc.tn = w % C.tiles_n;
       pm = w / C.tiles_n;
     } else {
@@ -274,10 +286,227 @@ __device__ __forceinline__ void abort_pair(volatile int* abort_flag) {
   st_cluster_s32(abort_flag, 1, 1);
 }
 
+// The TMA loads of k-blocks kb0 .. kb1-1 of one tile in operand mode MODE.
+// Returns false when the launch aborts.
 template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+__device__ __forceinline__ bool load_tile(const GemmParams& p, const GemmClass& C,
+                                          const TileCoord& tc, uint32_t rank, int kb0, int kb1,
+                                          uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                          uint64_t* empty, int& stage, uint32_t& phase,
+                                          uint32_t& inflight, uint32_t& inflight_par,
+                                          volatile int* abort_flag) {
   constexpr bool a_mn = MODE == GEMM_MODE_MM;
   constexpr bool b_mn = MODE != GEMM_MODE_KK;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_TMA,
+                           p.wait_limit))
+      return false;
+    mbar_arrive_expect_tx(&full[stage], kStageABytes + kStageBBytes);
+    uint8_t* a_dst = sA + stage * kStageABytes;
+    if constexpr (a_mn) {
+      // 128 columns of T as two MN-major 64-column chunks.
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        tma_load_3d(a_dst + j * kApplyChunkBytes, &C.tmA, &full[stage], tc.tm * kBM + j * 64,
+                    kb * kBK, tc.view);
+    } else {
+      tma_load_3d(a_dst, &C.tmA, &full[stage], kb * kBK, tc.tm * kBM, tc.view);
+    }
+    uint8_t* b_dst = sB + stage * kStageBBytes;
+    if constexpr (b_mn) {
+      // This CTA's two 64-column chunks of the 256-column B block.
+#pragma unroll
+      for (int j = 2 * static_cast<int>(rank); j < 2 * static_cast<int>(rank) + 2; ++j)
+        tma_load_3d_mc(b_dst + j * kApplyChunkBytes, &C.tmB, &full[stage], tc.tn * kBN + j * 64,
+                       kb * kBK, tc.view, kPairMask);
+    } else {
+      // This CTA's 128 of the 256 B rows.
+      tma_load_3d_mc(b_dst + rank * kHalfBBytes, &C.tmB, &full[stage], kb * kBK,
+                     tc.tn * kBN + static_cast<int>(rank) * kBM, tc.view, kPairMask);
+    }
+    inflight |= 1u << stage;
+    inflight_par = (inflight_par & ~(1u << stage)) | (phase << stage);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+// The MMAs of k-blocks kb0 .. kb1-1 of one tile in operand mode MODE into the
+// accumulator at d_tmem (k-block 0 overwrites it). Returns false when the
+// launch aborts.
+template <int MODE>
+__device__ __forceinline__ bool mma_tile(const GemmParams& p, int kb0, int kb1, uint32_t d_tmem,
+                                         uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                         uint64_t* empty, int& stage, uint32_t& phase,
+                                         bool& issued, volatile int* abort_flag) {
+  constexpr bool a_mn = MODE == GEMM_MODE_MM;
+  constexpr bool b_mn = MODE != GEMM_MODE_KK;
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  // K-major: 16 bf16 of k = 32 bytes inside the 128-byte swizzle row.
+  // MN-major: 16 k-rows = two 1024-byte atoms, 64-column chunks 8 KB apart.
+  constexpr uint32_t a_kstep = a_mn ? 2048u : 32u, a_lbo = a_mn ? kApplyChunkBytes : 16u;
+  constexpr uint32_t b_kstep = b_mn ? 2048u : 32u, b_lbo = b_mn ? kApplyChunkBytes : 16u;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, DEV_TIMEOUT_MMA,
+                           p.wait_limit))
+      return false;
+    tc_fence_after();
+    const uint32_t a0 = smem_addr(sA + stage * kStageABytes);
+    const uint32_t b0 = smem_addr(sB + stage * kStageBBytes);
+#pragma unroll
+    for (int k = 0; k < kBK / 16; ++k) {
+      const uint64_t ad = smem_desc_sw128(a0 + k * a_kstep, a_lbo, 1024);
+      const uint64_t bd = smem_desc_sw128(b0 + k * b_kstep, b_lbo, 1024);
+      tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+    }
+    issued = true;
+    tc_commit_mc(&empty[stage], kPairMask);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+constexpr int kModeKK = 1 << GEMM_MODE_KK, kModeKM = 1 << GEMM_MODE_KM, kModeMM = 1 << GEMM_MODE_MM;
+
+// The loads of one tile in a kernel specialised on the set MODES of operand
+// modes its launch contains: a single mode needs no dispatch at all.
+template <int MODES>
+__device__ __forceinline__ bool load_tile_of(const GemmParams& p, const GemmClass& C,
+                                             const TileCoord& tc, uint32_t rank, int kb0, int kb1,
+                                             uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                             uint64_t* empty, int& stage, uint32_t& phase,
+                                             uint32_t& inflight, uint32_t& inflight_par,
+                                             volatile int* abort_flag) {
+  if constexpr ((MODES & kModeKK) != 0)
+    if (MODES == kModeKK || C.mode == GEMM_MODE_KK)
+      return load_tile<GEMM_MODE_KK>(p, C, tc, rank, kb0, kb1, sA, sB, full, empty, stage,
+                                     phase, inflight, inflight_par, abort_flag);
+  if constexpr ((MODES & kModeKM) != 0)
+    if (MODES == kModeKM || C.mode == GEMM_MODE_KM || (MODES & kModeMM) == 0)
+      return load_tile<GEMM_MODE_KM>(p, C, tc, rank, kb0, kb1, sA, sB, full, empty, stage,
+                                     phase, inflight, inflight_par, abort_flag);
+  if constexpr ((MODES & kModeMM) != 0)
+    return load_tile<GEMM_MODE_MM>(p, C, tc, rank, kb0, kb1, sA, sB, full, empty, stage, phase,
+                                   inflight, inflight_par, abort_flag);
+  return false;
+}
+
+template <int MODES>
+__device__ __forceinline__ bool mma_tile_of(const GemmParams& p, int mode, int kb0, int kb1,
+                                            uint32_t d_tmem, uint8_t* sA, uint8_t* sB,
+                                            uint64_t* full, uint64_t* empty, int& stage,
+                                            uint32_t& phase, bool& issued,
+                                            volatile int* abort_flag) {
+  if constexpr ((MODES & kModeKK) != 0)
+    if (MODES == kModeKK || mode == GEMM_MODE_KK)
+      return mma_tile<GEMM_MODE_KK>(p, kb0, kb1, d_tmem, sA, sB, full, empty, stage, phase,
+                                    issued, abort_flag);
+  if constexpr ((MODES & kModeKM) != 0)
+    if (MODES == kModeKM || mode == GEMM_MODE_KM || (MODES & kModeMM) == 0)
+      return mma_tile<GEMM_MODE_KM>(p, kb0, kb1, d_tmem, sA, sB, full, empty, stage, phase,
+                                    issued, abort_flag);
+  if constexpr ((MODES & kModeMM) != 0)
+    return mma_tile<GEMM_MODE_MM>(p, kb0, kb1, d_tmem, sA, sB, full, empty, stage, phase,
+                                  issued, abort_flag);
+  return false;
+}
+
+// The pair's shared tile sequence. Entries 0 and 1 are static, the pair's
+// own index p and p + npairs: every pair starts without waiting for a claim,
+// a launch of at most two rounds of blocks claims nothing, and the first
+// claim has a whole block's time to return. From entry 2 on, CTA 0's
+// producer claims block indices from the launch's counter (offset by
+// 2 npairs).
+//
+// Entry i >= 1 travels at ring position i - 1 (slot (i - 1) mod kTileRing)
+// through two rings. The pair ring carries it from CTA 0's producer to CTA
+// 1's producer only (cluster scope, one consumer). Each CTA's producer then
+// publishes it on its own CTA's local ring, which that CTA's MMA issuer and
+// four epilogue warps read (CTA scope, kLocalConsumers arrivals per entry),
+// so the roles on the critical path never wait on the other CTA.
+constexpr uint32_t kLocalConsumers = 5;
+
+struct Rings {
+  uint64_t* pair_full;   // in CTA 1: CTA 0 arrives once per entry
+  uint64_t* pair_empty;  // in CTA 0: CTA 1's producer arrives once per entry
+  uint32_t* pair_slots;  // in CTA 1, written by CTA 0
+  uint64_t* local_full;  // this CTA's producer arrives once per entry
+  uint64_t* local_empty; // this CTA's MMA issuer and epilogue warps arrive
+  uint32_t* local_slots;
+};
+
+// CTA 0: hands the tile index t at ring position i to CTA 1's producer.
+// Returns false when the launch aborts.
+__device__ __forceinline__ bool pair_publish(const GemmParams& p, const Rings& R, uint32_t i,
+                                             uint32_t t, volatile int* abort_flag) {
+  const uint32_t s = i % kTileRing;
+  const uint32_t par = (i / kTileRing) & 1u;
+  if (!mbar_wait_bounded<true>(&R.pair_empty[s], par ^ 1u, abort_flag, p.status,
+                               DEV_TIMEOUT_TMA, p.wait_limit))
+    return false;
+  // The index travels as an asynchronous store whose completion counts on
+  // CTA 1's barrier, so no release (which would wait for this thread's TMA
+  // loads in flight) is needed to order it before the arrive.
+  mbar_arrive_expect_tx_relaxed(&R.pair_full[s], 1, 4);
+  st_async_u32(&R.pair_slots[s], 1, t, &R.pair_full[s]);
+  return true;
+}
+
+// CTA 1: the tile index at ring position i from CTA 0, then the slot is
+// released; -1 when the launch aborts. The slot is read with acquire
+// semantics, so the relaxed release arrive cannot be performed before it.
+__device__ __forceinline__ int64_t pair_read(const GemmParams& p, const Rings& R, uint32_t i,
+                                             volatile int* abort_flag) {
+  const uint32_t s = i % kTileRing;
+  const uint32_t par = (i / kTileRing) & 1u;
+  if (!mbar_wait_bounded<true>(&R.pair_full[s], par, abort_flag, p.status, DEV_TIMEOUT_TMA,
+                               p.wait_limit))
+    return -1;
+  const uint32_t t = ld_acquire_cluster_u32(&R.pair_slots[s]);
+  mbar_arrive_cluster_relaxed(&R.pair_empty[s], 0);
+  return static_cast<int64_t>(t);
+}
+
+// A CTA's producer: publishes the tile index t at ring position i to its
+// own CTA's MMA issuer and epilogue warps. Returns false when the launch
+// aborts.
+__device__ __forceinline__ bool local_publish(const GemmParams& p, const Rings& R, uint32_t i,
+                                              uint32_t t, volatile int* abort_flag) {
+  const uint32_t s = i % kTileRing;
+  const uint32_t par = (i / kTileRing) & 1u;
+  if (!mbar_wait_bounded(&R.local_empty[s], par ^ 1u, abort_flag, p.status, DEV_TIMEOUT_TMA,
+                         p.wait_limit))
+    return false;
+  // As in pair_publish, to this CTA's own ring.
+  const uint32_t self = cluster_ctarank();
+  mbar_arrive_expect_tx_relaxed(&R.local_full[s], self, 4);
+  st_async_u32(&R.local_slots[s], self, t, &R.local_full[s]);
+  return true;
+}
+
+// The tile index at ring position i of this CTA's local ring, read by one
+// thread, which then releases the slot; -1 when the launch aborts. The read
+// has acquire semantics and the release arrive is relaxed: the reader's own
+// writes (an epilogue's parameter stores) need not wait for it.
+__device__ __forceinline__ int64_t local_read(const GemmParams& p, const Rings& R, uint32_t i,
+                                              volatile int* abort_flag, int code) {
+  const uint32_t s = i % kTileRing;
+  const uint32_t par = (i / kTileRing) & 1u;
+  if (!mbar_wait_bounded(&R.local_full[s], par, abort_flag, p.status, code, p.wait_limit))
+    return -1;
+  const uint32_t t = ld_acquire_cta_u32(&R.local_slots[s]);
+  mbar_arrive_relaxed(&R.local_empty[s]);
+  return static_cast<int64_t>(t);
+}
+
+template <int MODES>
+__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -290,14 +519,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  Rings R;
+  R.pair_full = drain + 1;
+  R.pair_empty = R.pair_full + kTileRing;
+  R.local_full = R.pair_empty + kTileRing;
+  R.local_empty = R.local_full + kTileRing;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(R.local_empty + kTileRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  R.pair_slots = tmem_slot + 2;
+  R.local_slots = R.pair_slots + kTileRing;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const int64_t pair = blockIdx.x >> 1;
-  const int64_t npairs = gridDim.x >> 1;
+  const uint32_t total = static_cast<uint32_t>(p.total_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -309,6 +544,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       mbar_init(&tempty[a], 128);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(&R.pair_full[s], 1);
+      mbar_init(&R.pair_empty[s], 1);
+      mbar_init(&R.local_full[s], 1);
+      mbar_init(&R.local_empty[s], kLocalConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -336,65 +577,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   // resident by the time this grid finishes.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The launch after the next one claims from this counter: every launch
+  // before it has completed by then, this one included.
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.next_counter = 0u;
 
   if (step_skipped(p.skip)) {
     // A skipped step (gradient control): every thread of both CTAs reads the
     // same flag, no role runs, and the teardown below still pairs the
     // cluster barrier and frees TMEM.
   } else if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (CTA 0: also claims the tiles) ----------------
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t inflight = 0;     // stages with a load issued
       uint32_t inflight_par = 0; // parity of that load's phase
       bool ok = true;
-      for (int64_t t = pair; ok && t < p.total_tiles; t += npairs) {
-        const TileCoord tc = map_tile<MODE>(p, t, rank);
+      // Entry i of the tile sequence is t. CTA 0 publishes entry i + 1 on
+      // both rings before tile i's first load (it is static, or was claimed
+      // during tile i - 1) and claims the index of entry i + 2, which it
+      // needs a whole tile later. CTA 1's producer reads entry i + 1 once
+      // tile i's loads are issued and publishes it on its own local ring. So
+      // every read finds an entry published a tile earlier, and CTA 1's loads
+      // never wait for CTA 0.
+      const uint32_t npairs = gridDim.x >> 1;
+      uint32_t i = 0;
+      int64_t t = blockIdx.x >> 1;
+      uint32_t next = (blockIdx.x >> 1) + npairs;  // CTA 0: entry i + 1
+      auto claim = [&]() { return 2u * npairs + atomicAdd(p.tile_counter, 1u); };
+      while (ok && t < total) {
+        if (rank == 0) {
+          ok = pair_publish(p, R, i, next, abort_flag) &&
+               local_publish(p, R, i, next, abort_flag);
+          if (!ok) break;
+        }
+        const int64_t t_pub = next;
+        if (rank == 0 && next < total) next = claim();
+        const TileCoord tc = map_tile(p, t, rank);
         const GemmClass& C = p.cls[tc.cls];
         const int nk = (C.K + kBK - 1) / kBK;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_TMA)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], kStageABytes + kStageBBytes);
-          uint8_t* a_dst = sA + stage * kStageABytes;
-          if constexpr (a_mn) {
-            // 128 columns of T as two MN-major 64-column chunks.
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_3d(a_dst + j * kApplyChunkBytes, &C.tmA, &full[stage],
-                          tc.tm * kBM + j * 64, kb * kBK, tc.view);
-          } else {
-            tma_load_3d(a_dst, &C.tmA, &full[stage], kb * kBK, tc.tm * kBM, tc.view);
-          }
-          uint8_t* b_dst = sB + stage * kStageBBytes;
-          if constexpr (b_mn) {
-            // This CTA's two 64-column chunks of the 256-column B block.
-#pragma unroll
-            for (int j = 2 * static_cast<int>(rank); j < 2 * static_cast<int>(rank) + 2; ++j)
-              tma_load_3d_mc(b_dst + j * kApplyChunkBytes, &C.tmB, &full[stage],
-                             tc.tn * kBN + j * 64, kb * kBK, tc.view, kPairMask);
-          } else {
-            // This CTA's 128 of the 256 B rows.
-            tma_load_3d_mc(b_dst + rank * kHalfBBytes, &C.tmB, &full[stage], kb * kBK,
-                           tc.tn * kBN + static_cast<int>(rank) * kBM, tc.view, kPairMask);
-          }
-          inflight |= 1u << stage;
-          inflight_par = (inflight_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+        ok = load_tile_of<MODES>(p, C, tc, rank, 0, nk, sA, sB, full, empty, stage, phase,
+                                 inflight, inflight_par, abort_flag);
+        if (!ok) break;
+        int64_t t_next = t_pub;
+        if (rank != 0) {
+          t_next = pair_read(p, R, i, abort_flag);
+          ok = t_next >= 0 && local_publish(p, R, i, static_cast<uint32_t>(t_next), abort_flag);
+          if (!ok) break;
         }
+        t = t_next;
+        ++i;
       }
       if (ok) {
         // Wait until both CTAs' MMAs have released every stage this CTA
         // filled: after this, no arrive from the peer can still be on its way
         // to this CTA's barriers.
-        for (int i = 0; i < kStages; ++i) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_TMA)) {
+        for (int k = 0; k < kStages; ++k) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_TMA,
+                                 p.wait_limit)) {
             ok = false;
             break;
           }
@@ -414,51 +654,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
-      // K-major: 16 bf16 of k = 32 bytes inside the 128-byte swizzle row.
-      // MN-major: 16 k-rows = two 1024-byte atoms, 64-column chunks 8 KB apart.
-      constexpr uint32_t a_kstep = a_mn ? 2048u : 32u, a_lbo = a_mn ? kApplyChunkBytes : 16u;
-      constexpr uint32_t b_kstep = b_mn ? 2048u : 32u, b_lbo = b_mn ? kApplyChunkBytes : 16u;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
-      for (int64_t t = pair; ok && t < p.total_tiles; t += npairs) {
-        const TileCoord tc = map_tile<MODE>(p, t, rank);
+      int64_t t = blockIdx.x >> 1;
+      for (uint32_t i = 0;; ++i) {
+        if (t < 0) {
+          ok = false;
+          break;
+        }
+        if (t >= total) break;
+        const TileCoord tc = map_tile(p, t, rank);
         const GemmClass& C = p.cls[tc.cls];
         const int nk = (C.K + kBK - 1) / kBK;
-        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_MMA,
+                               p.wait_limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_addr(sA + stage * kStageABytes);
-          const uint32_t b0 = smem_addr(sB + stage * kStageBBytes);
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = smem_desc_sw128(a0 + k * a_kstep, a_lbo, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + k * b_kstep, b_lbo, 1024);
-            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-          }
-          issued = true;
-          tc_commit_mc(&empty[stage], kPairMask);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        ok = mma_tile_of<MODES>(p, C.mode, 0, nk, d_tmem, sA, sB, full, empty, stage, phase,
+                                issued, abort_flag);
         if (!ok) break;
         tc_commit(&tfull[acc]);
+        // Entry i + 1 was published before this tile's loads.
+        const int64_t t_next = local_read(p, R, i, abort_flag, DEV_TIMEOUT_MMA);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
+        t = t_next;
       }
       if (!ok) abort_pair(abort_flag);
       if (!ok && issued) {
@@ -473,8 +699,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     uint32_t staged = 0;  // chunks this warp has handed to TMA stores (buffer = parity)
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = pair; t < p.total_tiles; t += npairs) {
-      const TileCoord tc = map_tile<MODE>(p, t, rank);
+    // Lane 0 reads each entry and releases its slot; the others take it from
+    // lane 0, so the whole warp agrees on the tile (or on an abort). Entry
+    // i + 1 (ring position i) is read once tile i's accumulator is full.
+    auto read_entry = [&](uint32_t idx) -> int64_t {
+      long long tl = 0;
+      if (lane == 0)
+        tl = local_read(p, R, idx, abort_flag, DEV_TIMEOUT_EPI);
+      return __shfl_sync(0xffffffffu, tl, 0);
+    };
+    int64_t t = blockIdx.x >> 1;
+    for (uint32_t i = 0;; ++i) {
+      if (t < 0) {
+        if (lane == 0) abort_pair(abort_flag);
+        break;
+      }
+      if (t >= total) break;
+      const TileCoord tc = map_tile(p, t, rank);
       const GemmClass& C = p.cls[tc.cls];
       const int r0 = tc.tm * kBM + ew * 32;  // first row of this warp
       const int r = r0 + lane;
@@ -499,11 +740,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const bf16* wbase = w_pf ? static_cast<const bf16*>(R.param) + R.elem0 : nullptr;
       uint4 pw[4];
       prefetch_aux32(wbase, fin ? R.cols : 0, r, tc.tn * kBN, rows_out, n_out, w_pf, pw);
-      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPI)) {
-        abort_pair(abort_flag);
+      // Every lane waits for the accumulator; the warp goes on only if all
+      // of them saw it full, so a timeout never splits the warp before the
+      // warp-wide TMEM loads.
+      const bool full_ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status,
+                                             DEV_TIMEOUT_EPI, p.wait_limit);
+      if (!__all_sync(0xffffffffu, full_ok)) {
+        if (lane == 0) abort_pair(abort_flag);
         break;
       }
       tc_fence_after();
+      const int64_t t_next = read_entry(i);
 
       float sc = 1.0f;
       if (p.first_iter) {
@@ -661,6 +908,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+      t = t_next;
     }
     // Every TMA store of this warp has landed before the kernel ends.
     if (lane == 0) bulk_wait_all();
@@ -680,9 +928,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 }  // namespace
 
 size_t gemm_smem_bytes() {
+  // 1 KB alignment slack, operand ring, epilogue staging, mbarriers (stage
+  // full/empty, two accumulators full/empty, drain, pair and local tile
+  // rings full/empty), then the TMEM address, the abort flag and the two
+  // rings' slots.
   return 1024 + kStages * (kStageABytes + kStageBBytes) + 4 * kOutWarpBytes +
-         (2 * kStages + 5) * sizeof(uint64_t) + 16;
+         (2 * kStages + 5 + 4 * kTileRing) * sizeof(uint64_t) + 2 * sizeof(uint32_t) +
+         2 * kTileRing * sizeof(uint32_t);
 }
+static_assert(1024 + kStages * (kStageABytes + kStageBBytes) + 4 * kOutWarpBytes +
+                  (2 * kStages + 5 + 4 * kTileRing) * 8 + 8 + 8 * kTileRing <= 232448,
+              "GEMM shared memory exceeds the 227 KB a CTA may use");
 
 // Maximum number of co-resident CTA pairs on the current device (GPCs with an
 // odd number of free SMs leave one SM out), cached per device.
@@ -704,7 +960,7 @@ int gemm_max_pairs(int dev, int num_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, ns_gemm_kernel<GEMM_MODE_KK>, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&clusters, ns_gemm_kernel<kModeKK>, &cfg) != cudaSuccess ||
       clusters <= 0) {
     (void)cudaGetLastError();
     clusters = num_sms / 2;
@@ -715,10 +971,20 @@ int gemm_max_pairs(int dev, int num_sms) {
 
 cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  if (p.mode < 0 || p.mode >= kGemmModes) return cudaErrorInvalidValue;
+  int modes = 0;
+  for (int c = 0; c < p.num_classes; ++c) {
+    if (p.cls[c].mode < 0 || p.cls[c].mode >= kGemmModes) return cudaErrorInvalidValue;
+    modes |= 1 << p.cls[c].mode;
+  }
+  if (p.tile_counter == nullptr || p.next_counter == nullptr) return cudaErrorInvalidValue;
+  // One instantiation per set of operand modes a stage can contain: gram
+  // {KK, MM}, poly {KK}, apply {KK, KM}, each mode alone or with the other.
   using Kernel = void (*)(GemmParams);
-  static constexpr Kernel kKernels[kGemmModes] = {
-      ns_gemm_kernel<GEMM_MODE_KK>, ns_gemm_kernel<GEMM_MODE_KM>, ns_gemm_kernel<GEMM_MODE_MM>};
+  static constexpr Kernel kKernels[8] = {
+      nullptr, ns_gemm_kernel<kModeKK>, ns_gemm_kernel<kModeKM>, ns_gemm_kernel<kModeKK | kModeKM>,
+      ns_gemm_kernel<kModeMM>, ns_gemm_kernel<kModeKK | kModeMM>, nullptr, nullptr};
+  const Kernel kernel = kKernels[modes];
+  if (kernel == nullptr) return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes();
   static thread_local int configured_device = -1;
   int dev = 0;
@@ -726,6 +992,7 @@ cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     for (Kernel k : kKernels) {
+      if (k == nullptr) continue;
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
@@ -748,7 +1015,7 @@ cudaError_t launch_ns_gemm(const GemmParams& p, int num_sms, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kKernels[p.mode], p);
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
