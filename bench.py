@@ -363,6 +363,53 @@ def ns_flops(wl) -> float:
     return tot
 
 
+# Nominal dense bf16 tensor-core rate of one GB300 (NVIDIA datasheet, without
+# sparsity): context beside the measured peaks the fractions are taken of.
+DATASHEET_BF16_TFLOPS = 2250.0
+
+
+def tensor_peak(peaks: dict, peak_src: str, clk: dict):
+    """The measured bf16 peak that applies to a timed region: the sustained
+    cuBLAS rate when the power cap was active while it ran (a long step), the
+    burst rate otherwise."""
+    capped = "sw_power_cap" in (clk or {}).get("reasons", [])
+    key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    return peaks[key], f"bf16 {'sustained' if capped else 'burst'} cuBLAS, of {peak_src}"
+
+
+def gemm_roofline(v: dict, peaks: dict, peak_src: str, clk: dict, traffic=None) -> dict:
+    """Roofline of the Newton-Schulz GEMM family from its event-timed stats:
+    led by the executed FLOPs (the work the tensor cores do), with the
+    contract's nominal count and the datasheet fraction beside it."""
+    t = v["total_ms"] * 1e-3
+    ex = v["flops_executed"] / t / 1e12
+    nom = v["flops"] / t / 1e12
+    peak, src = tensor_peak(peaks, peak_src, clk)
+    return {"kernel": "ns_gemm", "bound": "tensor", "achieved": round(ex, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(ex / peak, 4), "traffic": traffic,
+            "achieved_basis": "executed FLOPs per launch (upper block triangle of XX^T and of "
+                              "A A, every block of the apply) / CUDA-event time",
+            "peak_source": src,
+            "frac_of_datasheet": round(ex / DATASHEET_BF16_TFLOPS, 4),
+            "datasheet_peak": DATASHEET_BF16_TFLOPS,
+            "nominal_tflops": round(nom, 1), "nominal_frac": round(nom / peak, 4),
+            "nominal_basis": "4m^2n + 2m^3 per view and iteration; counts the symmetric "
+                             "products in full, so it exceeds the executed work",
+            "launches": v["launches"],
+            "algorithmic_bytes_per_launch": round(v["bytes"] / max(v["launches"], 1)),
+            "traffic_unit": "DRAM bytes per launch (ncu record in profiles/, or null)"}
+
+
+def hbm_roofline(name: str, v: dict, peaks: dict, peak_src: str, traffic=None) -> dict:
+    ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "achieved_basis": "algorithmic bytes per launch (each operand read and each result "
+                              "written once) / CUDA-event time",
+            "algorithmic_bytes_per_launch": round(v["bytes"] / max(v["launches"], 1)),
+            "launches": v["launches"], "peak_source": f"HBM copy, of {peak_src}"}
+
+
 # ---- host buffers for the end-to-end measurement -------------------------------------
 
 class PinnedMirror:
@@ -715,30 +762,75 @@ def sample_desc(wl, views, adam):
             "; Muon time scaled to the full step by nominal NS FLOPs, AdamW time by elements")
 
 
+# One bounded oracle sample per workload, shared by the CPU baseline of our
+# arm and by every step of the reference arm, so the two time the same work:
+# whole Muon views up to about 6 TFLOP of fp64 Newton-Schulz (a few seconds
+# on the host cores) and up to 2^25 AdamW elements.
+ORACLE_NS_FLOP_BUDGET = 6e12
+ORACLE_ADAM_ELEMS = 1 << 25
+
+
+def oracle_plan(wl):
+    return oracle_sample_plan(wl, ORACLE_NS_FLOP_BUDGET, ORACLE_ADAM_ELEMS)
+
+
+def blas_name() -> str:
+    try:
+        from threadpoolctl import threadpool_info
+        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return f"{info[0].get('internal_api', '?')} {info[0].get('version', '')}".strip()
+    except Exception:
+        pass
+    return "numpy's BLAS"
+
+
+def cpu_baseline_record(wl, views, adam, sample, seconds, ms: float) -> dict:
+    """The oracle's time for the full step (extrapolated from the sample when
+    the sample is not the whole step) with what it covered."""
+    nsf = ns_flops(wl)
+    f_ns = sum(f for _, _, f in views) / nsf if nsf else 1.0
+    f_ad = sum(c for _, c in adam) / wl.adam_elems if wl.adam_elems else 1.0
+    return {"value": round(ms, 3), "unit": "ms/step", "cores": blas_threads(),
+            "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
+            "sample": sample_desc(wl, views, adam),
+            "extrapolated": bool(f_ns < 1.0 - 1e-12 or f_ad < 1.0 - 1e-12),
+            "sample_fraction": {"ns_flops": round(f_ns, 6), "adamw_elems": round(f_ad, 6)},
+            "sample_seconds": round(seconds, 3)}
+
+
+def metric_for(wl) -> str:
+    """The 7B-shape set carries the headline metric; the other sets are named
+    by their workload in the same form."""
+    if wl.name.startswith("llama7b"):
+        return METRIC
+    return f"Muon+AdamW step ms ({wl.name}); Newton–Schulz TFLOP/s vs bf16 TC peak"
+
+
 # ---- main ---------------------------------------------------------------------------------
 
 def run_reference(args, wl):
+    """The reference arm: the fp64 oracle timed on the host cores, each step
+    the workload's bounded sample (oracle_plan), scaled to the full step."""
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
-    # One bounded sample per step: about a second of CPU work.
-    views, adam = oracle_sample_plan(wl, muon_flop_budget=2.0e11, adam_elems=1 << 22)
+    views, adam = oracle_plan(wl)
     sample = OracleSample(wl, views, adam, args.max_grad_norm)
     for _ in range(args.warmup):
         sample.run()
-    per = []
+    per, secs = [], []
     for _ in range(args.steps):
         ms_muon, ms_adam, ms_ctl = sample.run()
+        secs.append(ms_muon + ms_adam + ms_ctl)
         per.append(oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam, ms_ctl,
                                           sample.grad_elems()))
     ms = statistics.mean(per)
-    cores = blas_threads()
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms/step",
+        "impl": "reference", "metric": metric_for(wl), "value": round(ms, 3), "unit": "ms/step",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(wl, args.max_grad_norm),
-        "cpu_baseline": {"value": round(ms, 3), "unit": "ms/step", "cores": cores,
-                         "kind": "oracle", "sample": sample_desc(wl, views, adam)},
+        "cpu_baseline": cpu_baseline_record(wl, views, adam, sample, statistics.mean(secs), ms),
         "e2e": {"value": round(ms, 3), "unit": "ms/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -746,28 +838,38 @@ def run_reference(args, wl):
     return 0
 
 
-def config_dict(wl, max_grad_norm=None):
+L2_BYTES = 129e6               # GB300 L2
+FLUSH_BELOW_BYTES = 4 * L2_BYTES   # resident sets smaller than this get an L2 flush per step
+
+
+def config_dict(wl, max_grad_norm=None, l2=None):
     extra = {} if max_grad_norm is None else {
         "grad_control": {"max_grad_norm": max_grad_norm, "inv_loss_scale": 1.0}}
+    pdt = sorted({s.param_dtype for s in wl.muon} | {s.param_dtype for s in wl.adamw})
+    gdt = sorted({s.grad_dtype for s in wl.muon} | {s.grad_dtype for s in wl.adamw})
+    state = ("fp32 optimizer state" if wl.state_dtype == "f32"
+             else "bf16 optimizer state, stochastically rounded")
     return {**{"workload": wl.name,
             "muon_tensors": len(wl.muon), "muon_views": sum(s.views for s in wl.muon),
             "muon_elems": wl.muon_elems, "adamw_tensors": len(wl.adamw),
             "adamw_elems": wl.adam_elems, "ns_steps": wl.muon_hp["ns_steps"],
             "variants": {k: wl.muon_hp.get(k) for k in ("normuon", "muon_plus", "cautious")
                          if wl.muon_hp.get(k)},
-            "precision": "bf16 tensor-core NS operands, fp32 accumulate; fp32 elementwise math "
-                         + ("and optimizer state; bf16 params/grads" if wl.state_dtype == "f32"
-                            else "; bf16 optimizer state and bf16 params, stochastically rounded; "
-                                 "bf16 grads"),
+            "precision": ("bf16 tensor-core NS operands, fp32 accumulate; fp32 elementwise math; "
+                          f"{state}; params {'/'.join(pdt)}; grads {'/'.join(gdt)}"),
             "parallelism": "single GPU",
-            "l2": "inputs larger than L2 (no flush needed)"}, **extra}
+            "l2": l2 or "inputs larger than L2 (no flush needed)"}, **extra}
 
 
 def run_ns_only(args):
     """Newton-Schulz alone on a batch of n x n, n x 4n or 4n x n matrices
-    (entries N(0,1), bf16 in and out), timed like the full step."""
+    (entries N(0,1), bf16 in and out), timed like the full step; the oracle
+    baseline runs the fp64 iteration on one view of the batch."""
+    import numpy as np
     import torch
     import muon_adamw_hybrid_gb300 as mh
+    import oracle
+    import synth
     from synth.gpu import fill_normal
     device = gpu_setup()
     stream = torch.cuda.current_stream(device)
@@ -785,7 +887,7 @@ def run_ns_only(args):
 
     def call():
         mh.newton_schulz_batched(probs, 5, a_, b_, c_, 1e-7, ws.data_ptr(), need, stream.cuda_stream)
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, 0)):
         call()
     torch.cuda.synchronize()
     clocks = ClockSampler(0)
@@ -805,26 +907,53 @@ def run_ns_only(args):
     ks = family_stats(mh.profiler_read())
     m_, n_ = min(r, c), max(r, c)
     flops = b * 5 * (4.0 * m_ * m_ * n_ + 2.0 * m_ ** 3)
-    g = ks.get("ns_gemm", {"total_ms": 0.0, "flops": 0.0, "flops_executed": 0.0, "launches": 0})
-    peak = peaks["bf16_tflops"]
-    ach = g["flops"] / (g["total_ms"] * 1e-3) / 1e12 if g["total_ms"] else 0.0
+    roofline = gemm_roofline(ks["ns_gemm"], peaks, peak_src, clk) if "ns_gemm" in ks else None
+
+    # End to end: the batch copied in from page-locked host memory, the call,
+    # and the result copied back, every call.
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xh.copy_(x)
+    oh = torch.empty_like(xh, pin_memory=True)
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        x.copy_(xh, non_blocking=True)
+        call()
+        oh.copy_(out, non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e2.elapsed_time(e3) / args.steps
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        q = synth.normal(0, 5000 + n, (r, c), dtype="bf16").astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.newton_schulz(q)
+        sec = time.perf_counter() - t0
+        cpu = {"value": round(1e3 * sec * b, 3), "unit": "ms/call", "cores": blas_threads(),
+               "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
+               "sample": f"fp64 oracle on view 0 ({r}x{c}) of the batch, scaled by the batch "
+                         f"count {b}",
+               "extrapolated": b > 1, "sample_fraction": {"ns_flops": round(1.0 / b, 6)},
+               "sample_seconds": round(sec, 3)}
     print(json.dumps({
-            "metric": "Newton-Schulz TFLOP/s (nominal 4m^2n+2m^3 per iteration)",
-            "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": f"ns_{args.ns_aspect}_n{n}_batch{b}", "rows": r, "cols": c,
-                       "batch": b, "l2": "X operand " + ("larger" if b * r * c * 2 > 129e6
-                                                         else "smaller") + " than L2"},
-            "roofline": {"kernel": "ns_gemm", "bound": "tensor", "achieved": round(ach, 1),
-                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                         "traffic": None, "peak_source": f"bf16 burst, of {peak_src}",
-                         "executed_tflops": round(g["flops_executed"] / (g["total_ms"] * 1e-3) / 1e12, 1)
-                         if g["total_ms"] else None},
-            "kernels": {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3)}
-                        for k, v in ks.items()},
-            "gpu_launches": sum(v["launches"] for v in ks.values()), "clocks": clk}), flush=True)
+        "metric": "Newton-Schulz call ms (5 quintic iterations, bf16 operands)",
+        "value": round(ms, 4), "unit": "ms/call", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"ns_{args.ns_aspect}_n{n}_batch{b}", "rows": r, "cols": c,
+                   "batch": b, "l2": "X operand " + ("larger" if b * r * c * 2 > 129e6
+                                                     else "smaller") + " than L2 (no flush)"},
+        "ns_tflops_nominal": round(flops / (ms * 1e-3) / 1e12, 1),
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms/call",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size()},
+        "kernels": {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3)}
+                    for k, v in ks.items()},
+        "gpu_launches": sum(v["launches"] for v in ks.values()), "clocks": clk}), flush=True)
     return 0
 
 
@@ -935,20 +1064,42 @@ def main():
     dw.check_status(stream)
 
     # ---- timed region: K device-resident steps --------------------------------------
+    # Sets far larger than L2 are timed as one span; smaller ones get an L2
+    # flush (a write of twice L2) between steps, each step timed on its own.
+    flush = None
+    l2_note = None
+    if dw.resident_bytes < FLUSH_BELOW_BYTES:
+        flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=device)
+        l2_note = (f"L2 flushed between timed steps (a {flush.numel() >> 20} MiB write, outside "
+                   f"the timed spans); resident set {dw.resident_bytes / 1e6:.1f} MB")
     clocks = ClockSampler(0)
     clocks.start()
     mh.profiler_reset()
     mh.profiler_enable(True)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        dw.step(stream)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    if flush is None:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            dw.step(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_total = ev0.elapsed_time(ev1)
+    else:
+        spans = []
+        for _ in range(args.steps):
+            mh.profiler_enable(False)
+            flush.fill_(1)
+            mh.profiler_enable(True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dw.step(stream)
+            e1.record(stream)
+            spans.append((e0, e1))
+        torch.cuda.synchronize()
+        ms_total = sum(a.elapsed_time(b) for a, b in spans)
     mh.profiler_enable(False)
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
     ms_step = ms_total / args.steps
     stage_stats = mh.profiler_read()
     dw.check_status(stream)
@@ -976,39 +1127,16 @@ def main():
         if v["bytes"] > 0:
             kernels[name]["gbs"] = round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1)
     traffic = traffic_records(args.workload)
-    roofline = None
-    if kstats:
-        top = max(kstats, key=lambda k: kstats[k]["total_ms"])
-        v = kstats[top]
-        if v["flops"] > 0:
-            peak = peaks["bf16_tflops_sustained"]
-            ach = v["flops"] / (v["total_ms"] * 1e-3) / 1e12
-            roofline = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
-                        "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                        "traffic": traffic.get(top),
-                        "peak_source": f"bf16 sustained, of {peak_src}",
-                        "achieved_basis": "nominal NS FLOPs (2m^2n gram, 2m^3 poly, 2m^2n apply "
-                                          "per view) / event time",
-                        "executed_tflops": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1),
-                        "executed_frac": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12 / peak, 4),
-                        "traffic_unit": "DRAM bytes per launch (ncu, profiles/)"}
-        else:
-            peak = peaks["hbm_gbs"]
-            ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
-            roofline = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
-                        "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic.get(top),
-                        "peak_source": f"HBM copy, of {peak_src}"}
     hbm = {k: v for k, v in kstats.items() if v["flops"] == 0 and v["bytes"] > 0}
-    roofline_hbm = None
-    if hbm:
-        top = max(hbm, key=lambda k: hbm[k]["total_ms"])
-        v = hbm[top]
-        ach = v["bytes"] / (v["total_ms"] * 1e-3) / 1e9
-        roofline_hbm = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1),
-                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic.get(top),
-                        "algorithmic_bytes_per_launch": hbm[top]["bytes"] / max(hbm[top]["launches"], 1),
-                        "peak_source": f"HBM copy, of {peak_src}"}
+    top_hbm = max(hbm, key=lambda k: hbm[k]["total_ms"]) if hbm else None
+    roofline_hbm = (hbm_roofline(top_hbm, hbm[top_hbm], peaks, peak_src, traffic.get(top_hbm))
+                    if top_hbm else None)
+    # The dominant kernel: the Newton-Schulz GEMMs wherever the set has Muon
+    # tensors, AdamW for the AdamW-only set.
+    if "ns_gemm" in kstats:
+        roofline = gemm_roofline(kstats["ns_gemm"], peaks, peak_src, clk, traffic.get("ns_gemm"))
+    else:
+        roofline = roofline_hbm
     stages = {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
                   "tflops_executed": round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)}
               for k, v in stage_stats.items() if "." in k and v["total_ms"] > 0}
@@ -1067,23 +1195,21 @@ def main():
                "pinned": bool(gin.registered and pout.registered)}
         pipe.close()
 
-    # ---- CPU oracle baseline (rank 0, one GPU) -------------------------------------------
+    # ---- CPU oracle baseline: the same sample the reference arm times ----------------------
     cpu = None
     if not args.no_cpu_baseline:
-        views, adam = oracle_sample_plan(wl, muon_flop_budget=1.2e13, adam_elems=1 << 24)
+        views, adam = oracle_plan(wl)
         osample = OracleSample(wl, views, adam, args.max_grad_norm)
         ms_muon, ms_adam, ms_ctl = osample.run()
         cpu_ms = oracle_extrapolated_ms(wl, views, adam, ms_muon, ms_adam, ms_ctl,
                                         osample.grad_elems())
-        cpu = {"value": round(cpu_ms, 1), "unit": "ms/step", "cores": blas_threads(),
-               "kind": "oracle", "sample": sample_desc(wl, views, adam),
-               "sample_seconds": round(ms_muon + ms_adam + ms_ctl, 2)}
+        cpu = cpu_baseline_record(wl, views, adam, osample, ms_muon + ms_adam + ms_ctl, cpu_ms)
 
     line = {
-        "metric": METRIC, "value": round(ms_step, 3), "unit": "ms/step", "n_gpus": 1,
+        "metric": metric_for(wl), "value": round(ms_step, 3), "unit": "ms/step", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_dict(wl, args.max_grad_norm),
+        "data": "synthetic", "config": config_dict(wl, args.max_grad_norm, l2_note),
         "ns_tflops": round(nsf / (ns_ms * 1e-3) / 1e12, 1) if ns_ms > 0 else None,
         "ns_ms_per_step": round(ns_ms, 3),
         "roofline": roofline, "roofline_hbm": roofline_hbm, "kernels": kernels,

@@ -78,3 +78,41 @@ def test_missing_profile_gives_no_records(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(_fake_root(tmp_path)))
     assert bench.traffic_records("absent") == {}
 
+
+
+def test_tensor_peak_follows_the_power_cap():
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+    assert bench.tensor_peak(peaks, "measured", {"reasons": ["sw_power_cap"]})[0] == 1700.0
+    assert bench.tensor_peak(peaks, "measured", {"reasons": []})[0] == 1900.0
+
+
+def test_gemm_roofline_leads_with_executed_flops():
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "hbm_gbs": 6800.0}
+    v = dict(launches=4, total_ms=1000.0, bytes=8e9, flops=2.0e15, flops_executed=1.5e15)
+    r = bench.gemm_roofline(v, peaks, "measured", {"reasons": ["sw_power_cap"]}, traffic=3e9)
+    assert r["achieved"] == 1500.0 and r["frac"] == round(1500.0 / 1600.0, 4)
+    assert r["nominal_tflops"] == 2000.0 and r["nominal_frac"] == 1.25
+    assert r["frac_of_datasheet"] == round(1500.0 / bench.DATASHEET_BF16_TFLOPS, 4)
+    assert r["algorithmic_bytes_per_launch"] == 2e9 and r["traffic"] == 3e9
+
+
+def test_cpu_baseline_and_reference_arm_share_one_sample():
+    for name in ("single", "gpt124m", "llama7b", "moe_mla", "adamw_2p30"):
+        wl = W.WORKLOADS[name]()
+        assert bench.oracle_plan(wl) == bench.oracle_plan(wl)
+        views, adam = bench.oracle_plan(wl)
+        assert sum(f for *_, f in views) <= bench.ORACLE_NS_FLOP_BUDGET
+        assert sum(c for _, c in adam) <= bench.ORACLE_ADAM_ELEMS
+
+
+def test_cpu_baseline_record_states_what_it_covers():
+    wl = W.single_matrix()
+    views, adam = bench.oracle_plan(wl)
+    rec = bench.cpu_baseline_record(wl, views, adam, None, 0.01, 5.0)
+    assert rec["extrapolated"] is False and rec["sample_fraction"]["ns_flops"] == 1.0
+    wl = W.llama7b()
+    views, adam = bench.oracle_plan(wl)
+    rec = bench.cpu_baseline_record(wl, views, adam, None, 8.0, 1e6)
+    assert rec["extrapolated"] is True
+    assert 0 < rec["sample_fraction"]["ns_flops"] < 0.05
+    assert rec["kind"] == "oracle" and rec["cores"] >= 1
