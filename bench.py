@@ -93,22 +93,45 @@ def sources_digest(family: str) -> str:
 
 
 def traffic_records(workload: str) -> dict:
-    """bytes_per_launch of each kernel family from `traffic-record:` lines of
-    profiles/dram_<workload>.md, kept only if the sources still match."""
-    path = os.path.join(ROOT, "profiles", f"dram_{workload}.md")
+    """DRAM traffic of each kernel family from the `traffic-record:` lines of
+    profiles/dram_*.md, kept only if the sources still match. A record gives
+    either bytes_per_launch measured on this very workload, or the ratio of
+    measured to algorithmic bytes on a slice of it (applies_to names the
+    workloads it covers); the caller scales a ratio by its own algorithmic
+    bytes per launch. Returns {family: ("bytes", value) or ("ratio", value)}."""
+    import glob
     out = {}
-    try:
-        with open(path) as f:
-            for line in f:
-                if not line.startswith("traffic-record:"):
-                    continue
-                kv = dict(tok.split("=", 1) for tok in line.split()[1:])
-                fam = kv["kernel"]
-                if fam in KERNEL_SOURCES and kv.get("sources") == sources_digest(fam):
-                    out[fam] = float(kv["bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
-        pass
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "dram_*.md"))):
+        here = os.path.basename(path)[len("dram_"):-len(".md")]
+        try:
+            with open(path) as f:
+                for line in f:
+                    if not line.startswith("traffic-record:"):
+                        continue
+                    kv = dict(tok.split("=", 1) for tok in line.split()[1:])
+                    fam = kv["kernel"]
+                    applies = kv.get("applies_to", here).split(",")
+                    if (workload not in applies or fam not in KERNEL_SOURCES
+                            or kv.get("sources") != sources_digest(fam)):
+                        continue
+                    if "ratio" in kv:
+                        out[fam] = ("ratio", float(kv["ratio"]))
+                    else:
+                        out[fam] = ("bytes", float(kv["bytes_per_launch"]))
+        except (OSError, KeyError, ValueError):
+            continue
     return out
+
+
+def traffic_for(traffic: dict, fam: str, alg_bytes_per_launch: float):
+    """DRAM bytes per launch of a family: measured, or the measured ratio on
+    a slice times this run's algorithmic bytes per launch; None without a
+    valid record."""
+    rec = traffic.get(fam)
+    if rec is None:
+        return None
+    kind, val = rec
+    return round(val * alg_bytes_per_launch) if kind == "ratio" else val
 
 
 def load_peaks():
@@ -802,7 +825,7 @@ def cpu_baseline_record(wl, views, adam, sample, seconds, ms: float) -> dict:
 def metric_for(wl) -> str:
     """The 7B-shape set carries the headline metric; the other sets are named
     by their workload in the same form."""
-    if wl.name.startswith("llama7b"):
+    if wl.name.startswith("llama7b_d4096_l32"):
         return METRIC
     return f"Muon+AdamW step ms ({wl.name}); Newton–Schulz TFLOP/s vs bf16 TC peak"
 
@@ -1129,12 +1152,21 @@ def main():
     traffic = traffic_records(args.workload)
     hbm = {k: v for k, v in kstats.items() if v["flops"] == 0 and v["bytes"] > 0}
     top_hbm = max(hbm, key=lambda k: hbm[k]["total_ms"]) if hbm else None
-    roofline_hbm = (hbm_roofline(top_hbm, hbm[top_hbm], peaks, peak_src, traffic.get(top_hbm))
+    def alg(fam):
+        v = kstats[fam]
+        return v["bytes"] / max(v["launches"], 1)
+    roofline_hbm = (hbm_roofline(top_hbm, hbm[top_hbm], peaks, peak_src,
+                                 traffic_for(traffic, top_hbm, alg(top_hbm)))
                     if top_hbm else None)
     # The dominant kernel: the Newton-Schulz GEMMs wherever the set has Muon
     # tensors, AdamW for the AdamW-only set.
     if "ns_gemm" in kstats:
-        roofline = gemm_roofline(kstats["ns_gemm"], peaks, peak_src, clk, traffic.get("ns_gemm"))
+        roofline = gemm_roofline(kstats["ns_gemm"], peaks, peak_src, clk,
+                                 traffic_for(traffic, "ns_gemm", alg("ns_gemm")))
+        if traffic.get("ns_gemm", ("", 0))[0] == "ratio":
+            roofline["traffic_basis"] = ("measured DRAM bytes / algorithmic bytes on a slice of "
+                                         "this workload (profiles/), times this run's "
+                                         "algorithmic bytes per launch")
     else:
         roofline = roofline_hbm
     stages = {k: {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),

@@ -130,23 +130,33 @@ def gpt124m() -> Workload:
     return Workload("gpt124m_d768_l12", muon, adamw, dict(MUON_HP), dict(ADAM_HP), steps=10)
 
 
-def llama7b() -> Workload:
+def llama7b(layers: int = 32, vocab_rows: int = 128256) -> Workload:
     """d=4096, 32 layers, GQA: Q/O 4096^2, K/V 1024 x 4096, gate_up
     (2, 14336, 4096), down 4096 x 14336 on Muon; untied embedding and head
-    128256 x 4096 plus 65 norms on AdamW; bf16 params/grads, fp32 state."""
+    128256 x 4096 plus 65 norms on AdamW; bf16 params/grads, fp32 state.
+    ``layers`` / ``vocab_rows`` give a slice of the same shapes (profiling)."""
     muon, adamw = [], []
-    for l in range(32):
+    for l in range(layers):
         muon.append(MuonSpec(f"l{l}.q", 1, 4096, 4096))
         muon.append(MuonSpec(f"l{l}.k", 1, 1024, 4096))
         muon.append(MuonSpec(f"l{l}.v", 1, 1024, 4096))
         muon.append(MuonSpec(f"l{l}.o", 1, 4096, 4096))
         muon.append(MuonSpec(f"l{l}.gate_up", 2, 14336, 4096))
         muon.append(MuonSpec(f"l{l}.down", 1, 4096, 14336))
-    adamw.append(AdamSpec("embed", (128256, 4096)))
-    adamw.append(AdamSpec("head", (128256, 4096)))
-    for k in range(65):
+    adamw.append(AdamSpec("embed", (vocab_rows, 4096)))
+    adamw.append(AdamSpec("head", (vocab_rows, 4096)))
+    for k in range(2 * layers + 1):
         adamw.append(AdamSpec(f"norm{k}", (4096,), w_const=1.0))
-    return Workload("llama7b_d4096_l32", muon, adamw, dict(MUON_HP), dict(ADAM_HP), steps=1)
+    name = ("llama7b_d4096_l32" if (layers, vocab_rows) == (32, 128256)
+            else f"llama7b_slice_l{layers}_v{vocab_rows}")
+    return Workload(name, muon, adamw, dict(MUON_HP), dict(ADAM_HP), steps=1)
+
+
+def llama7b_layer() -> Workload:
+    """One layer of the 7B-shape set (every Newton-Schulz shape class, 7 views)
+    with an 8192-row slice of embedding and head: about 3.5 GB on the device,
+    small enough for a multi-pass profile of every kernel of the step."""
+    return llama7b(layers=1, vocab_rows=8192)
 
 
 def llama7b_bf16_state() -> Workload:
@@ -209,6 +219,7 @@ WORKLOADS = {
     "single": single_matrix,
     "gpt124m": gpt124m,
     "llama7b": llama7b,
+    "llama7b_layer": llama7b_layer,
     "llama7b_bf16state": llama7b_bf16_state,
     "gpt124m_bf16state": gpt124m_bf16_state,
     "moe_mla": moe_mla,

@@ -66,7 +66,7 @@ def test_traffic_record_is_dropped_once_its_sources_change(tmp_path, monkeypatch
         f"traffic-record: kernel=adamw bytes_per_launch=1.5e+09 sources={digest}\n"
         "traffic-record: kernel=ns_gemm bytes_per_launch=2.0e+09 sources=0000000000000000\n"
         "traffic-record: kernel=unknown bytes_per_launch=3.0e+09 sources=0000000000000000\n")
-    assert bench.traffic_records("toy") == {"adamw": 1.5e9}
+    assert bench.traffic_records("toy") == {"adamw": ("bytes", 1.5e9)}
     # any byte of any source of the family invalidates the record
     with open(root / "muon_adamw_hybrid_gb300" / "csrc" / "adamw.cu", "a") as f:
         f.write("\n")
@@ -116,3 +116,16 @@ def test_cpu_baseline_record_states_what_it_covers():
     assert rec["extrapolated"] is True
     assert 0 < rec["sample_fraction"]["ns_flops"] < 0.05
     assert rec["kind"] == "oracle" and rec["cores"] >= 1
+
+
+def test_ratio_record_applies_to_named_workloads_and_scales(tmp_path, monkeypatch):
+    root = _fake_root(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    digest = bench.sources_digest("ns_gemm")
+    (root / "profiles" / "dram_slice.md").write_text(
+        f"traffic-record: kernel=ns_gemm ratio=1.25 applies_to=big,slice sources={digest}\n")
+    rec = bench.traffic_records("big")
+    assert rec == {"ns_gemm": ("ratio", 1.25)}
+    assert bench.traffic_for(rec, "ns_gemm", 8e9) == 1e10
+    assert bench.traffic_for(rec, "adamw", 8e9) is None
+    assert bench.traffic_records("other") == {}
