@@ -786,6 +786,23 @@ void set_last_error(const char* msg) { g_err = msg ? msg : ""; }
 std::atomic<long long> g_wait_limit{kWaitLimitCycles};
 long long gemm_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
+bool encode_stream_map(CUtensorMap* tm, const void* base, bool f32, int64_t inner, int64_t rows,
+                       int64_t views, int64_t ld) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(views)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es,
+                           static_cast<cuuint64_t>(ld) * es * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kEwTileC), static_cast<cuuint32_t>(kEwTileR), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mh
 
 using namespace mh;
@@ -876,6 +893,8 @@ int mh_muon_step_batched(const mh_muon_tensor* tensors, int32_t n, const mh_muon
   proto.u_scale_from_sumsq = hp->ns_steps == 0 ? 1 : 0;
   proto.grad_mult = hp->grad_mult;
   proto.skip = hp->skip;
+  proto.status = reinterpret_cast<int*>(ws);
+  proto.wait_limit = gemm_wait_limit();
 
   int final_buf = 0;
   auto fill_common = [&](const TensorInfo& T, EwJob& J, int xbuf) {

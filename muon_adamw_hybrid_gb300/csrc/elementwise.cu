@@ -29,6 +29,7 @@
 // Muon+ row factor; flaxchat step 3, Speedtronic "Muon+").
 #include <atomic>
 #include "mh_internal.h"
+#include "mh_ptx.cuh"
 #include "mh_sr.cuh"
 #include "muonhybrid.h"
 
@@ -709,6 +710,446 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
   }
 }
 
+// ---- streaming passes -------------------------------------------------------
+// The plain apply and the Muon+ column statistics read every element once and
+// (apply) write the parameter once, so they are bound by HBM. Each block (one
+// per SM) runs one producer warp and sixteen consumer warps over its range of
+// 32 x 256 tiles through a ring of shared-memory stages:
+//   producer  waits for a free stage, writes the stage's descriptor (and, at a
+//             tensor boundary, the job record), then issues one TMA box of U
+//             (from the Newton-Schulz buffer) and one of the parameter, each
+//             32 x 256 with zero fill past the tensor's edges, and cp.async
+//             copies of the tile's row and column factors. The stage's full
+//             barrier completes when all have landed: 32 plain arrivals (each
+//             lane's own writes), 32 cp.async arrivals and the boxes' bytes.
+//             The job's fields and the tile coordinates stay in registers
+//             (stepped tile by tile), so a tile costs the producer a few
+//             instructions. (One box per operand: 32 row-sized bulk copies
+//             per tile cost the copy engine about as much time per tile as
+//             the HBM does.)
+//   consumers two groups of eight warps take alternate tiles. A group waits
+//             for the full barrier, computes the tile from shared memory (each
+//             warp 4 rows, each lane 8 columns: a warp reads 512 consecutive
+//             bytes per row, so no bank conflicts), stores the parameter
+//             (apply) and releases the stage (one arrival per warp). The
+//             statistics write each warp's column partials to one of the
+//             group's four reduction buffers and arrive on its mbarrier; the
+//             cross-warp sum of the group's previous tile is taken after this
+//             tile's partials are written, so a warp seldom waits for the
+//             others. Two tiles in the consumers at once halve the share of
+//             each tile's fixed chain of waits and shared-memory round trips.
+// Nothing a consumer waits for is a dependent global load. The apply's step
+// scalars ride on the column factors (decrement lr s U f h, decay 1 - lr wd in
+// one fma), which keeps its instruction count per element near ten: with the
+// sixteen warps it is otherwise bound by instruction issue, not by HBM.
+// Every wait is bounded by the launch's wait limit; on a
+// timeout the block records DEV_TIMEOUT_STREAM in the status word, lets every
+// copy it issued land and returns. A parameter whose rows are not whole
+// aligned 16-byte groups (bf16 with cols % 8 != 0, unaligned storage, an fp32
+// parameter in the bf16 layout) is read directly when the tile is processed,
+// as ew_kernel does.
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool valid) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(sa), "l"(gmem),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Two groups of eight consumer warps (4 rows of a 32-row tile each) and the
+// producer warp: four warps per scheduler keep the per-element latency of the
+// apply hidden.
+constexpr int kStreamGroupWarps = kEwTileR / 4;
+constexpr int kStreamGroups = 2;
+constexpr int kStreamConsumerWarps = kStreamGroups * kStreamGroupWarps;
+constexpr int kStreamThreads = (kStreamConsumerWarps + 1) * 32;
+
+// Stage layout of ew_stream_kernel<KIND, WB> (bytes from the stage's start).
+// WB: parameter bytes per 8 elements (16: bf16, 32: fp32, 0: no parameter).
+template <int KIND, int WB>
+struct StreamLayout {
+  static constexpr bool kApply = KIND == EW_APPLY;
+  static constexpr int kURow = kEwTileC * 2;            // 512 B of bf16 U per row
+  static constexpr int kWRow = kEwTileC / 8 * WB;       // parameter bytes per row
+  static constexpr int kU = 0;
+  static constexpr int kW = kU + kEwTileR * kURow;
+  static constexpr int kC = kW + kEwTileR * kWRow;      // column factors (apply)
+  static constexpr int kR = kC + (kApply ? kEwTileC * 4 : 0);  // row factors
+  static constexpr int kD = kR + kEwTileR * 4;          // descriptor: 4 x int32
+  static constexpr int kStage = (kD + 16 + 127) / 128 * 128;
+  // Column statistics: per consumer group four [warp][256] float reduction
+  // buffers after the stages.
+  static constexpr int kRedBufs = kApply ? 0 : 4;
+  static constexpr int kRedBytes = kStreamGroups * kRedBufs * kStreamGroupWarps * kEwTileC * 4;
+  static constexpr int kBudget = 204800 - kRedBytes;
+  static constexpr int kStages = kBudget / kStage > 8 ? 8 : kBudget / kStage;
+  static constexpr size_t kRed = static_cast<size_t>(kStages) * kStage;
+  static constexpr size_t kSmem = kRed + kRedBytes;
+  static_assert(kStages >= 3, "stage layout too large");
+};
+
+template <int KIND, int WB>
+__host__ __device__ constexpr size_t stream_smem_bytes() {
+  return StreamLayout<KIND, WB>::kSmem + 128;  // + alignment slack
+}
+
+// Whether the parameter rows of a job are bulk-copied: 16-byte aligned storage
+// whose rows are whole 16-byte groups, of a dtype the layout holds.
+template <int WB>
+__device__ __forceinline__ bool stream_w_staged(const EwJob& J) {
+  const bool vec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
+  return vec && (J.dst_dtype == MH_BF16 ? WB >= 16 : WB >= 32);
+}
+
+__device__ __forceinline__ int64_t job_end_tile(const EwJob& J) {
+  return J.tile_begin + J.views * J.tiles_r * J.tiles_c;
+}
+
+// Launch parameters of the streaming passes: the elementwise parameters and,
+// per job, tensor maps of its U view stack and of its parameter (the latter
+// encoded only where stream_w_staged holds).
+struct StreamParams {
+  CUtensorMap tmU[kMaxJobs];
+  CUtensorMap tmW[kMaxJobs];
+  EwParams ew;
+};
+
+template <int KIND, int WB>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    ew_stream_kernel(const __grid_constant__ StreamParams sp) {
+  using L = StreamLayout<KIND, WB>;
+  constexpr int kS = L::kStages;
+  const EwParams& p = sp.ew;
+  extern __shared__ uint8_t stream_smem_raw[];
+  // TMA destinations: 128-byte aligned stage bases (the launch adds the slack).
+  uint8_t* stream_smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(stream_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  __shared__ __align__(16) EwJob sJ[kS];
+  __shared__ __align__(8) uint64_t full[kS], empty[kS], red_bar[kStreamGroups][4];
+  __shared__ int abort_flag;
+  if (step_skipped(p.skip)) return;
+  int64_t tile_begin, tile_end;
+  block_tile_range(p.total_tiles, tile_begin, tile_end);
+  const int64_t ntiles = tile_end - tile_begin;
+  if (ntiles <= 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(&full[s], 64);
+      mbar_init(&empty[s], kStreamGroupWarps);
+    }
+    for (int g = 0; g < kStreamGroups; ++g)
+      for (int b = 0; b < 4; ++b) mbar_init(&red_bar[g][b], kStreamGroupWarps);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* abort_v = &abort_flag;
+
+  if (warp == kStreamConsumerWarps) {
+    // ---- producer warp ----
+    constexpr int kWords = sizeof(EwJob) / 4;
+    static_assert(sizeof(EwJob) % 4 == 0, "EwJob must be a whole number of words");
+    int pj = -1, pseq = -1, slot = 0;
+    int64_t pend = tile_begin;  // forces a job record for the first tile
+    // The job's fields and the tile's coordinates live in registers: they are
+    // reloaded at a tensor boundary and stepped tile by tile, so a tile costs
+    // no shared-memory round trips and no divisions.
+    int64_t rows = 0, cols = 0;
+    int32_t tiles_r = 0, tiles_c = 0;
+    const float* rowfac = nullptr;
+    const float* colfac = nullptr;
+    const int32_t* active = nullptr;
+    uint32_t wbytes = 0;
+    int32_t v = 0, tr = 0, tc = 0;
+    bool new_view = true;
+    const float* rf_view = nullptr;
+    const float* cf_view = nullptr;
+    bool act = true;
+    int64_t issued = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t i = 0; i < ntiles; ++i) {
+      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_v, p.status, DEV_TIMEOUT_STREAM,
+                             p.wait_limit))
+        break;
+      const int64_t tile = tile_begin + i;
+      if (tile >= pend) {  // warp-uniform: the next tensor takes the oldest job slot
+        pj = find_job(p, tile);
+        ++pseq;
+        slot = pseq % kS;
+        for (int w = lane; w < kWords; w += 32)
+          reinterpret_cast<uint32_t*>(&sJ[slot])[w] =
+              reinterpret_cast<const uint32_t*>(&p.jobs[pj])[w];
+        __syncwarp();
+        const EwJob& J = sJ[slot];
+        pend = job_end_tile(J);
+        rows = J.rows;
+        cols = J.cols;
+        tiles_r = J.tiles_r;
+        tiles_c = J.tiles_c;
+        rowfac = J.rowfac;
+        colfac = J.colfac;
+        active = J.active;
+        // A box always completes its full size in bytes, zero-filled or not.
+        wbytes = (WB > 0 && stream_w_staged<WB>(J))
+                     ? kEwTileR * kEwTileC * (J.dst_dtype == MH_F32 ? 4u : 2u)
+                     : 0u;
+        const TileInfo t = tile_info_in(J, pj, tile);
+        v = static_cast<int32_t>(t.v);
+        tr = static_cast<int32_t>(t.r0 / kEwTileR);
+        tc = static_cast<int32_t>(t.c0 / kEwTileC);
+        new_view = true;
+      }
+      if (new_view) {
+        if (KIND == EW_COLSQ || p.use_rowfac) rf_view = rowfac + v * rows;
+        if (KIND == EW_APPLY && p.use_colfac) cf_view = colfac + v * cols;
+        // The active flag: one dependent load per view.
+        if constexpr (KIND == EW_APPLY) act = active == nullptr || active[v] != 0;
+        new_view = false;
+      }
+      const int32_t r0 = tr * kEwTileR, c0 = tc * kEwTileC;
+      uint8_t* st = stream_smem + static_cast<size_t>(stage) * L::kStage;
+      if (lane == 0) {
+        *reinterpret_cast<int4*>(st + L::kD) = make_int4(slot, v, r0, c0 | (act ? 0 : (1 << 30)));
+        if (act) {
+          mbar_expect_tx(&full[stage], kEwTileR * L::kURow + wbytes);
+          tma_load_3d(st + L::kU, &sp.tmU[pj], &full[stage], c0, r0, v);
+          if (wbytes) tma_load_3d(st + L::kW, &sp.tmW[pj], &full[stage], c0, r0, v);
+        }
+      }
+      if (act) {
+        if (KIND == EW_COLSQ || p.use_rowfac) {
+          const bool row_ok = r0 + lane < rows;
+          cp_async4(st + L::kR + lane * 4, row_ok ? rf_view + r0 + lane : rowfac, row_ok);
+        }
+        if constexpr (KIND == EW_APPLY) {
+          if (p.use_colfac) {
+            const int64_t col = c0 + lane * 8;
+            const float* cf = cf_view + col;
+            uint8_t* d = st + L::kC + lane * 32;
+            if (cols - col >= 8 && (reinterpret_cast<uintptr_t>(cf) & 15) == 0) {
+              cp_async16(d, cf, true);
+              cp_async16(d + 16, cf + 4, true);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const bool ok = cols - col > q;
+                cp_async4(d + 4 * q, ok ? cf + q : colfac, ok);
+              }
+            }
+          }
+        }
+      }
+      cp_async_mbar_arrive(&full[stage]);
+      mbar_arrive(&full[stage]);
+      ++issued;
+      if (++stage == kS) { stage = 0; phase ^= 1u; }
+      if (++tc == tiles_c) {
+        tc = 0;
+        if (++tr == tiles_r) {
+          tr = 0;
+          ++v;
+          new_view = true;
+        }
+      }
+    }
+    // Let every copy this warp issued land before the block can leave: the
+    // consumers normally wait for all of them; after an abort nobody does.
+    cp_async_wait_all();
+    for (int64_t j = issued > kS ? issued - kS : 0; j < issued; ++j)
+      mbar_wait_drain(&full[j % kS], static_cast<uint32_t>((j / kS) & 1));
+    return;
+  }
+
+  // ---- consumer warps ----
+  // Group g takes tiles g, g + 2, ...; its k-th tile is tile g + 2k.
+  const int grp = warp / kStreamGroupWarps, gw = warp % kStreamGroupWarps;
+  const int gtid = threadIdx.x - grp * kStreamGroupWarps * 32;  // 0..255 within the group
+  float (*const red_base)[kEwTileC] =
+      reinterpret_cast<float (*)[kEwTileC]>(stream_smem + L::kRed) + grp * 4 * kStreamGroupWarps;
+  // Column statistics: the group's previous tile's output (colpart row
+  // segment, valid cols), kept in registers: its job slot may be reused once
+  // the stage is released.
+  float* prev_out = nullptr;
+  int64_t prev_ncol = 0;
+  // Cross-warp sum of the group's k-th tile: thread gtid sums column gtid
+  // over the eight warps' partials in a fixed order.
+  auto finish = [&](int64_t k, float* out, int64_t ncol) -> bool {
+    if (!mbar_wait_bounded(&red_bar[grp][k & 3], static_cast<uint32_t>((k >> 2) & 1), abort_v,
+                           p.status, DEV_TIMEOUT_STREAM, p.wait_limit))
+      return false;
+    const float (*red)[kEwTileC] = red_base + (k & 3) * kStreamGroupWarps;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kStreamGroupWarps; ++w) sum += red[w][gtid];
+    if (gtid < ncol) out[gtid] = sum;
+    return true;
+  };
+  int64_t k = 0;
+  for (int64_t i = grp; i < ntiles; i += kStreamGroups, ++k) {
+    const int stage = static_cast<int>(i % kS);
+    const uint32_t phase = static_cast<uint32_t>((i / kS) & 1);
+    float* cur_out = nullptr;
+    int64_t cur_ncol = 0;
+    if (!mbar_wait_bounded(&full[stage], phase, abort_v, p.status, DEV_TIMEOUT_STREAM,
+                           p.wait_limit))
+      return;  // aborted: nothing further is written
+    const uint8_t* st = stream_smem + static_cast<size_t>(stage) * L::kStage;
+    const int4 d = *reinterpret_cast<const int4*>(st + L::kD);
+    const EwJob& J = sJ[d.x];
+    TileInfo t;
+    t.job = 0;
+    t.v = d.y;
+    t.r0 = d.z;
+    t.c0 = d.w & ((1 << 30) - 1);
+    const bool act = (d.w >> 30) == 0;
+    if (act) {
+      const int64_t col = t.c0 + lane * 8;
+      const int64_t ncol = J.cols - col;
+      const int nvalid = ncol >= 8 ? 8 : (ncol > 0 ? static_cast<int>(ncol) : 0);
+      // U's scale (1 unless U is the normalised momentum itself) is folded
+      // into the per-row factor.
+      const float uscale = p.u_scale_from_sumsq
+                               ? ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps)
+                               : 1.0f;
+      const int64_t row0 = t.r0 + gw * 4;
+      float u[4][8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(st + L::kU + (gw * 4 + r) * L::kURow + lane * 16);
+        const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          u[r][2 * q] = __uint_as_float(wd[q] << 16);
+          u[r][2 * q + 1] = __uint_as_float(wd[q] & 0xFFFF0000u);
+        }
+      }
+      // Columns past the last and rows past the last are zero in the box;
+      // they are still selected away in the rare ragged tile.
+      if (nvalid < 8 || row0 + 3 >= J.rows) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const bool row_ok = row0 + r < J.rows;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) u[r][q] = (row_ok && q < nvalid) ? u[r][q] : 0.0f;
+        }
+      }
+      float fr[4] = {1.f, 1.f, 1.f, 1.f};
+      if (KIND == EW_COLSQ || p.use_rowfac) {
+        const float4 f4 = *reinterpret_cast<const float4*>(st + L::kR + gw * 16);
+        fr[0] = f4.x; fr[1] = f4.y; fr[2] = f4.z; fr[3] = f4.w;
+      }
+      if constexpr (KIND == EW_COLSQ) {
+        float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float f = fr[r] * uscale;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float x = f * u[r][q];
+            cs[q] += x * x;
+          }
+        }
+        float (*red)[kEwTileC] = red_base + (k & 3) * kStreamGroupWarps;
+        *reinterpret_cast<float4*>(&red[gw][lane * 8]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+        *reinterpret_cast<float4*>(&red[gw][lane * 8 + 4]) = make_float4(cs[4], cs[5], cs[6], cs[7]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_bar[grp][k & 3]);
+        cur_out = J.colpart + (t.v * J.tiles_r + t.r0 / kEwTileR) * J.cols + t.c0;
+        cur_ncol = J.cols - t.c0;
+      } else {
+        const bool dvec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
+        const bool wst = stream_w_staged<WB>(J);
+        const int wrow = kEwTileC * (J.dst_dtype == MH_F32 ? 4 : 2);  // box row pitch
+        // The step's scalars ride on the column factors: ga = lr s U_ij f_i h_j
+        // is the decrement, keep = 1 - lr wd the decay.
+        const float lrs = J.lr * J.shape_scale * uscale;
+        const float keep = 1.0f - J.lr * J.wd;
+        float hs[8];
+        if (p.use_colfac) {
+          const float4 a = *reinterpret_cast<const float4*>(st + L::kC + lane * 32);
+          const float4 b = *reinterpret_cast<const float4*>(st + L::kC + lane * 32 + 16);
+          hs[0] = a.x * lrs; hs[1] = a.y * lrs; hs[2] = a.z * lrs; hs[3] = a.w * lrs;
+          hs[4] = b.x * lrs; hs[5] = b.y * lrs; hs[6] = b.z * lrs; hs[7] = b.w * lrs;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) hs[q] = lrs;
+        }
+        const bool cautious_wd = p.cautious == MH_CAUTIOUS_WD;
+        const int64_t view_elem0 = t.v * J.rows * J.cols;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int64_t row = row0 + r;
+          if (row >= J.rows || nvalid == 0) continue;
+          const int64_t off = view_elem0 + row * J.cols + col;
+          float w[8];
+          if (wst) {
+            const uint8_t* ws = st + L::kW + (gw * 4 + r) * wrow;
+            if (J.dst_dtype == MH_BF16) {
+              const uint4 wr = *reinterpret_cast<const uint4*>(ws + lane * 16);
+              const uint32_t wd4[4] = {wr.x, wr.y, wr.z, wr.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                w[2 * q] = __uint_as_float(wd4[q] << 16);
+                w[2 * q + 1] = __uint_as_float(wd4[q] & 0xFFFF0000u);
+              }
+            } else {
+              const float4 a = *reinterpret_cast<const float4*>(ws + lane * 32);
+              const float4 b = *reinterpret_cast<const float4*>(ws + lane * 32 + 16);
+              w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+              w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            }
+          } else {
+            load8(J.dst, J.dst_dtype, off, nvalid, dvec, w);
+          }
+          const float f = fr[r];
+          if (cautious_wd) {
+            // Weight decay only where the update and the weight agree in sign
+            // (lr s f h >= 0, so ga has the sign of the update direction).
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float ga = u[r][q] * f * hs[q];
+              w[q] = fmaf(w[q], ga * w[q] >= 0.0f ? keep : 1.0f, -ga);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w[q] = fmaf(w[q], keep, -(u[r][q] * f * hs[q]));
+          }
+          if (J.param_sr && J.dst_dtype == MH_BF16)
+            store_bf16_sr<8>(static_cast<bf16*>(J.dst) + off, nvalid, dvec, w, J.param_key,
+                             static_cast<uint64_t>(off));
+          else
+            store8(J.dst, J.dst_dtype, off, nvalid, dvec, w);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if constexpr (KIND == EW_COLSQ) {
+      // Buffer (k - 1) & 3 is rewritten by the group's tile k + 3 only after
+      // every warp of the group has arrived for tile k + 1, which each does
+      // after this sum.
+      if (k > 0 && !finish(k - 1, prev_out, prev_ncol)) return;
+      prev_out = cur_out;
+      prev_ncol = cur_ncol;
+    }
+  }
+  if constexpr (KIND == EW_COLSQ) {
+    if (k > 0) finish(k - 1, prev_out, prev_ncol);
+  }
+}
+
 // Inactive-expert rule: marks each view of a flagged tensor that has a
 // nonzero gradient entry. Chunks of views already marked are skipped, so an
 // active view usually costs one chunk; a silent view is read once in full.
@@ -907,6 +1348,53 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
     case EW_APPLY: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY>); break;
     case EW_APPLY_CU: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY_CU>); break;
     case EW_COPYOUT: fn = reinterpret_cast<const void*>(ew_kernel<EW_COPYOUT>); break;
+  }
+  // The plain apply (no cautious-update mask) and the Muon+ column statistics
+  // take the streaming kernel when the launch has a status word for its
+  // bounded waits: one block per SM, the stage layout sized for the
+  // parameter dtypes of the launch.
+  if ((kind == EW_APPLY || kind == EW_COLSQ) && p.status != nullptr) {
+    bool any_f32 = false;
+    for (int j = 0; j < p.njobs; ++j) any_f32 = any_f32 || p.jobs[j].dst_dtype == MH_F32;
+    const void* ks[3] = {reinterpret_cast<const void*>(ew_stream_kernel<EW_COLSQ, 0>),
+                         reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY, 16>),
+                         reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY, 32>)};
+    const size_t sz[3] = {stream_smem_bytes<EW_COLSQ, 0>(), stream_smem_bytes<EW_APPLY, 16>(),
+                          stream_smem_bytes<EW_APPLY, 32>()};
+    const int which = kind == EW_COLSQ ? 0 : (any_f32 ? 2 : 1);
+    static thread_local int configured = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured != dev) {
+      for (int k = 0; k < 3; ++k) {
+        e = cudaFuncSetAttribute(ks[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sz[k]));
+        if (e != cudaSuccess) return e;
+      }
+      configured = dev;
+    }
+    // Per job: the U view stack (row pitch ldx, zero fill past cols and
+    // rows) and, where the apply stages it, the parameter.
+    static thread_local StreamParams sp;
+    bool maps_ok = true;
+    for (int j = 0; j < p.njobs && maps_ok; ++j) {
+      const EwJob& J = p.jobs[j];
+      maps_ok = encode_stream_map(&sp.tmU[j], J.xf, false, J.cols, J.rows, J.views, J.ldx);
+      const bool wst = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0) &&
+                       (J.dst_dtype == MH_BF16 || any_f32);
+      if (maps_ok && kind == EW_APPLY && wst)
+        maps_ok = encode_stream_map(&sp.tmW[j], J.dst, J.dst_dtype == MH_F32, J.cols, J.rows,
+                                    J.views, J.cols);
+    }
+    if (maps_ok) {
+      sp.ew = p;
+      const int grid = static_cast<int>(p.total_tiles < num_sms ? p.total_tiles : num_sms);
+      void* args[] = {&sp};
+      e = cudaLaunchKernel(ks[which], dim3(grid), dim3(kStreamThreads), args, sz[which], s);
+      if (e != cudaSuccess) return e;
+      return cudaGetLastError();
+    }
   }
   const int per_sm = blocks_per_sm(kind, fn);
   const int64_t want = static_cast<int64_t>(num_sms) * per_sm;

@@ -92,6 +92,10 @@ struct EwParams {
   int32_t u_scale_from_sumsq;  // ns_steps == 0: U = X0
   const float* grad_mult;      // device: gradients are read as g * (*grad_mult), or null
   const int32_t* skip;         // device: *skip != 0 -> the kernel returns at once, or null
+  int* status;                 // device status word for bounded-wait timeouts, or null:
+                               // the streaming apply / column-statistics kernel runs only
+                               // with one (its waits report through it)
+  long long wait_limit;        // cycles a bounded wait may take before the launch aborts
 };
 
 // 1 / (||Q|| * norm_scale + eps), or 0 for a zero matrix with eps 0.
@@ -193,6 +197,13 @@ struct ActiveParams {
 cudaError_t launch_view_active(const ActiveParams& p, int num_sms, cudaStream_t s);
 
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s);
+
+// Tensor map over `views` stacked (rows x inner) matrices of row pitch `ld`
+// elements (bf16, or fp32 when `f32`), box 256 x 32 x 1, no swizzle, zero
+// fill: the tiles of the streaming elementwise passes. False if the driver
+// cannot encode it (the caller then takes the register-staged kernel).
+bool encode_stream_map(CUtensorMap* tm, const void* base, bool f32, int64_t inner, int64_t rows,
+                       int64_t views, int64_t ld);
 cudaError_t launch_row_finalize(const RowFinParams& p, cudaStream_t s);
 cudaError_t launch_col_finalize(const ColFinParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_view_norm(const NormParams& p, cudaStream_t s);

@@ -9,7 +9,13 @@
 namespace mh {
 
 // Device status codes written to the workspace status word.
-enum : int { DEV_OK = 0, DEV_TIMEOUT_TMA = 1, DEV_TIMEOUT_MMA = 2, DEV_TIMEOUT_EPI = 3 };
+enum : int {
+  DEV_OK = 0,
+  DEV_TIMEOUT_TMA = 1,      // a GEMM producer waited too long for a free stage
+  DEV_TIMEOUT_MMA = 2,      // a GEMM MMA issuer waited too long for operands / accumulators
+  DEV_TIMEOUT_EPI = 3,      // a GEMM epilogue waited too long for an accumulator
+  DEV_TIMEOUT_STREAM = 4    // a streaming elementwise pass waited too long for a stage
+};
 
 // A bounded wait gives up after this many SM clock cycles (about 1 s at the
 // GB300's clocks) unless the launch sets its own limit; no legitimate wait in
@@ -193,6 +199,22 @@ __device__ __forceinline__ void st_async_u32(const void* local, uint32_t cta, ui
 // cluster.
 __device__ __forceinline__ void st_cluster_u32(const void* local, uint32_t cta, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_map(local, cta)), "r"(v)
+               : "memory");
+}
+
+// Adds `bytes` to the transaction count of the mbarrier's current phase
+// without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Arrives on `bar` once every cp.async this thread issued so far has landed.
+// The arrival is not counted in advance (.noinc): the barrier's expected
+// count includes it.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
 }
 
