@@ -727,17 +727,18 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
 //             instructions. (One box per operand: 32 row-sized bulk copies
 //             per tile cost the copy engine about as much time per tile as
 //             the HBM does.)
-//   consumers two groups of eight warps take alternate tiles. A group waits
-//             for the full barrier, computes the tile from shared memory (each
-//             warp 4 rows, each lane 8 columns: a warp reads 512 consecutive
-//             bytes per row, so no bank conflicts), stores the parameter
+//   consumers groups of warps take turns with the tiles (apply: two groups of
+//             eight warps, 4 rows each; statistics: four groups of four warps,
+//             8 rows each). A group waits for the full barrier, computes the
+//             tile from shared memory (each lane 8 columns: a warp reads 512
+//             consecutive bytes per row, so no bank conflicts), stores the
 //             (apply) and releases the stage (one arrival per warp). The
 //             statistics write each warp's column partials to one of the
 //             group's four reduction buffers and arrive on its mbarrier; the
 //             cross-warp sum of the group's previous tile is taken after this
 //             tile's partials are written, so a warp seldom waits for the
-//             others. Two tiles in the consumers at once halve the share of
-//             each tile's fixed chain of waits and shared-memory round trips.
+//             others. Several tiles in the consumers at once share out each
+//             tile's fixed chain of waits and shared-memory round trips.
 // Nothing a consumer waits for is a dependent global load. The apply's step
 // scalars ride on the column factors (decrement lr s U f h, decay 1 - lr wd in
 // one fma), which keeps its instruction count per element near ten: with the
@@ -765,13 +766,20 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Two groups of eight consumer warps (4 rows of a 32-row tile each) and the
-// producer warp: four warps per scheduler keep the per-element latency of the
-// apply hidden.
-constexpr int kStreamGroupWarps = kEwTileR / 4;
-constexpr int kStreamGroups = 2;
-constexpr int kStreamConsumerWarps = kStreamGroups * kStreamGroupWarps;
+// Sixteen consumer warps and the producer warp: four warps per scheduler keep
+// the per-element latency of the apply hidden. The apply splits them into two
+// groups of eight (4 rows of a 32-row tile each); the column statistics, with
+// little work per element and a fixed chain per tile, into four groups of
+// four (8 rows each).
+constexpr int kStreamConsumerWarps = 16;
 constexpr int kStreamThreads = (kStreamConsumerWarps + 1) * 32;
+template <int KIND>
+struct StreamGroups {
+  static constexpr int kGroups = KIND == EW_COLSQ ? 4 : 2;
+  static constexpr int kWarps = kStreamConsumerWarps / kGroups;  // per group
+  static constexpr int kRows = kEwTileR / kWarps;                // per warp
+  static_assert(kRows % 4 == 0, "row factors are read four at a time");
+};
 
 // Stage layout of ew_stream_kernel<KIND, WB> (bytes from the stage's start).
 // WB: parameter bytes per 8 elements (16: bf16, 32: fp32, 0: no parameter).
@@ -787,9 +795,9 @@ struct StreamLayout {
   static constexpr int kD = kR + kEwTileR * 4;          // descriptor: 4 x int32
   static constexpr int kStage = (kD + 16 + 127) / 128 * 128;
   // Column statistics: per consumer group four [warp][256] float reduction
-  // buffers after the stages.
+  // buffers after the stages (sixteen warps' rows in all).
   static constexpr int kRedBufs = kApply ? 0 : 4;
-  static constexpr int kRedBytes = kStreamGroups * kRedBufs * kStreamGroupWarps * kEwTileC * 4;
+  static constexpr int kRedBytes = kRedBufs * kStreamConsumerWarps * kEwTileC * 4;
   static constexpr int kBudget = 204800 - kRedBytes;
   static constexpr int kStages = kBudget / kStage > 8 ? 8 : kBudget / kStage;
   static constexpr size_t kRed = static_cast<size_t>(kStages) * kStage;
@@ -827,6 +835,7 @@ template <int KIND, int WB>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     ew_stream_kernel(const __grid_constant__ StreamParams sp) {
   using L = StreamLayout<KIND, WB>;
+  using G = StreamGroups<KIND>;
   constexpr int kS = L::kStages;
   const EwParams& p = sp.ew;
   extern __shared__ uint8_t stream_smem_raw[];
@@ -834,7 +843,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   uint8_t* stream_smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(stream_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
   __shared__ __align__(16) EwJob sJ[kS];
-  __shared__ __align__(8) uint64_t full[kS], empty[kS], red_bar[kStreamGroups][4];
+  __shared__ __align__(8) uint64_t full[kS], empty[kS], red_bar[G::kGroups][4];
   __shared__ int abort_flag;
   if (step_skipped(p.skip)) return;
   int64_t tile_begin, tile_end;
@@ -845,10 +854,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kS; ++s) {
       mbar_init(&full[s], 64);
-      mbar_init(&empty[s], kStreamGroupWarps);
+      mbar_init(&empty[s], G::kWarps);
     }
-    for (int g = 0; g < kStreamGroups; ++g)
-      for (int b = 0; b < 4; ++b) mbar_init(&red_bar[g][b], kStreamGroupWarps);
+    for (int g = 0; g < G::kGroups; ++g)
+      for (int b = 0; b < 4; ++b) mbar_init(&red_bar[g][b], G::kWarps);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -972,31 +981,35 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   }
 
   // ---- consumer warps ----
-  // Group g takes tiles g, g + 2, ...; its k-th tile is tile g + 2k.
-  const int grp = warp / kStreamGroupWarps, gw = warp % kStreamGroupWarps;
-  const int gtid = threadIdx.x - grp * kStreamGroupWarps * 32;  // 0..255 within the group
+  // Group g takes tiles g, g + kGroups, ...; its k-th tile is g + k kGroups.
+  constexpr int kR = G::kRows;
+  const int grp = warp / G::kWarps, gw = warp % G::kWarps;
+  const int gtid = threadIdx.x - grp * G::kWarps * 32;  // thread within the group
   float (*const red_base)[kEwTileC] =
-      reinterpret_cast<float (*)[kEwTileC]>(stream_smem + L::kRed) + grp * 4 * kStreamGroupWarps;
+      reinterpret_cast<float (*)[kEwTileC]>(stream_smem + L::kRed) + grp * 4 * G::kWarps;
   // Column statistics: the group's previous tile's output (colpart row
   // segment, valid cols), kept in registers: its job slot may be reused once
   // the stage is released.
   float* prev_out = nullptr;
   int64_t prev_ncol = 0;
-  // Cross-warp sum of the group's k-th tile: thread gtid sums column gtid
-  // over the eight warps' partials in a fixed order.
+  // Cross-warp sum of the group's k-th tile: each column summed over the
+  // group's warps' partials in a fixed order.
   auto finish = [&](int64_t k, float* out, int64_t ncol) -> bool {
     if (!mbar_wait_bounded(&red_bar[grp][k & 3], static_cast<uint32_t>((k >> 2) & 1), abort_v,
                            p.status, DEV_TIMEOUT_STREAM, p.wait_limit))
       return false;
-    const float (*red)[kEwTileC] = red_base + (k & 3) * kStreamGroupWarps;
-    float sum = 0.0f;
+    const float (*red)[kEwTileC] = red_base + (k & 3) * G::kWarps;
 #pragma unroll
-    for (int w = 0; w < kStreamGroupWarps; ++w) sum += red[w][gtid];
-    if (gtid < ncol) out[gtid] = sum;
+    for (int c = gtid; c < kEwTileC; c += G::kWarps * 32) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < G::kWarps; ++w) sum += red[w][c];
+      if (c < ncol) out[c] = sum;
+    }
     return true;
   };
   int64_t k = 0;
-  for (int64_t i = grp; i < ntiles; i += kStreamGroups, ++k) {
+  for (int64_t i = grp; i < ntiles; i += G::kGroups, ++k) {
     const int stage = static_cast<int>(i % kS);
     const uint32_t phase = static_cast<uint32_t>((i / kS) & 1);
     float* cur_out = nullptr;
@@ -1022,12 +1035,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       const float uscale = p.u_scale_from_sumsq
                                ? ns_inv_norm(J.sumsq[t.v], p.ns_norm_scale, p.ns_eps)
                                : 1.0f;
-      const int64_t row0 = t.r0 + gw * 4;
-      float u[4][8];
+      const int64_t row0 = t.r0 + gw * kR;
+      float u[kR][8];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < kR; ++r) {
         const uint4 raw =
-            *reinterpret_cast<const uint4*>(st + L::kU + (gw * 4 + r) * L::kURow + lane * 16);
+            *reinterpret_cast<const uint4*>(st + L::kU + (gw * kR + r) * L::kURow + lane * 16);
         const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1037,23 +1050,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       }
       // Columns past the last and rows past the last are zero in the box;
       // they are still selected away in the rare ragged tile.
-      if (nvalid < 8 || row0 + 3 >= J.rows) {
+      if (nvalid < 8 || row0 + kR - 1 >= J.rows) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < kR; ++r) {
           const bool row_ok = row0 + r < J.rows;
 #pragma unroll
           for (int q = 0; q < 8; ++q) u[r][q] = (row_ok && q < nvalid) ? u[r][q] : 0.0f;
         }
       }
-      float fr[4] = {1.f, 1.f, 1.f, 1.f};
+      float fr[kR];
+#pragma unroll
+      for (int r = 0; r < kR; ++r) fr[r] = 1.0f;
       if (KIND == EW_COLSQ || p.use_rowfac) {
-        const float4 f4 = *reinterpret_cast<const float4*>(st + L::kR + gw * 16);
-        fr[0] = f4.x; fr[1] = f4.y; fr[2] = f4.z; fr[3] = f4.w;
+#pragma unroll
+        for (int r = 0; r < kR; r += 4) {
+          const float4 f4 = *reinterpret_cast<const float4*>(st + L::kR + (gw * kR + r) * 4);
+          fr[r] = f4.x; fr[r + 1] = f4.y; fr[r + 2] = f4.z; fr[r + 3] = f4.w;
+        }
       }
       if constexpr (KIND == EW_COLSQ) {
         float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < kR; ++r) {
           const float f = fr[r] * uscale;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -1061,7 +1079,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             cs[q] += x * x;
           }
         }
-        float (*red)[kEwTileC] = red_base + (k & 3) * kStreamGroupWarps;
+        float (*red)[kEwTileC] = red_base + (k & 3) * G::kWarps;
         *reinterpret_cast<float4*>(&red[gw][lane * 8]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
         *reinterpret_cast<float4*>(&red[gw][lane * 8 + 4]) = make_float4(cs[4], cs[5], cs[6], cs[7]);
         __syncwarp();
@@ -1089,13 +1107,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         const bool cautious_wd = p.cautious == MH_CAUTIOUS_WD;
         const int64_t view_elem0 = t.v * J.rows * J.cols;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < kR; ++r) {
           const int64_t row = row0 + r;
           if (row >= J.rows || nvalid == 0) continue;
           const int64_t off = view_elem0 + row * J.cols + col;
           float w[8];
           if (wst) {
-            const uint8_t* ws = st + L::kW + (gw * 4 + r) * wrow;
+            const uint8_t* ws = st + L::kW + (gw * kR + r) * wrow;
             if (J.dst_dtype == MH_BF16) {
               const uint4 wr = *reinterpret_cast<const uint4*>(ws + lane * 16);
               const uint32_t wd4[4] = {wr.x, wr.y, wr.z, wr.w};
