@@ -180,18 +180,24 @@ def gpt124m_bf16_state() -> Workload:
     return wl
 
 
-def moe_mla() -> Workload:
+def moe_mla(experts: int = 64) -> Workload:
     """One MoE layer with 64 experts (gate_up (2, 1408, 2048) as two wide
     views, down 2048 x 1408 tall) and the MLA kv up-projection, 32 heads x
     (128 K + 128 V rows) x 512, as 64 views of 128 x 512. NorMuon (beta2 0.95),
     Muon+ row_col and cautious weight decay on."""
     muon = []
-    for e in range(64):
+    for e in range(experts):
         muon.append(MuonSpec(f"e{e}.gate_up", 2, 1408, 2048))
         muon.append(MuonSpec(f"e{e}.down", 1, 2048, 1408))
     muon.append(MuonSpec("mla.kv_b", 64, 128, 512))
     hp = dict(MUON_HP, normuon=True, beta2=0.95, muon_plus=True, cautious=1)
-    return Workload("moe64_mla_all_variants", muon, [], hp, dict(ADAM_HP), steps=1)
+    return Workload(f"moe{experts}_mla_all_variants", muon, [], hp, dict(ADAM_HP), steps=1)
+
+
+def moe_mla_e16() -> Workload:
+    """The same layer with 16 experts (about 1.2 GB of parameters, gradients
+    and momentum): a profiler-sized case of the same passes."""
+    return moe_mla(16)
 
 
 def ns_sweep_shapes(max_x_bytes: int = 64 * 2 ** 30):
@@ -223,6 +229,7 @@ WORKLOADS = {
     "llama7b_bf16state": llama7b_bf16_state,
     "gpt124m_bf16state": gpt124m_bf16_state,
     "moe_mla": moe_mla,
+    "moe_mla_e16": moe_mla_e16,
     "adamw_2p30": adamw_2p30,
 }
 

@@ -8,6 +8,9 @@
   are the same launch (fused update, or row sums under NorMuon).
 * The cautious-update mask under NorMuon / Muon+ (the separate apply pass's
   own instantiation, which reads the gradient).
+* bf16 and fp32 parameters in one NorMuon / Muon+ apply launch: the streaming
+  pass's fp32 stage layout holding bf16 tiles, and a bf16 parameter whose
+  rows are not whole 16-byte groups (read directly instead of staged).
 * A call mixing empty tensors (zero rows, zero views' worth of elements) with
   ordinary ones: the empty ones are skipped, the rest match the oracle.
 """
@@ -89,11 +92,13 @@ def test_ragged_shapes_full_step(flags):
 # the separate apply pass.
 MIXED = [W.MuonSpec("m1", 1, 256, 512, "bf16", "f32", w_std=1.0, g_std=1.0),
          W.MuonSpec("m2", 2, 300, 128, "bf16", "f32", w_std=1.0, g_std=1.0),
-         W.MuonSpec("m3", 1, 96, 200, "f32", "bf16", w_std=1.0, g_std=1.0)]
+         W.MuonSpec("m3", 1, 96, 200, "f32", "bf16", w_std=1.0, g_std=1.0),
+         W.MuonSpec("m4", 1, 64, 100, "bf16", "bf16", w_std=0.02, g_std=1.0)]
 
 
 @pytest.mark.parametrize("flags", [dict(cautious=2), dict(cautious=1),
-                                   dict(normuon=True, cautious=2)])
+                                   dict(normuon=True, cautious=2), dict(normuon=True),
+                                   dict(normuon=True, muon_plus=True, cautious=1)])
 def test_mixed_dtypes_with_cautious_masks(flags):
     wl = _wl(MIXED, **flags)
     run = DeviceRun(wl)

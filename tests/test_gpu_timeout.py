@@ -1,4 +1,5 @@
-"""The bounded-wait failure path of the Newton-Schulz GEMM stages, on the GPU.
+"""The bounded-wait failure path of the Newton-Schulz GEMM stages and of the
+streaming apply / column-statistics passes, on the GPU.
 
 Every wait of a GEMM stage gives up after mh_set_wait_limit cycles; the
 launch then records MH_ETIMEOUT in the workspace status word, lets the copies
@@ -8,7 +9,9 @@ block of a 4096-deep contraction (64 k-steps of MMAs, some tens of
 microseconds), so the call must report the timeout; nothing faults, traps or
 waits without a bound. With the default restored,
 the same call on the same workspace then succeeds and matches the oracle, so
-the context stays usable.
+the context stays usable. A whole NorMuon + Muon+ step (GEMM stages and the
+streaming passes, whose waits take the same limit) is run the same way, with
+its state put back before the clean step.
 """
 import numpy as np
 import pytest
@@ -60,3 +63,33 @@ def test_short_wait_limit_times_out_then_a_normal_call_succeeds(shape):
     mh.workspace_status(ws.data_ptr(), stream)
     torch.cuda.synchronize()
     assert rel_fro(to_np(out), oracle.newton_schulz(q)) < 2e-2
+
+
+@pytest.mark.gpu
+def test_short_wait_limit_in_a_full_step_then_a_clean_step():
+    import torch
+    from muon_adamw_hybrid_gb300 import _lib
+    from synth import workloads as W
+    from tests.helpers import DeviceRun
+    from tests.test_gpu_muon import _check, _wl
+    wl = _wl([W.MuonSpec("t", 2, 1024, 4096, "bf16", "bf16")], normuon=True, muon_plus=True,
+             cautious=1)
+    run = DeviceRun(wl)
+    state = run.mW + run.mB + [s for s in run.sm if s is not None]
+    saved = [t.clone() for t in state]
+    stream = torch.cuda.current_stream().cuda_stream
+    try:
+        _lib.set_wait_limit(2000)
+        run.step()
+        rc = _lib.LIB.mh_workspace_status(run.ws.data_ptr(), stream)
+        assert rc == _lib.MH_ETIMEOUT, (rc, _lib.last_error())
+    finally:
+        _lib.set_wait_limit(0)
+    torch.cuda.synchronize()
+    for t, c in zip(state, saved):
+        t.copy_(c)
+    run.step_count = 0
+    run.step()
+    run.status_ok()
+    torch.cuda.synchronize()
+    _check(wl, run)
