@@ -28,6 +28,8 @@
 // Plus the per-view row finalisation (NorMuon state update, norm restore,
 // Muon+ row factor; flaxchat step 3, Speedtronic "Muon+").
 #include <atomic>
+#include <cstring>
+#include <unordered_map>
 #include "mh_internal.h"
 #include "mh_ptx.cuh"
 #include "mh_sr.cuh"
@@ -1346,6 +1348,42 @@ int blocks_per_sm(EwKind kind, const void* kernel) {
   return b;
 }
 
+// Tensor maps of the streaming passes, per host thread: a map depends only on
+// the base address, the dtype, the extents and the row pitch, so a step that
+// is called again on the same tensors encodes nothing.
+struct StreamMapKey {
+  const void* base;
+  int64_t inner, rows, views, ld;
+  bool f32;
+  bool operator==(const StreamMapKey& o) const {
+    return base == o.base && inner == o.inner && rows == o.rows && views == o.views &&
+           ld == o.ld && f32 == o.f32;
+  }
+};
+struct StreamMapKeyHash {
+  size_t operator()(const StreamMapKey& k) const {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+    for (int64_t v : {k.inner, k.rows, k.views, k.ld, static_cast<int64_t>(k.f32)})
+      h = (h ^ static_cast<uint64_t>(v)) * 0x100000001B3ull;
+    return static_cast<size_t>(h ^ (h >> 29));
+  }
+};
+
+static bool cached_stream_map(CUtensorMap* tm, const void* base, bool f32, int64_t inner,
+                              int64_t rows, int64_t views, int64_t ld) {
+  static thread_local std::unordered_map<StreamMapKey, CUtensorMap, StreamMapKeyHash> cache;
+  const StreamMapKey key{base, inner, rows, views, ld, f32};
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    std::memcpy(tm, &it->second, sizeof(CUtensorMap));
+    return true;
+  }
+  if (!encode_stream_map(tm, base, f32, inner, rows, views, ld)) return false;
+  if (cache.size() >= 4096) cache.clear();  // bounded: tensors come and go
+  cache.emplace(key, *tm);
+  return true;
+}
+
 cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
   if (kind == EW_APPLY && p.cautious == MH_CAUTIOUS_UPDATE) kind = EW_APPLY_CU;
@@ -1398,11 +1436,11 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
     bool maps_ok = true;
     for (int j = 0; j < p.njobs && maps_ok; ++j) {
       const EwJob& J = p.jobs[j];
-      maps_ok = encode_stream_map(&sp.tmU[j], J.xf, false, J.cols, J.rows, J.views, J.ldx);
+      maps_ok = cached_stream_map(&sp.tmU[j], J.xf, false, J.cols, J.rows, J.views, J.ldx);
       const bool wst = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0) &&
                        (J.dst_dtype == MH_BF16 || any_f32);
       if (maps_ok && kind == EW_APPLY && wst)
-        maps_ok = encode_stream_map(&sp.tmW[j], J.dst, J.dst_dtype == MH_F32, J.cols, J.rows,
+        maps_ok = cached_stream_map(&sp.tmW[j], J.dst, J.dst_dtype == MH_F32, J.cols, J.rows,
                                     J.views, J.cols);
     }
     if (maps_ok) {
