@@ -399,13 +399,15 @@ int mh_profiler_read(mh_kernel_stats* out, int32_t max, int32_t* count);
  * bounded wait gave up (its outputs are then undefined). */
 int mh_workspace_status(const void* workspace, void* stream);
 
-/* Bounded waits of the Newton-Schulz GEMM stages. The pages have no
- * counterpart: every wait of a GEMM stage on its pipeline (operand loads,
- * MMAs, accumulators, the pair's shared block sequence) gives up after this
- * many SM clock cycles; the launch then records MH_ETIMEOUT in the workspace
- * status word (mh_workspace_status), lets whatever copies and MMAs it had
- * issued land, frees its tensor memory and returns, and the call's outputs
- * are undefined. The default, about one second at GB300 clocks, is far above
+/* Bounded waits of the Newton-Schulz GEMM stages and of the streaming
+ * NorMuon / Muon+ apply and column-statistics passes of mh_muon_step_batched.
+ * The pages have no counterpart: every wait of such a launch on its pipeline
+ * (operand loads, MMAs, accumulators, the pair's shared block sequence, a
+ * stage of the streaming ring) gives up after this many SM clock cycles; the
+ * launch then records MH_ETIMEOUT in the workspace status word
+ * (mh_workspace_status), lets whatever copies and MMAs it had issued land,
+ * frees its tensor memory and returns, and the call's outputs are
+ * undefined. The default, about one second at GB300 clocks, is far above
  * any legitimate wait. A smaller value makes the failure path observable in
  * a test without a fault or a hang.
  *   cycles: > 0 sets the limit for launches enqueued from now on, process
