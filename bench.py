@@ -78,6 +78,8 @@ def parse_args():
 KERNEL_SOURCES = {
     "ns_gemm": ["ns_gemm.cu", "mh_ptx.cuh", "mh_internal.h", "mh_sr.cuh"],
     "muon_prologue": ["elementwise.cu", "mh_internal.h", "mh_sr.cuh"],
+    "muon_apply": ["elementwise.cu", "mh_ptx.cuh", "mh_internal.h", "mh_sr.cuh"],
+    "muon_colstats": ["elementwise.cu", "mh_ptx.cuh", "mh_internal.h"],
     "adamw": ["adamw.cu", "mh_internal.h", "mh_sr.cuh"],
     "grad_norm": ["grad_control.cu", "mh_internal.h"],
 }
@@ -939,7 +941,13 @@ def run_ns_only(args):
     ks = family_stats(mh.profiler_read())
     m_, n_ = min(r, c), max(r, c)
     flops = b * 5 * (4.0 * m_ * m_ * n_ + 2.0 * m_ ** 3)
-    roofline = gemm_roofline(ks["ns_gemm"], peaks, peak_src, clk) if "ns_gemm" in ks else None
+    ns_workload = f"ns_{args.ns_aspect}_n{n}_batch{b}"
+    traffic = traffic_records(ns_workload)
+    roofline = None
+    if "ns_gemm" in ks:
+        v = ks["ns_gemm"]
+        roofline = gemm_roofline(v, peaks, peak_src, clk,
+                                 traffic_for(traffic, "ns_gemm", v["bytes"] / max(v["launches"], 1)))
 
     # End to end: the batch copied in from page-locked host memory, the call,
     # and the result copied back, every call.
@@ -1186,6 +1194,7 @@ def main():
             kernels[name]["tflops_executed"] = round(v["flops_executed"] / (v["total_ms"] * 1e-3) / 1e12, 1)
         if v["bytes"] > 0:
             kernels[name]["gbs"] = round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1)
+            kernels[name]["algorithmic_bytes_per_launch"] = round(v["bytes"] / max(v["launches"], 1))
     traffic = traffic_records(args.workload)
     hbm = {k: v for k, v in kstats.items() if v["flops"] == 0 and v["bytes"] > 0}
     top_hbm = max(hbm, key=lambda k: hbm[k]["total_ms"]) if hbm else None

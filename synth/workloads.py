@@ -214,11 +214,16 @@ def ns_sweep_shapes(max_x_bytes: int = 64 * 2 ** 30):
     return out
 
 
-def adamw_2p30() -> Workload:
+def adamw_2p30(log2_elems: int = 30) -> Workload:
     """AdamW alone on 2^30 fp32 elements (HBM roofline case)."""
-    return Workload("adamw_2p30_fp32", [], [AdamSpec("flat", (1 << 30,), "f32", "f32",
-                                                     w_std=1.0, g_std=1e-3)],
+    return Workload(f"adamw_2p{log2_elems}_fp32",
+                    [], [AdamSpec("flat", (1 << log2_elems,), "f32", "f32", w_std=1.0, g_std=1e-3)],
                     dict(MUON_HP), dict(ADAM_HP), steps=1)
+
+
+def adamw_2p26() -> Workload:
+    """The same on 2^26 elements (1.8 GB on the device): a profiler-sized case."""
+    return adamw_2p30(26)
 
 
 WORKLOADS = {
@@ -230,6 +235,7 @@ WORKLOADS = {
     "gpt124m_bf16state": gpt124m_bf16_state,
     "moe_mla": moe_mla,
     "moe_mla_e16": moe_mla_e16,
+    "adamw_2p26": adamw_2p26,
     "adamw_2p30": adamw_2p30,
 }
 
