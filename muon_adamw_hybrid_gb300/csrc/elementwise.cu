@@ -734,7 +734,8 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
 //             8 rows each). A group waits for the full barrier, computes the
 //             tile from shared memory (each lane 8 columns: a warp reads 512
 //             consecutive bytes per row, so no bank conflicts), stores the
-//             (apply) and releases the stage (one arrival per warp). The
+//             parameter (apply) and releases the stage (one arrival per
+//             warp). The
 //             statistics write each warp's column partials to one of the
 //             group's four reduction buffers and arrive on its mbarrier; the
 //             cross-warp sum of the group's previous tile is taken after this
@@ -812,8 +813,8 @@ __host__ __device__ constexpr size_t stream_smem_bytes() {
   return StreamLayout<KIND, WB>::kSmem + 128;  // + alignment slack
 }
 
-// Whether the parameter rows of a job are bulk-copied: 16-byte aligned storage
-// whose rows are whole 16-byte groups, of a dtype the layout holds.
+// Whether the parameter of a job is loaded as TMA boxes: 16-byte aligned
+// storage whose rows are whole 16-byte groups, of a dtype the layout holds.
 template <int WB>
 __device__ __forceinline__ bool stream_w_staged(const EwJob& J) {
   const bool vec = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
