@@ -713,14 +713,17 @@ __global__ void __launch_bounds__(kEwThreads, 2) ew_kernel(const __grid_constant
 }
 
 // ---- streaming passes -------------------------------------------------------
-// The plain apply and the Muon+ column statistics read every element once and
-// (apply) write the parameter once, so they are bound by HBM. Each block (one
+// The NorMuon / Muon+ apply (plain, cautious weight decay, or cautious update,
+// which also reads the gradient) and the Muon+ column statistics read every
+// element once and (apply) write the parameter once, so they are bound by
+// HBM. Each block (one
 // per SM) runs one producer warp and sixteen consumer warps over its range of
 // 32 x 256 tiles through a ring of shared-memory stages:
 //   producer  waits for a free stage, writes the stage's descriptor (and, at a
 //             tensor boundary, the job record), then issues one TMA box of U
-//             (from the Newton-Schulz buffer) and one of the parameter, each
-//             32 x 256 with zero fill past the tensor's edges, and cp.async
+//             (from the Newton-Schulz buffer), one of the parameter and, for
+//             the cautious update, one of the gradient, each 32 x 256 with
+//             zero fill past the tensor's edges, and cp.async
 //             copies of the tile's row and column factors. The stage's full
 //             barrier completes when all have landed: 32 plain arrivals (each
 //             lane's own writes), 32 cp.async arrivals and the boxes' bytes.
@@ -788,12 +791,14 @@ struct StreamGroups {
 // WB: parameter bytes per 8 elements (16: bf16, 32: fp32, 0: no parameter).
 template <int KIND, int WB>
 struct StreamLayout {
-  static constexpr bool kApply = KIND == EW_APPLY;
+  static constexpr bool kApply = KIND == EW_APPLY || KIND == EW_APPLY_CU;
+  static constexpr bool kGrad = KIND == EW_APPLY_CU;    // bf16 gradient box
   static constexpr int kURow = kEwTileC * 2;            // 512 B of bf16 U per row
   static constexpr int kWRow = kEwTileC / 8 * WB;       // parameter bytes per row
   static constexpr int kU = 0;
   static constexpr int kW = kU + kEwTileR * kURow;
-  static constexpr int kC = kW + kEwTileR * kWRow;      // column factors (apply)
+  static constexpr int kG = kW + kEwTileR * kWRow;      // gradient (cautious update)
+  static constexpr int kC = kG + (kGrad ? kEwTileR * kURow : 0);  // column factors (apply)
   static constexpr int kR = kC + (kApply ? kEwTileC * 4 : 0);  // row factors
   static constexpr int kD = kR + kEwTileR * 4;          // descriptor: 4 x int32
   static constexpr int kStage = (kD + 16 + 127) / 128 * 128;
@@ -821,13 +826,24 @@ __device__ __forceinline__ bool stream_w_staged(const EwJob& J) {
   return vec && (J.dst_dtype == MH_BF16 ? WB >= 16 : WB >= 32);
 }
 
+// Whether the gradient of a job is loaded as TMA boxes (cautious update): a
+// bf16 gradient in 16-byte aligned storage whose rows are whole 16-byte
+// groups. Others are read directly when the tile is processed.
+__device__ __host__ __forceinline__ bool stream_g_staged(const EwJob& J) {
+  return J.src_vec && J.src_dtype == MH_BF16 && (J.cols % 8) == 0;
+}
+
 __device__ __forceinline__ int64_t job_end_tile(const EwJob& J) {
   return J.tile_begin + J.views * J.tiles_r * J.tiles_c;
 }
 
 // Launch parameters of the streaming passes: the elementwise parameters and,
 // per job, tensor maps of its U view stack and of its parameter (the latter
-// encoded only where stream_w_staged holds).
+// encoded only where stream_w_staged holds). A cautious-update launch carries
+// at most kStreamCuJobs jobs and keeps job j's gradient map (where
+// stream_g_staged holds) in tmU[kStreamCuJobs + j]: three maps per job for 64
+// jobs would exceed the kernel parameter space.
+constexpr int kStreamCuJobs = kMaxJobs / 2;
 struct StreamParams {
   CUtensorMap tmU[kMaxJobs];
   CUtensorMap tmW[kMaxJobs];
@@ -881,7 +897,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const float* rowfac = nullptr;
     const float* colfac = nullptr;
     const int32_t* active = nullptr;
-    uint32_t wbytes = 0;
+    uint32_t wbytes = 0, gbytes = 0;
     int32_t v = 0, tr = 0, tc = 0;
     bool new_view = true;
     const float* rf_view = nullptr;
@@ -916,6 +932,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         wbytes = (WB > 0 && stream_w_staged<WB>(J))
                      ? kEwTileR * kEwTileC * (J.dst_dtype == MH_F32 ? 4u : 2u)
                      : 0u;
+        gbytes = (L::kGrad && stream_g_staged(J)) ? kEwTileR * L::kURow : 0u;
         const TileInfo t = tile_info_in(J, pj, tile);
         v = static_cast<int32_t>(t.v);
         tr = static_cast<int32_t>(t.r0 / kEwTileR);
@@ -924,9 +941,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       }
       if (new_view) {
         if (KIND == EW_COLSQ || p.use_rowfac) rf_view = rowfac + v * rows;
-        if (KIND == EW_APPLY && p.use_colfac) cf_view = colfac + v * cols;
+        if (L::kApply && p.use_colfac) cf_view = colfac + v * cols;
         // The active flag: one dependent load per view.
-        if constexpr (KIND == EW_APPLY) act = active == nullptr || active[v] != 0;
+        if constexpr (L::kApply) act = active == nullptr || active[v] != 0;
         new_view = false;
       }
       const int32_t r0 = tr * kEwTileR, c0 = tc * kEwTileC;
@@ -934,9 +951,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if (lane == 0) {
         *reinterpret_cast<int4*>(st + L::kD) = make_int4(slot, v, r0, c0 | (act ? 0 : (1 << 30)));
         if (act) {
-          mbar_expect_tx(&full[stage], kEwTileR * L::kURow + wbytes);
+          mbar_expect_tx(&full[stage], kEwTileR * L::kURow + wbytes + gbytes);
           tma_load_3d(st + L::kU, &sp.tmU[pj], &full[stage], c0, r0, v);
           if (wbytes) tma_load_3d(st + L::kW, &sp.tmW[pj], &full[stage], c0, r0, v);
+          if (gbytes) tma_load_3d(st + L::kG, &sp.tmU[kStreamCuJobs + pj], &full[stage], c0, r0, v);
         }
       }
       if (act) {
@@ -944,7 +962,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           const bool row_ok = r0 + lane < rows;
           cp_async4(st + L::kR + lane * 4, row_ok ? rf_view + r0 + lane : rowfac, row_ok);
         }
-        if constexpr (KIND == EW_APPLY) {
+        if constexpr (L::kApply) {
           if (p.use_colfac) {
             const int64_t col = c0 + lane * 8;
             const float* cf = cf_view + col;
@@ -1108,6 +1126,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           for (int q = 0; q < 8; ++q) hs[q] = lrs;
         }
         const bool cautious_wd = p.cautious == MH_CAUTIOUS_WD;
+        const bool gst = L::kGrad && stream_g_staged(J);
+        const bool svec = J.src_vec && (J.src_dtype == MH_F32 || (J.cols % 8) == 0);
+        const float lrwd = J.lr * J.wd;
         const int64_t view_elem0 = t.v * J.rows * J.cols;
 #pragma unroll
         for (int r = 0; r < kR; ++r) {
@@ -1135,7 +1156,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             load8(J.dst, J.dst_dtype, off, nvalid, dvec, w);
           }
           const float f = fr[r];
-          if (cautious_wd) {
+          if constexpr (L::kGrad) {
+            // Cautious update: the whole step delta = lr wd W + lr s U f h
+            // applies only where it agrees in sign with the gradient.
+            float g[8];
+            if (gst) {
+              const uint4 gr = *reinterpret_cast<const uint4*>(
+                  st + L::kG + (gw * kR + r) * L::kURow + lane * 16);
+              const uint32_t g4[4] = {gr.x, gr.y, gr.z, gr.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                g[2 * q] = __uint_as_float(g4[q] << 16);
+                g[2 * q + 1] = __uint_as_float(g4[q] & 0xFFFF0000u);
+              }
+            } else {
+              load8(J.src, J.src_dtype, off, nvalid, svec, g);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float delta = fmaf(lrwd, w[q], u[r][q] * f * hs[q]);
+              if (delta * g[q] > 0.0f) w[q] = w[q] - delta;
+            }
+          } else if (cautious_wd) {
             // Weight decay only where the update and the weight agree in sign
             // (lr s f h >= 0, so ga has the sign of the update direction).
 #pragma unroll
@@ -1406,67 +1448,100 @@ cudaError_t launch_elementwise(EwKind kind, const EwParams& p, int num_sms, cuda
     case EW_APPLY_CU: fn = reinterpret_cast<const void*>(ew_kernel<EW_APPLY_CU>); break;
     case EW_COPYOUT: fn = reinterpret_cast<const void*>(ew_kernel<EW_COPYOUT>); break;
   }
-  // The plain apply (no cautious-update mask) and the Muon+ column statistics
-  // take the streaming kernel when the launch has a status word for its
-  // bounded waits: one block per SM, the stage layout sized for the
-  // parameter dtypes of the launch.
-  if ((kind == EW_APPLY || kind == EW_COLSQ) && p.status != nullptr) {
+  // The register-staged kernels, on the whole launch or on a part of it.
+  auto launch_staged = [&](const EwParams& q) -> cudaError_t {
+    const int per_sm = blocks_per_sm(kind, fn);
+    const int64_t want = static_cast<int64_t>(num_sms) * per_sm;
+    const int grid = static_cast<int>(q.total_tiles < want ? q.total_tiles : want);
+    if (grid <= 0) return cudaSuccess;
+    switch (kind) {
+      case EW_PROLOGUE: prologue_kernel<<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_PROLOGUE_FLAT: prologue_flat_kernel<false><<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_PROLOGUE_FLAT_B16: prologue_flat_kernel<true><<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_APPLY_CU: ew_kernel<EW_APPLY_CU><<<grid, kEwThreads, 0, s>>>(q); break;
+      case EW_COPYOUT: ew_kernel<EW_COPYOUT><<<grid, kEwThreads, 0, s>>>(q); break;
+    }
+    return cudaGetLastError();
+  };
+  // The apply (every cautious form) and the Muon+ column statistics take the
+  // streaming kernel when the launch has a status word for its bounded waits:
+  // one block per SM, the stage layout sized for the parameter dtypes of the
+  // launch. The cautious update, with a gradient map per job as well, runs in
+  // parts of at most kStreamCuJobs jobs.
+  if ((kind == EW_APPLY || kind == EW_APPLY_CU || kind == EW_COLSQ) && p.status != nullptr) {
     bool any_f32 = false;
     for (int j = 0; j < p.njobs; ++j) any_f32 = any_f32 || p.jobs[j].dst_dtype == MH_F32;
-    const void* ks[3] = {reinterpret_cast<const void*>(ew_stream_kernel<EW_COLSQ, 0>),
+    const void* ks[5] = {reinterpret_cast<const void*>(ew_stream_kernel<EW_COLSQ, 0>),
                          reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY, 16>),
-                         reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY, 32>)};
-    const size_t sz[3] = {stream_smem_bytes<EW_COLSQ, 0>(), stream_smem_bytes<EW_APPLY, 16>(),
-                          stream_smem_bytes<EW_APPLY, 32>()};
-    const int which = kind == EW_COLSQ ? 0 : (any_f32 ? 2 : 1);
+                         reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY, 32>),
+                         reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY_CU, 16>),
+                         reinterpret_cast<const void*>(ew_stream_kernel<EW_APPLY_CU, 32>)};
+    const size_t sz[5] = {stream_smem_bytes<EW_COLSQ, 0>(), stream_smem_bytes<EW_APPLY, 16>(),
+                          stream_smem_bytes<EW_APPLY, 32>(), stream_smem_bytes<EW_APPLY_CU, 16>(),
+                          stream_smem_bytes<EW_APPLY_CU, 32>()};
+    const bool cu = kind == EW_APPLY_CU;
+    const int which = kind == EW_COLSQ ? 0 : (cu ? 3 : 1) + (any_f32 ? 1 : 0);
     static thread_local int configured = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured != dev) {
-      for (int k = 0; k < 3; ++k) {
+      for (int k = 0; k < 5; ++k) {
         e = cudaFuncSetAttribute(ks[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(sz[k]));
         if (e != cudaSuccess) return e;
       }
       configured = dev;
     }
-    // Per job: the U view stack (row pitch ldx, zero fill past cols and
-    // rows) and, where the apply stages it, the parameter.
     static thread_local StreamParams sp;
-    bool maps_ok = true;
-    for (int j = 0; j < p.njobs && maps_ok; ++j) {
-      const EwJob& J = p.jobs[j];
-      maps_ok = cached_stream_map(&sp.tmU[j], J.xf, false, J.cols, J.rows, J.views, J.ldx);
-      const bool wst = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0) &&
-                       (J.dst_dtype == MH_BF16 || any_f32);
-      if (maps_ok && kind == EW_APPLY && wst)
-        maps_ok = cached_stream_map(&sp.tmW[j], J.dst, J.dst_dtype == MH_F32, J.cols, J.rows,
-                                    J.views, J.cols);
-    }
-    if (maps_ok) {
+    const int per = cu ? kStreamCuJobs : kMaxJobs;
+    for (int j0 = 0; j0 < p.njobs; j0 += per) {
+      const int j1 = p.njobs - j0 < per ? p.njobs : j0 + per;
+      // This part's jobs, their tile indices counted from its first tile.
       sp.ew = p;
-      const int grid = static_cast<int>(p.total_tiles < num_sms ? p.total_tiles : num_sms);
+      if (j0 > 0 || j1 < p.njobs) {
+        const int64_t base = p.jobs[j0].tile_begin;
+        const int64_t end = j1 < p.njobs ? p.jobs[j1].tile_begin : p.total_tiles;
+        for (int k = 0; k < j1 - j0; ++k) {
+          sp.ew.jobs[k] = p.jobs[j0 + k];
+          sp.ew.jobs[k].tile_begin -= base;
+        }
+        sp.ew.njobs = j1 - j0;
+        sp.ew.total_tiles = end - base;
+      }
+      const EwParams& q = sp.ew;
+      if (q.total_tiles <= 0) continue;
+      // Per job: the U view stack (row pitch ldx, zero fill past cols and
+      // rows) and, where the apply stages them, the parameter and the
+      // gradient.
+      bool maps_ok = true;
+      for (int k = 0; k < q.njobs && maps_ok; ++k) {
+        const EwJob& J = q.jobs[k];
+        maps_ok = cached_stream_map(&sp.tmU[k], J.xf, false, J.cols, J.rows, J.views, J.ldx);
+        const bool wst = J.dst_vec && (J.dst_dtype == MH_F32 || (J.cols % 8) == 0);
+        if (maps_ok && kind != EW_COLSQ && wst)
+          maps_ok = cached_stream_map(&sp.tmW[k], J.dst, J.dst_dtype == MH_F32, J.cols, J.rows,
+                                      J.views, J.cols);
+        if (maps_ok && cu && stream_g_staged(J))
+          maps_ok = cached_stream_map(&sp.tmU[kStreamCuJobs + k], J.src, false, J.cols, J.rows,
+                                      J.views, J.cols);
+      }
+      if (!maps_ok) {
+        if ((e = launch_staged(q)) != cudaSuccess) return e;
+        continue;
+      }
+      const int grid = static_cast<int>(q.total_tiles < num_sms ? q.total_tiles : num_sms);
       void* args[] = {&sp};
       e = cudaLaunchKernel(ks[which], dim3(grid), dim3(kStreamThreads), args, sz[which], s);
       if (e != cudaSuccess) return e;
-      return cudaGetLastError();
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    return cudaSuccess;
   }
-  const int per_sm = blocks_per_sm(kind, fn);
-  const int64_t want = static_cast<int64_t>(num_sms) * per_sm;
-  const int grid = static_cast<int>(p.total_tiles < want ? p.total_tiles : want);
-  switch (kind) {
-    case EW_PROLOGUE: prologue_kernel<<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_PROLOGUE_FLAT: prologue_flat_kernel<false><<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_PROLOGUE_FLAT_B16: prologue_flat_kernel<true><<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_ROWSQ: ew_kernel<EW_ROWSQ><<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_COLSQ: ew_kernel<EW_COLSQ><<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_APPLY: ew_kernel<EW_APPLY><<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_APPLY_CU: ew_kernel<EW_APPLY_CU><<<grid, kEwThreads, 0, s>>>(p); break;
-    case EW_COPYOUT: ew_kernel<EW_COPYOUT><<<grid, kEwThreads, 0, s>>>(p); break;
-  }
-  return cudaGetLastError();
+  return launch_staged(p);
 }
 
 cudaError_t launch_view_active(const ActiveParams& p, int num_sms, cudaStream_t s) {

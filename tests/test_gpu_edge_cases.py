@@ -6,11 +6,14 @@
   of the GEMM epilogue's row sums.
 * ns_steps = 1: the first iteration's normalisation and the last apply stage
   are the same launch (fused update, or row sums under NorMuon).
-* The cautious-update mask under NorMuon / Muon+ (the separate apply pass's
-  own instantiation, which reads the gradient).
+* The cautious-update mask under NorMuon / Muon+ (the apply pass's own
+  instantiation, which reads the gradient: staged as a TMA box when it is
+  bf16 with whole 16-byte rows, read directly otherwise).
 * bf16 and fp32 parameters in one NorMuon / Muon+ apply launch: the streaming
   pass's fp32 stage layout holding bf16 tiles, and a bf16 parameter whose
   rows are not whole 16-byte groups (read directly instead of staged).
+* Seventy tensors: several elementwise batches, and several parts of a
+  streaming cautious-update launch.
 * A call mixing empty tensors (zero rows, zero views' worth of elements) with
   ordinary ones: the empty ones are skipped, the rest match the oracle.
 """
@@ -101,6 +104,24 @@ MIXED = [W.MuonSpec("m1", 1, 256, 512, "bf16", "f32", w_std=1.0, g_std=1.0),
                                    dict(normuon=True, muon_plus=True, cautious=1)])
 def test_mixed_dtypes_with_cautious_masks(flags):
     wl = _wl(MIXED, **flags)
+    run = DeviceRun(wl)
+    run.step()
+    run.status_ok()
+    _check(wl, run)
+
+
+# More tensors than one elementwise batch (64) and than one part of a
+# streaming cautious-update launch (32): the parts count their tiles from their
+# own first tile. Mixed shapes, views and parameter dtypes, bf16 gradients.
+MANY = [W.MuonSpec(f"t{i}", 1 + i % 3, 64 + 32 * (i % 5), 256 + 64 * (i % 4),
+                   "bf16" if i % 2 else "f32", "bf16",
+                   w_std=0.02 if i % 2 else 1.0, g_std=1.0) for i in range(70)]
+
+
+@pytest.mark.parametrize("flags", [dict(normuon=True, muon_plus=True, cautious=2),
+                                   dict(normuon=True, cautious=1)])
+def test_many_tensors_span_several_launches(flags):
+    wl = _wl(MANY, **flags)
     run = DeviceRun(wl)
     run.step()
     run.status_ok()
