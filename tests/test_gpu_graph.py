@@ -4,7 +4,9 @@ With gradient control on, AdamW takes its step count from the device
 (mh_adamw_step_ctl), so nothing that changes from step to step is baked into
 the graph. Three replays of a captured step on the 124M set give bit for bit
 the parameters and state of three eager steps. This also holds with the Muon
-step in its two phases and a parameter fence recorded inside the capture.
+step in its two phases and a parameter fence recorded inside the capture, and
+with NorMuon, Muon+ and the cautious-update mask on (the streaming apply and
+column-statistics launches, whose tensor maps are encoded at capture time).
 """
 import pytest
 
@@ -15,13 +17,16 @@ pytestmark = pytest.mark.gpu
 
 
 def _state(dw):
-    return dw.mW + dw.mB + dw.aW + dw.am + dw.av
+    return dw.mW + dw.mB + dw.aW + dw.am + dw.av + [s for s in dw.sm if s is not None]
 
 
-@pytest.mark.parametrize("split", [False, True])
-def test_graph_replay_equals_eager_steps(split):
+@pytest.mark.parametrize("split,variants", [(False, {}), (True, {}),
+                                            (False, dict(normuon=True, muon_plus=True,
+                                                         cautious=2))])
+def test_graph_replay_equals_eager_steps(split, variants):
     import torch
     wl = W.gpt124m()
+    wl.muon_hp = dict(wl.muon_hp, **variants)
     dev = torch.device("cuda", 0)
     eager = bench.DeviceWorkload(wl, dev, max_grad_norm=1.0)
     graphed = bench.DeviceWorkload(wl, dev, max_grad_norm=1.0)
