@@ -200,6 +200,16 @@ def moe_mla_e16() -> Workload:
     return moe_mla(16)
 
 
+def moe_mla_e16_cu() -> Workload:
+    """The 16-expert layer with the cautious-update mask (Speedtronic
+    "Cautious updates") in place of the cautious weight decay: the apply pass
+    then reads the gradient too."""
+    wl = moe_mla(16)
+    wl.name = "moe16_mla_cautious_update"
+    wl.muon_hp = dict(wl.muon_hp, cautious=2)
+    return wl
+
+
 def ns_sweep_shapes(max_x_bytes: int = 64 * 2 ** 30):
     """Newton-Schulz-only sweep: square n x n, wide n x 4n and tall 4n x n for
     n in {512 .. 8192}, batch counts 1..256 capped at `max_x_bytes` of bf16
@@ -235,6 +245,7 @@ WORKLOADS = {
     "gpt124m_bf16state": gpt124m_bf16_state,
     "moe_mla": moe_mla,
     "moe_mla_e16": moe_mla_e16,
+    "moe_mla_e16_cu": moe_mla_e16_cu,
     "adamw_2p26": adamw_2p26,
     "adamw_2p30": adamw_2p30,
 }
