@@ -129,3 +129,34 @@ def test_ratio_record_applies_to_named_workloads_and_scales(tmp_path, monkeypatc
     assert bench.traffic_for(rec, "ns_gemm", 8e9) == 1e10
     assert bench.traffic_for(rec, "adamw", 8e9) is None
     assert bench.traffic_records("other") == {}
+
+
+def test_committed_traffic_records_are_well_formed():
+    """Every traffic-record line under profiles/ names a kernel family the
+    benchmark hashes, a ratio or a byte count in a plausible range, a
+    16-hex-digit source digest, and only workloads the benchmark can run
+    (a registered set or an NS-only point), so a typo cannot silently leave a
+    configuration without its record."""
+    import glob
+    import os
+    import re
+    from synth import workloads as W
+    paths = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "dram_*.md")))
+    assert paths
+    seen = 0
+    for path in paths:
+        for line in open(path):
+            if not line.startswith("traffic-record:"):
+                continue
+            seen += 1
+            kv = dict(tok.split("=", 1) for tok in line.split()[1:])
+            assert kv["kernel"] in bench.KERNEL_SOURCES, (path, line)
+            assert re.fullmatch(r"[0-9a-f]{16}", kv["sources"]), (path, line)
+            if "ratio" in kv:
+                assert 0.5 < float(kv["ratio"]) < 3.0, (path, line)
+            else:
+                assert float(kv["bytes_per_launch"]) > 0, (path, line)
+            for w in kv["applies_to"].split(","):
+                assert w in W.WORKLOADS or re.fullmatch(r"ns_(1:1|1:4|4:1)_n\d+_batch\d+", w), \
+                    (path, w)
+    assert seen >= 10
